@@ -1,0 +1,228 @@
+/*
+ * memq_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously correct CPU oracle of the m <= 8 quantized decode chain, written in
+ * f64 from the definitions on the source pages of memra-engine 0.125.0:
+ *   - q8_fuse_gate.rs, module doc and `run_shape`: the fused RMSNorm -> q8_1 producer
+ *     (z = x * rsqrt(mean(x^2) + eps) * w, then per 32-element block d = amax/127 and
+ *     qs = round(z/d), emitted as f32 z, int8 qs and an f32 per-block scale d);
+ *   - gemv_e4m3_bench.rs, module doc ("THE COMPARISON", "THE BLOCK-128 ARM") and the
+ *     generators `synth_e4m3`, `synth_blk_grid`, `synth_q8_0`: the m=1..8 GEMV of a q8_1
+ *     activation against three weight containers (raw E4M3 + one per-tensor scale, E4M3 + an
+ *     f32 [ceil(out_f/128), ceil(in_f/128)] block-128 scale grid, ggml block_q8_0).
+ *
+ * Only the tests, the package's smoke check and the bench's CPU-baseline leg may load this
+ * library.  It shares no code, header or table with the CUDA path and includes nothing from it.
+ * Every sum here is a straight loop in the definition's order; there is no blocking, fusion or
+ * reordering.  No fast-math: build with plain -O2.
+ *
+ * Parity pins (what each function is checked against, by the CPU tests):
+ *   memq_oracle_e4m3     closed-form spot values of the OCP E4M3 format + all 256 codes vs the
+ *                        float8_e4m3fn decode of a tensor library (NaN exactly at 0x7F/0xFF)
+ *   memq_oracle_f16      all 65536 codes vs numpy.float16
+ *   memq_oracle_rmsnorm  closed forms (constant rows) + a library rms_norm in f64
+ *   memq_oracle_quantize closed forms, rounding-tie cases, invariants |qs|<=127, amax -> +-127,
+ *                        |z - d*qs| <= d/2
+ *   memq_oracle_gemv_*   library matmul of independently dequantized operands on small
+ *                        shapes, one-hot activations, sign-flip / zero / constant-grid
+ *                        identities, and the exact cross-container identity
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+/* ---------------------------------------------------------------------------------------------
+ * Format decoders.
+ * ------------------------------------------------------------------------------------------- */
+
+/* FP8 E4M3 (OCP "E4M3FN"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities;
+ * exponent 15 with mantissa 7 is NaN -- gemv_e4m3_bench.rs, `synth_e4m3` doc: "Magnitude 0x7F is
+ * the e4m3 NaN code". */
+double memq_oracle_e4m3(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int expo = (b >> 3) & 15;
+    int mant = b & 7;
+    double mag;
+    if (expo == 15 && mant == 7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)mant, -9);                 /* subnormal: mant/8 * 2^(1-7) */
+    else
+        mag = ldexp(1.0 + (double)mant / 8.0, expo - 7);
+    return sign ? -mag : mag;
+}
+
+/* IEEE-754 binary16, the block_q8_0 scale (gemv_e4m3_bench.rs, `synth_q8_0`: "d = f16 0x1400 =
+ * 2^-10"; two little-endian bytes at the start of each 34-byte block). */
+double memq_oracle_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 31;
+    int frac = h & 1023;
+    double mag;
+    if (expo == 31)
+        mag = frac ? NAN : INFINITY;
+    else if (expo == 0)
+        mag = ldexp((double)frac, -24);
+    else
+        mag = ldexp(1.0 + (double)frac / 1024.0, expo - 15);
+    return sign ? -mag : mag;
+}
+
+void memq_oracle_e4m3_table(double *out256)
+{
+    for (int b = 0; b < 256; ++b)
+        out256[b] = memq_oracle_e4m3((uint8_t)b);
+}
+
+void memq_oracle_f16_decode(const uint16_t *h, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = memq_oracle_f16(h[i]);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Stage 1: RMSNorm, then q8_1 quantization (q8_fuse_gate.rs, module doc: `rms_norm` then
+ * `quantize_q8_1`, fused as `rms_norm_zq8_f32`).
+ * ------------------------------------------------------------------------------------------- */
+
+/* z[r][i] = x[r][i] * r_row * w[i],  r_row = 1 / sqrt(sum_i x[r][i]^2 / ncols + eps).
+ * x: [rows][ncols] f32, w: [ncols] f32, z: [rows][ncols] f64.  eps arrives as the f32 the
+ * callers use (1e-6f in `run_shape`) and is promoted to f64. */
+void memq_oracle_rmsnorm(const float *x, const float *w, int64_t rows, int64_t ncols, float eps,
+                         double *z)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * ncols;
+        double ss = 0.0;
+        for (int64_t i = 0; i < ncols; ++i)
+            ss += (double)xr[i] * (double)xr[i];
+        double rr = 1.0 / sqrt(ss / (double)ncols + (double)eps);
+        for (int64_t i = 0; i < ncols; ++i)
+            z[r * ncols + i] = (double)xr[i] * rr * (double)w[i];
+    }
+}
+
+/* Per 32-element block of each row: amax = max |z|, d = amax / 127 stored as an f32 (the q8_1
+ * scale is an f32 per block), qs = round(z / d) with ties away from zero, and qs = 0 when d = 0
+ * (the `id = 1/d` branch named in q8_fuse_gate.rs, `Xorshift64::next_f32` doc).
+ * z: [rows][ncols] f64 -> d: [rows][ncols/32] f32, qs: [rows][ncols] int8,
+ * ratio: [rows][ncols] f64 = z / d (the exact quotient whose rounding gives qs), may be NULL. */
+void memq_oracle_quantize_q8_1(const double *z, int64_t rows, int64_t ncols, float *d,
+                               int8_t *qs, double *ratio)
+{
+    int64_t nb = ncols / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const double *zb = z + r * ncols + b * 32;
+            double amax = 0.0;
+            for (int k = 0; k < 32; ++k)
+                if (fabs(zb[k]) > amax)
+                    amax = fabs(zb[k]);
+            float dd = (float)(amax / 127.0);
+            d[r * nb + b] = dd;
+            for (int k = 0; k < 32; ++k) {
+                int64_t i = r * ncols + b * 32 + k;
+                double t = (dd != 0.0f) ? zb[k] / (double)dd : 0.0;
+                qs[i] = (int8_t)round(t);
+                if (ratio)
+                    ratio[i] = t;
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Stage 2: y[j][r] = sum_i W(r, i) * X(j, i), with X(j, i) = d[j][i/32] * qs[j][i] the
+ * dequantized q8_1 activation row j (j < m) and W the dequantized weight
+ * (gemv_e4m3_bench.rs, "THE COMPARISON" and "THE BLOCK-128 ARM").
+ *
+ * Every GEMV takes an optional list of output rows (row_idx, nrows; NULL = all out_f rows in
+ * order) so that full-size problems can be checked on sampled rows.  Outputs are
+ * y[j][t] and sabs[j][t] = sum_i |W(r,i) X(j,i)| for t < nrows, r = row_idx[t].
+ * ------------------------------------------------------------------------------------------- */
+
+static double act(const int8_t *qs, const float *d, int64_t in_f, int64_t j, int64_t i)
+{
+    return (double)d[j * (in_f / 32) + i / 32] * (double)qs[j * in_f + i];
+}
+
+/* Raw E4M3 plane [out_f][in_f] (row stride in_f, 1 byte per weight), one per-tensor scale:
+ * W(r, i) = scale * e4m3(w[r][i]). */
+void memq_oracle_gemv_e4m3(const uint8_t *w, float scale, const int8_t *qs, const float *d,
+                           int64_t out_f, int64_t in_f, int m, const int64_t *row_idx,
+                           int64_t nrows, double *y, double *sabs)
+{
+    double tab[256];
+    memq_oracle_e4m3_table(tab);
+    if (!row_idx)
+        nrows = out_f;
+    for (int64_t t = 0; t < nrows; ++t) {
+        int64_t r = row_idx ? row_idx[t] : t;
+        for (int j = 0; j < m; ++j) {
+            double acc = 0.0, s = 0.0;
+            for (int64_t i = 0; i < in_f; ++i) {
+                double p = (double)scale * tab[w[r * in_f + i]] * act(qs, d, in_f, j, i);
+                acc += p;
+                s += fabs(p);
+            }
+            y[j * nrows + t] = acc;
+            sabs[j * nrows + t] = s;
+        }
+    }
+}
+
+/* E4M3 plane plus the block-128 scale grid, f32 [ceil(out_f/128)][ceil(in_f/128)] row-major
+ * (the `F8BlockGrid` order): W(r, i) = grid[r/128][i/128] * e4m3(w[r][i]); a partial edge tile
+ * keeps its own grid entry. */
+void memq_oracle_gemv_e4m3_blk128(const uint8_t *w, const float *grid, const int8_t *qs,
+                                  const float *d, int64_t out_f, int64_t in_f, int m,
+                                  const int64_t *row_idx, int64_t nrows, double *y, double *sabs)
+{
+    double tab[256];
+    int64_t gcols = (in_f + 127) / 128;
+    memq_oracle_e4m3_table(tab);
+    if (!row_idx)
+        nrows = out_f;
+    for (int64_t t = 0; t < nrows; ++t) {
+        int64_t r = row_idx ? row_idx[t] : t;
+        for (int j = 0; j < m; ++j) {
+            double acc = 0.0, s = 0.0;
+            for (int64_t i = 0; i < in_f; ++i) {
+                double g = (double)grid[(r / 128) * gcols + i / 128];
+                double p = g * tab[w[r * in_f + i]] * act(qs, d, in_f, j, i);
+                acc += p;
+                s += fabs(p);
+            }
+            y[j * nrows + t] = acc;
+            sabs[j * nrows + t] = s;
+        }
+    }
+}
+
+/* ggml block_q8_0 rows: in_f/32 blocks of 34 bytes per row, each an f16 scale (little-endian,
+ * bytes 0-1) followed by 32 int8 weights: W(r, i) = f16(block.d) * block.qs[i % 32]. */
+void memq_oracle_gemv_q8_0(const uint8_t *w, const int8_t *qs, const float *d, int64_t out_f,
+                           int64_t in_f, int m, const int64_t *row_idx, int64_t nrows, double *y,
+                           double *sabs)
+{
+    int64_t nb = in_f / 32;
+    if (!row_idx)
+        nrows = out_f;
+    for (int64_t t = 0; t < nrows; ++t) {
+        int64_t r = row_idx ? row_idx[t] : t;
+        for (int j = 0; j < m; ++j) {
+            double acc = 0.0, s = 0.0;
+            for (int64_t i = 0; i < in_f; ++i) {
+                const uint8_t *blk = w + (r * nb + i / 32) * 34;
+                double dw = memq_oracle_f16((uint16_t)(blk[0] | (blk[1] << 8)));
+                double p = dw * (double)(int8_t)blk[2 + i % 32] * act(qs, d, in_f, j, i);
+                acc += p;
+                s += fabs(p);
+            }
+            y[j * nrows + t] = acc;
+            sabs[j * nrows + t] = s;
+        }
+    }
+}
