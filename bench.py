@@ -1,0 +1,558 @@
+"""DRAM-cold benchmark of the quantized decode chain on GB300.
+
+A step is one pass of the whole hot path over one synthetic decode token: the fused
+RMSNorm -> q8_1 producer on the token's activation row, then the GEMV against that q8_1
+activation, reading the next of several rotated weight copies so that no launch finds its
+weights in L2.  The default workload is the Q8_0 4096 x 4096 m = 1 GEMV with 16 rotated copies
+(285 MB, well past the 129 MB L2).
+
+Printed (rank 0, one JSON line):
+  value       whole-step throughput: algorithmic bytes of the step (GEMV weights + scales +
+              activation, plus the producer's x, w, qs, d) / device time per step, inputs
+              resident in HBM; K steps replayed from CUDA graphs, timed with CUDA events.
+  roofline    the GEMV alone: algorithmic bytes per launch / mean launch duration (CUDA events
+              around each launch, DRAM-cold), against the measured HBM copy bandwidth.
+  e2e         the same metric through the public API with host buffers: per step the
+              activation row is copied host->device from pinned memory, the chain runs, the
+              result y is copied device->host and the host waits for it.
+  cpu_baseline  the f64 oracle on the host cores on a bounded sample of the same workload.
+With --impl reference the oracle itself is the timed arm (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "m=1 quantized GEMV achieved HBM GB/s (DRAM-cold) and % of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+
+# Workloads by name: (container, out_f, in_f, m, rotated copies)
+WORKLOADS = {
+    "q8_0_4096x4096_m1": ("q8_0", 4096, 4096, 1, 16),
+    "e4m3_1024x4096_m1": ("e4m3", 1024, 4096, 1, 64),
+    "blk128_17408x5120_m1": ("blk", 17408, 5120, 1, 4),
+    "e4m3_17408x5120_m1": ("e4m3", 17408, 5120, 1, 4),
+    "q8_0_17408x5120_m1": ("q8_0", 17408, 5120, 1, 4),
+}
+DEFAULT_WORKLOAD = "q8_0_4096x4096_m1"
+
+
+# ------------------------------------------------------------------------------------------
+# Byte accounting (algorithmic bytes, outputs excluded for the GEMV per the metric)
+# ------------------------------------------------------------------------------------------
+
+def gemv_bytes(kind: str, out_f: int, in_f: int, m: int) -> int:
+    act = m * (in_f + in_f // 32 * 4)
+    if kind == "q8_0":
+        return out_f * (in_f // 32) * 34 + act
+    if kind == "blk":
+        return out_f * in_f + 4 * (-(-out_f // 128)) * (-(-in_f // 128)) + act
+    return out_f * in_f + 4 + act
+
+
+def producer_bytes(rows: int, ncols: int) -> int:
+    return rows * ncols * 4 + ncols * 4 + rows * ncols + rows * (ncols // 32) * 4
+
+
+# ------------------------------------------------------------------------------------------
+# Distributed plumbing (replicas only: no data-path collective)
+# ------------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(elapsed_s: float, units: float, group=None):
+    """Max elapsed over ranks and the sum of units over ranks (whole-job throughput)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="memq_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [c.strip() for c in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                    power.append(float(p[3]))
+                except ValueError:
+                    continue
+                for name, flag in zip(names, p[5:9]):
+                    if flag.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "samples": len(sm), "power_w_max": float(max(power)) if power else None,
+                "reasons": sorted(reasons)}
+
+
+def measured_peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = json.load(f).get("hbm_gbs")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------------------------
+# Workload
+# ------------------------------------------------------------------------------------------
+
+class DecodeStep:
+    """Producer + GEMV with rotated weight copies, all buffers preallocated on the device."""
+
+    def __init__(self, kind, out_f, in_f, m, copies, device, seed=0x51ED0002):
+        import torch
+        import quantized_decode_memq_gb300 as memq
+        from quantized_decode_memq_gb300 import synth
+        self.memq = memq
+        self.kind, self.out_f, self.in_f, self.m, self.copies = kind, out_f, in_f, m, copies
+        self.device = device
+        x, wn = synth.activation_rows(in_f, m)
+        self.x_host = x
+        self.x = torch.from_numpy(x).to(device)
+        self.wn = torch.from_numpy(wn).to(device)
+        self.qs = torch.empty((m, in_f), dtype=torch.int8, device=device)
+        self.d = torch.empty((m, in_f // 32), dtype=torch.float32, device=device)
+        self.y = torch.empty((m, out_f), dtype=torch.float32, device=device)
+        if kind == "q8_0":
+            wh = synth.q8_0_bytes(seed, out_f, in_f)
+            aux = None
+        else:
+            wh = synth.e4m3_bytes(seed + 1, out_f, in_f)
+            if kind == "blk":
+                aux = synth.grid_log2_uniform(seed + 2, out_f, in_f)
+            else:
+                aux = np.array([2.0 ** -4], np.float32)
+        w0 = torch.from_numpy(wh).to(device)
+        self.w = [w0] + [w0.clone() for _ in range(copies - 1)]
+        self.aux = None if aux is None else [torch.from_numpy(aux).to(device) for _ in range(copies)]
+        torch.cuda.synchronize()
+        self.gemv_bytes = gemv_bytes(kind, out_f, in_f, m)
+        self.step_bytes = self.gemv_bytes + producer_bytes(m, in_f)
+
+    def producer(self):
+        self.memq.memq_rmsnorm_q8_1(self.x, self.wn, 1e-6, qs=self.qs, d=self.d, want_z=False)
+
+    def gemv(self, i):
+        c = i % self.copies
+        if self.kind == "q8_0":
+            self.memq.memq_gemv_q8_0(self.w[c], self.qs, self.d, y=self.y)
+        elif self.kind == "blk":
+            self.memq.memq_gemv_e4m3_blk128(self.w[c], self.aux[c], self.qs, self.d, y=self.y)
+        else:
+            self.memq.memq_gemv_e4m3(self.w[c], self.aux[c], self.qs, self.d, y=self.y)
+
+    def step(self, i):
+        self.producer()
+        self.gemv(i)
+
+
+def capture(fn, n, stream):
+    """A CUDA graph of fn(0..n-1) launched on `stream`."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from quantized_decode_memq_gb300 import build
+    build.build()
+    kind, out_f, in_f, m, copies = WORKLOADS[args.workload]
+    wl = DecodeStep(kind, out_f, in_f, m, copies, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # Eager warm-up of every launch shape (sets kernel attributes outside any capture).
+    with torch.cuda.stream(stream):
+        for i in range(copies):
+            wl.step(i)
+    stream.synchronize()
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        g_full = capture(wl.step, copies, stream)
+        rem = K % copies
+        g_rem = capture(wl.step, rem, stream) if rem else None
+    reps = K // copies
+
+    # Warm-up: W steps (rounded up to whole graphs).
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-W // copies))):
+            g_full.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    t_max, units = aggregate(elapsed, float(K * wl.step_bytes))
+    value = units / t_max / 1e9
+    ms_per_step = t_max / K * 1e3
+
+    # Roofline: the GEMV alone, one launch at a time, DRAM-cold (rotated copies).
+    gemv_s = time_gemv_launches(wl, stream, n=max(64, 4 * copies))
+    achieved = wl.gemv_bytes / gemv_s / 1e9
+    peak, peak_kind = measured_peak_hbm()
+    # Back-to-back GEMVs (graph of rotated launches, programmatic overlap between them).
+    b2b_s = time_gemv_back_to_back(wl, stream, n=16 * copies)
+
+    e2e = time_e2e(wl, stream, steps=min(K, args.e2e_steps))
+    e2e_t, e2e_units = aggregate(e2e["elapsed"], float(e2e["steps"] * wl.step_bytes))
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8" if kind == "q8_0" else "fp8",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: fused RMSNorm->q8_1 (1x{in_f} f32) then "
+                        f"{kind} GEMV out_f={out_f} in_f={in_f} m={m}",
+            "weight_copies": copies,
+            "rotation_bytes": copies * (wl.gemv_bytes - m * (in_f + in_f // 8)),
+            "l2": "inputs larger than L2: each step reads the next of the rotated weight "
+                  "copies (DRAM-cold)",
+            "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+            "step_bytes": wl.step_bytes,
+            "timing": "K steps replayed from CUDA graphs, CUDA events on the launch stream",
+        },
+        "pct_of_peak": round(100.0 * value / peak, 2),
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": args.traffic,
+            "kernel": f"gemv_stream_kernel<{kind}, m={m}>",
+            "bytes_per_launch": wl.gemv_bytes,
+            "launch_us": round(gemv_s * 1e6, 3),
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                           else "fallback 6.8 TB/s",
+            "back_to_back_us": round(b2b_s * 1e6, 3),
+            "back_to_back_gbs": round(wl.gemv_bytes / b2b_s / 1e9, 2),
+        },
+        "e2e": {
+            "value": round(e2e_units / e2e_t / 1e9, 3),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": e2e["h2d"],
+            "d2h_bytes_per_step": e2e["d2h"],
+            "steps": e2e["steps"],
+            "us_per_step": round(e2e_t / e2e["steps"] * 1e6, 2),
+        },
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def time_gemv_launches(wl, stream, n):
+    """Mean duration of n individually bracketed GEMV launches (rotated copies)."""
+    import torch
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
+
+        def body(i):
+            evs[i][0].record(stream)
+            wl.gemv(i)
+            evs[i][1].record(stream)
+        with torch.cuda.stream(stream):
+            g = capture(body, n, stream)
+            for _ in range(3):
+                g.replay()
+        stream.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+    except TypeError:
+        # No event-record graph nodes in this torch: queue each launch behind a GPU-side spin so
+        # the CPU enqueue time never lands between the two events.
+        res = []
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                torch.cuda._sleep(200000)
+                a.record(stream)
+                wl.gemv(i)
+                b.record(stream)
+                stream.synchronize()
+                res.append(a.elapsed_time(b))
+        return float(np.mean(res[3:] if len(res) > 8 else res)) / 1e3
+
+
+def time_gemv_back_to_back(wl, stream, n):
+    import torch
+    with torch.cuda.stream(stream):
+        g = capture(wl.gemv, n, stream)
+        g.replay()
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(4):
+            g.replay()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / 1e3 / (4 * n)
+
+
+def time_e2e(wl, stream, steps):
+    """Public API with host buffers: H2D of the activation row, the chain, D2H of y, wait."""
+    import torch
+    x_pin = torch.from_numpy(wl.x_host.copy()).pin_memory()
+    y_pin = torch.empty(wl.y.shape, dtype=torch.float32).pin_memory()
+    h2d = x_pin.numel() * 4
+    d2h = y_pin.numel() * 4
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            wl.x.copy_(x_pin, non_blocking=True)
+            wl.step(i)
+            y_pin.copy_(wl.y, non_blocking=True)
+            stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record(stream)
+        for i in range(steps):
+            wl.x.copy_(x_pin, non_blocking=True)
+            wl.step(i)
+            y_pin.copy_(wl.y, non_blocking=True)
+            stream.synchronize()
+        b.record(stream)
+        stream.synchronize()
+        wall = time.perf_counter() - t0
+    return {"elapsed": max(wall, a.elapsed_time(b) / 1e3), "steps": steps, "h2d": h2d, "d2h": d2h}
+
+
+# ------------------------------------------------------------------------------------------
+# The oracle on the host cores (CPU baseline and the reference arm)
+# ------------------------------------------------------------------------------------------
+
+def _oracle_inputs(kind, out_f, in_f, m, seed=0x51ED0002):
+    from quantized_decode_memq_gb300 import synth
+    x, wn = synth.activation_rows(in_f, m)
+    if kind == "q8_0":
+        return x, wn, synth.q8_0_bytes(seed, out_f, in_f), None
+    w = synth.e4m3_bytes(seed + 1, out_f, in_f)
+    aux = synth.grid_log2_uniform(seed + 2, out_f, in_f) if kind == "blk" else 2.0 ** -4
+    return x, wn, w, aux
+
+
+def _oracle_step(oracle, kind, x, wn, w, aux, in_f, rows=None):
+    _, d, qs, _ = oracle.rmsnorm_q8_1(x, wn, 1e-6)
+    if kind == "q8_0":
+        return oracle.gemv_q8_0(w, in_f, qs, d, rows=rows)
+    if kind == "blk":
+        return oracle.gemv_e4m3_blk128(w, aux, qs, d, rows=rows)
+    return oracle.gemv_e4m3(w, aux, qs, d, rows=rows)
+
+
+def _sample_bytes(kind, nrows, in_f, m):
+    """Algorithmic bytes of one oracle step that computes `nrows` output rows."""
+    return gemv_bytes(kind, nrows, in_f, m) - (4 if kind == "e4m3" else 0) + producer_bytes(m, in_f)
+
+
+def cpu_baseline(wl, seconds):
+    import oracle
+    oracle.build()
+    kind, out_f, in_f, m = wl.kind, wl.out_f, wl.in_f, wl.m
+    x, wn, w, aux = _oracle_inputs(kind, out_f, in_f, m)
+    _oracle_step(oracle, kind, x, wn, w, aux, in_f)  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(oracle, kind, x, wn, w, aux, in_f)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 10000:
+            break
+    return {"value": round(n * wl.step_bytes / el / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} full decode steps (f64 C oracle: producer + {kind} GEMV "
+                      f"{out_f}x{in_f} m={m}), {el:.1f} s wall, single thread",
+            "host_cpus": os.cpu_count()}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the timed arm: every step is the producer plus a bounded row sample of the
+    GEMV, sized from a calibration step so that warm-up + K steps take about a minute."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    kind, out_f, in_f, m, copies = WORKLOADS[args.workload]
+    x, wn, w, aux = _oracle_inputs(kind, out_f, in_f, m)
+    t0 = time.perf_counter()
+    _oracle_step(oracle, kind, x, wn, w, aux, in_f, rows=np.arange(min(out_f, 256)))
+    per_row = (time.perf_counter() - t0) / min(out_f, 256)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    nrows = int(max(1, min(out_f, budget / max(per_row, 1e-9))))
+    rng = np.random.default_rng(7)
+    samples = [np.sort(rng.choice(out_f, size=nrows, replace=False)) for _ in range(8)]
+    for i in range(args.warmup):
+        _oracle_step(oracle, kind, x, wn, w, aux, in_f, rows=samples[i % 8])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_step(oracle, kind, x, wn, w, aux, in_f, rows=samples[i % 8])
+    el = time.perf_counter() - t0
+    v = args.steps * _sample_bytes(kind, nrows, in_f, m) / el / 1e9
+    sample = (f"each step: producer 1x{in_f} + {nrows} of {out_f} GEMV rows ({kind}, m={m}), "
+              f"f64 C oracle, single thread")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(v, 5),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: f64 C oracle of the same decode step "
+                               f"(producer + {kind} GEMV out_f={out_f} in_f={in_f} m={m})",
+                   "sample_rows_per_step": nrows},
+        "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=3000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per GEMV launch from an ncu capture of this kernel")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

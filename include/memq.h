@@ -1,0 +1,136 @@
+/*
+ * memq.h -- C ABI of libmemq: the m <= 8 quantized decode chain on GB300 (sm_103a).
+ *
+ * Two stages, each one asynchronous kernel launch on the caller's CUDA stream:
+ *
+ *   1. memq_rmsnorm_q8_1      f32 rows -> RMSNorm -> q8_1 activation (int8 qs + f32 d per 32)
+ *   2. memq_gemv_e4m3         raw FP8 E4M3 weights, one per-tensor f32 scale   (1.0 B/weight)
+ *      memq_gemv_e4m3_blk128  E4M3 weights + f32 block-128 scale grid          (1.0 B/weight)
+ *      memq_gemv_q8_0         ggml block_q8_0 weights (f16 scale + 32 int8)     (1.0625 B/weight)
+ *
+ * The operations are the ones defined on the memra-engine 0.125.0 source pages:
+ * q8_fuse_gate.rs (module doc: the `rms_norm` -> `quantize_q8_1` chain and the fused
+ * `rms_norm_zq8_f32` producer) and gemv_e4m3_bench.rs (module doc, "THE COMPARISON" and "THE
+ * BLOCK-128 ARM", and the container generators `synth_e4m3`, `synth_blk_grid`, `synth_q8_0`).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must be device-accessible memory of the current CUDA device
+ *     (cudaMalloc / torch CUDA tensors).  The caller owns every buffer; the library never
+ *     allocates, frees or keeps a pointer after the call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue work;
+ *     they never synchronize.  Results are ready when the stream reaches the launch.
+ *   - Arguments are validated on the host before anything is launched; on any error the call
+ *     returns a nonzero memq_status and writes nothing.  A launch failure returns
+ *     MEMQ_ERR_LAUNCH.  Device-side waits are bounded: if one ever expires, the kernel records
+ *     a fault bit that memq_device_fault() reports, and returns without hanging.
+ *   - Outputs must not alias inputs.
+ *   - Row-major layouts throughout; "m" is the number of activation rows (decode tokens),
+ *     1 <= m <= 8.
+ */
+#ifndef MEMQ_H
+#define MEMQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum memq_status {
+    MEMQ_OK = 0,
+    MEMQ_ERR_NULL = 1,    /* a required pointer is NULL */
+    MEMQ_ERR_SHAPE = 2,   /* a size is out of range or not a multiple of 32 */
+    MEMQ_ERR_ALIGN = 3,   /* a pointer breaks its documented alignment */
+    MEMQ_ERR_M_RANGE = 4, /* m outside [1, 8] */
+    MEMQ_ERR_LAUNCH = 5,  /* the CUDA launch (or a device query before it) failed */
+    MEMQ_ERR_DEVICE = 6   /* memq_device_fault() could not read the device fault word */
+} memq_status;
+
+/* Maximum activation rows per GEMV call. */
+#define MEMQ_MAX_M 8
+/* Largest row width accepted by memq_rmsnorm_q8_1. */
+#define MEMQ_MAX_NCOLS 32768
+
+/*
+ * memq_rmsnorm_q8_1 -- fused RMSNorm -> q8_1 producer.
+ * Defined by q8_fuse_gate.rs (module doc; `run_shape` compares the two-launch `rms_norm` +
+ * `quantize_q8_1` chain with the fused `rms_norm_zq8_f32`).  For each row r < rows:
+ *     z[r][i] = (x[r][i] * rr) * w[i],   rr = 1 / sqrt(sum_i x[r][i]^2 / ncols + eps)
+ * then for each 32-element block b of the row:
+ *     d[r][b]  = max_{i in b} |z[r][i]| / 127              (f32)
+ *     qs[r][i] = round(z[r][i] / d[r][b]) (ties away from zero), or 0 when d[r][b] == 0
+ * so |qs| <= 127 and the block's largest |z| maps to +-127.
+ *   x   device, f32 [rows][ncols], 16-byte aligned
+ *   w   device, f32 [ncols], 16-byte aligned (one weight vector shared by all rows)
+ *   z   device, f32 [rows][ncols], 16-byte aligned, or NULL to skip writing z
+ *   qs  device, int8 [rows][ncols], 4-byte aligned
+ *   d   device, f32 [rows][ncols/32]
+ *   ncols: 32 <= ncols <= MEMQ_MAX_NCOLS, ncols % 32 == 0;  eps >= 0;  rows >= 0, where
+ *   rows == 0 is a no-op that accepts NULL pointers.
+ * Numerics: the row statistic is accumulated in f32 per thread and f64 across threads, r uses
+ * IEEE f32 divide and square root; z uses f32 products; qs uses an IEEE f32 division z/d.
+ */
+int memq_rmsnorm_q8_1(const float *x, const float *w, float *z, int8_t *qs, float *d,
+                      int64_t ncols, int64_t rows, float eps, void *stream);
+
+/*
+ * memq_gemv_e4m3 -- y = s * W_e4m3 . X_q8_1 (per-tensor scale).
+ * Defined by gemv_e4m3_bench.rs (module doc, "THE COMPARISON", arm E4M3: raw checkpoint E4M3
+ * bytes as the weight stream, row_bytes == in_f; `synth_e4m3`).  For j < m, r < out_f:
+ *     y[j][r] = s * sum_i e4m3(w[r][i]) * d[j][i/32] * qs[j][i]
+ *   w        device, uint8 E4M3 codes [out_f][in_f] (0x7F/0xFF are NaN and propagate)
+ *   w_scale  device, one f32 (the per-tensor scale s); read by the kernel, so it may change
+ *            between graph replays
+ *   qs, d    device, the q8_1 activation: int8 [m][in_f] and f32 [m][in_f/32]
+ *   y        device, f32 [m][out_f]
+ *   in_f % 32 == 0, 32 <= in_f <= 2^24; 1 <= m <= MEMQ_MAX_M; out_f >= 0, where out_f == 0
+ *   is a no-op that accepts NULL pointers.
+ * The fast path wants w 16-byte and qs 8-byte aligned; other alignments take a slower generic
+ * kernel with the same results contract.
+ */
+int memq_gemv_e4m3(const uint8_t *w, const float *w_scale, const int8_t *qs, const float *d,
+                   float *y, int64_t out_f, int64_t in_f, int m, void *stream);
+
+/*
+ * memq_gemv_e4m3_blk128 -- y = (G (x) W_e4m3) . X_q8_1 with a block-128 scale grid.
+ * Defined by gemv_e4m3_bench.rs (module doc, "THE BLOCK-128 ARM": the raw E4M3 plane plus a
+ * resident f32 [ceil(out_f/128), ceil(in_f/128)] grid in F8BlockGrid order; `synth_blk_grid`):
+ *     y[j][r] = sum_i grid[r/128][i/128] * e4m3(w[r][i]) * d[j][i/32] * qs[j][i]
+ *   grid  device, f32 [ceil(out_f/128)][ceil(in_f/128)] row-major; a partial edge tile uses
+ *         its own entry.  Other arguments as memq_gemv_e4m3.
+ */
+int memq_gemv_e4m3_blk128(const uint8_t *w, const float *grid, const int8_t *qs, const float *d,
+                          float *y, int64_t out_f, int64_t in_f, int m, void *stream);
+
+/*
+ * memq_gemv_q8_0 -- y = W_q8_0 . X_q8_1.
+ * Defined by gemv_e4m3_bench.rs (module doc, arm Q8_0, row_bytes = in_f/32*34; `synth_q8_0`:
+ * ggml block_q8_0 = a little-endian f16 scale then 32 int8 weights, 34 bytes per 32 weights):
+ *     y[j][r] = sum_i f16(blk(r, i/32).d) * blk(r, i/32).qs[i%32] * d[j][i/32] * qs[j][i]
+ *   w   device, out_f rows of in_f/32 blocks of 34 bytes, rows packed back to back
+ *   Other arguments as memq_gemv_e4m3.  The fast path wants w and qs 16-byte aligned and
+ *   in_f % 256 == 0 (so every row starts 16-byte aligned); anything else takes the generic
+ *   kernel.  The full int8 range (including -128) is accepted in both operands.
+ */
+int memq_gemv_q8_0(const void *w, const int8_t *qs, const float *d, float *y, int64_t out_f,
+                   int64_t in_f, int m, void *stream);
+
+/* Human-readable name of a memq_status value (static storage; never NULL). */
+const char *memq_status_string(int status);
+
+/*
+ * memq_device_fault -- read and clear the current device's fault word.
+ * Synchronizes `stream`, then stores the word in *fault_out (0 = no fault) and resets it.
+ * Bit 0: a bounded wait on a shared-memory barrier in a GEMV kernel expired.
+ * Returns MEMQ_ERR_NULL for a NULL fault_out, MEMQ_ERR_DEVICE if the copy fails.
+ */
+int memq_device_fault(void *stream, uint32_t *fault_out);
+
+/* ABI version of this header: (major << 16) | minor. */
+int memq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEMQ_H */

@@ -1,0 +1,29 @@
+"""memq for GB300: the m <= 8 quantized decode chain as hand-written sm_103a CUDA kernels.
+
+The compute lives in ``libmemq.so`` behind the C ABI of ``include/memq.h``; this module is a
+thin ctypes binding with the same entry-point names.  It only checks and marshals arguments
+(torch CUDA tensors -> device pointers, the current torch stream -> ``cudaStream_t``) and
+raises on a nonzero status.  There is no CPU fallback: if the library is missing every call
+raises.
+
+Stage 1 -- ``memq_rmsnorm_q8_1``: q8_fuse_gate.rs (memra-engine 0.125.0), the fused
+``rms_norm_zq8_f32`` producer.  Stage 2 -- ``memq_gemv_e4m3``, ``memq_gemv_e4m3_blk128``,
+``memq_gemv_q8_0``: gemv_e4m3_bench.rs, the E4M3 / block-128 / Q8_0 arms.
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    MAX_M,
+    MAX_NCOLS,
+    MemqError,
+    Status,
+    lib,
+    lib_path,
+    memq_device_fault,
+    memq_gemv_e4m3,
+    memq_gemv_e4m3_blk128,
+    memq_gemv_q8_0,
+    memq_rmsnorm_q8_1,
+    memq_status_string,
+    memq_version,
+)

@@ -1,0 +1,200 @@
+"""ctypes binding of libmemq.so (argument marshalling only; all compute is in the kernels)."""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libmemq.so")
+_lock = threading.Lock()
+_lib = None
+
+MAX_M = 8
+MAX_NCOLS = 32768
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_NULL = 1
+    ERR_SHAPE = 2
+    ERR_ALIGN = 3
+    ERR_M_RANGE = 4
+    ERR_LAUNCH = 5
+    ERR_DEVICE = 6
+
+
+class MemqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: memq status {status} ({memq_status_string(status)})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmemq.so; raise (never fall back) if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"libmemq.so is missing at {_LIB_PATH}: build it with "
+                    "quantized_decode_memq_gb300.build.build() (there is no CPU fallback)")
+            L = ctypes.CDLL(_LIB_PATH)
+            P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            L.memq_rmsnorm_q8_1.argtypes = [P, P, P, P, P, I64, I64, ctypes.c_float, P]
+            L.memq_gemv_e4m3.argtypes = [P, P, P, P, P, I64, I64, I32, P]
+            L.memq_gemv_e4m3_blk128.argtypes = [P, P, P, P, P, I64, I64, I32, P]
+            L.memq_gemv_q8_0.argtypes = [P, P, P, P, I64, I64, I32, P]
+            L.memq_device_fault.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            L.memq_status_string.argtypes = [I32]
+            L.memq_status_string.restype = ctypes.c_char_p
+            L.memq_version.argtypes = []
+            for name in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
+                         "memq_gemv_q8_0", "memq_device_fault", "memq_version"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def memq_status_string(status: int) -> str:
+    return lib().memq_status_string(int(status)).decode()
+
+
+def memq_version() -> int:
+    return lib().memq_version()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise MemqError(fn, rc)
+
+
+def _cuda(name: str, t: torch.Tensor, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def memq_rmsnorm_q8_1(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *, z=None, qs=None,
+                      d=None, want_z: bool = True, stream=None):
+    """Fused RMSNorm -> q8_1.  x: f32 [rows, ncols], w: f32 [ncols].
+
+    Returns (z f32 [rows, ncols] or None, qs int8 [rows, ncols], d f32 [rows, ncols/32]).
+    Output tensors may be passed in (z/qs/d) to avoid allocation.
+    """
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    _cuda("x", x2, torch.float32)
+    rows, ncols = x2.shape
+    _cuda("w", w, torch.float32, (ncols,))
+    if qs is None:
+        qs = torch.empty((rows, ncols), dtype=torch.int8, device=x.device)
+    if d is None:
+        d = torch.empty((rows, ncols // 32), dtype=torch.float32, device=x.device)
+    if z is None and want_z:
+        z = torch.empty((rows, ncols), dtype=torch.float32, device=x.device)
+    _cuda("qs", qs, torch.int8, (rows, ncols))
+    _cuda("d", d, torch.float32, (rows, ncols // 32))
+    if z is not None:
+        _cuda("z", z, torch.float32, (rows, ncols))
+    rc = lib().memq_rmsnorm_q8_1(_ptr(x2), _ptr(w), _ptr(z), _ptr(qs), _ptr(d), ncols, rows,
+                                 ctypes.c_float(eps), _stream(stream))
+    _check("memq_rmsnorm_q8_1", rc)
+    return z, qs, d
+
+
+def _act(qs, d, in_f):
+    qs2 = qs if qs.dim() == 2 else qs.reshape(1, -1)
+    _cuda("qs", qs2, torch.int8)
+    m = qs2.shape[0]
+    if qs2.shape[1] != in_f:
+        raise ValueError(f"qs has {qs2.shape[1]} columns, expected in_f={in_f}")
+    d2 = d if d.dim() == 2 else d.reshape(1, -1)
+    _cuda("d", d2, torch.float32, (m, in_f // 32))
+    return qs2, d2, m
+
+
+def _out(y, m, out_f, device):
+    if y is None:
+        y = torch.empty((m, out_f), dtype=torch.float32, device=device)
+    _cuda("y", y, torch.float32, (m, out_f))
+    return y
+
+
+def memq_gemv_e4m3(w: torch.Tensor, w_scale: torch.Tensor, qs: torch.Tensor, d: torch.Tensor, *,
+                   y=None, stream=None):
+    """y[m, out_f] = scale * e4m3(w) . (d*qs).  w: uint8 [out_f, in_f]; w_scale: f32 [1]."""
+    _cuda("w", w, torch.uint8)
+    out_f, in_f = w.shape
+    _cuda("w_scale", w_scale, torch.float32, (1,))
+    qs2, d2, m = _act(qs, d, in_f)
+    y = _out(y, m, out_f, w.device)
+    rc = lib().memq_gemv_e4m3(_ptr(w), _ptr(w_scale), _ptr(qs2), _ptr(d2), _ptr(y), out_f, in_f,
+                              m, _stream(stream))
+    _check("memq_gemv_e4m3", rc)
+    return y
+
+
+def memq_gemv_e4m3_blk128(w: torch.Tensor, grid: torch.Tensor, qs: torch.Tensor, d: torch.Tensor,
+                          *, y=None, stream=None):
+    """y = (grid (x) e4m3(w)) . (d*qs); grid: f32 [ceil(out_f/128), ceil(in_f/128)]."""
+    _cuda("w", w, torch.uint8)
+    out_f, in_f = w.shape
+    _cuda("grid", grid, torch.float32, ((out_f + 127) // 128, (in_f + 127) // 128))
+    qs2, d2, m = _act(qs, d, in_f)
+    y = _out(y, m, out_f, w.device)
+    rc = lib().memq_gemv_e4m3_blk128(_ptr(w), _ptr(grid), _ptr(qs2), _ptr(d2), _ptr(y), out_f,
+                                     in_f, m, _stream(stream))
+    _check("memq_gemv_e4m3_blk128", rc)
+    return y
+
+
+def memq_gemv_q8_0(w: torch.Tensor, qs: torch.Tensor, d: torch.Tensor, *, y=None, stream=None):
+    """y = W_q8_0 . (d*qs); w: uint8 [out_f, in_f/32*34] (ggml block_q8_0 rows)."""
+    _cuda("w", w, torch.uint8)
+    out_f, row_bytes = w.shape
+    if row_bytes % 34 != 0:
+        raise ValueError("Q8_0 rows must be a whole number of 34-byte blocks")
+    in_f = row_bytes // 34 * 32
+    qs2, d2, m = _act(qs, d, in_f)
+    y = _out(y, m, out_f, w.device)
+    rc = lib().memq_gemv_q8_0(_ptr(w), _ptr(qs2), _ptr(d2), _ptr(y), out_f, in_f, m,
+                              _stream(stream))
+    _check("memq_gemv_q8_0", rc)
+    return y
+
+
+def memq_device_fault(stream=None) -> int:
+    """Synchronize the stream, then read and clear the device fault word (0 = none)."""
+    v = ctypes.c_uint32(0)
+    rc = lib().memq_device_fault(_stream(stream), ctypes.byref(v))
+    _check("memq_device_fault", rc)
+    return int(v.value)

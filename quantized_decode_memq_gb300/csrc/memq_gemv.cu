@@ -1,0 +1,592 @@
+// memq_gemv.cu -- weight-stream GEMVs against a q8_1 activation, m <= 8 activation rows.
+//
+// Operations: gemv_e4m3_bench.rs (memra-engine 0.125.0), module doc -- "THE COMPARISON" (arm
+// E4M3: raw E4M3 bytes, one per-tensor scale; arm Q8_0: ggml block_q8_0, 34 B per 32 weights)
+// and "THE BLOCK-128 ARM" (E4M3 plus an f32 [ceil(out_f/128), ceil(in_f/128)] scale grid).
+//
+// Fast path ("stream" kernel), one skeleton for all three containers:
+//   * CTA c owns output rows [R0, R1), an equal share (+-1 row) of out_f, so every SM streams
+//     the same number of weight bytes.  Its rows are processed in tiles; the K dimension of
+//     every tile is split into 8 equal slices, one per warp, so all warps stream every tile.
+//   * Each warp runs its own S-stage ring of shared-memory slots.  A stage is one chunk of the
+//     warp's K slice for all rows of the tile, filled with one 1-D bulk asynchronous copy
+//     (cp.async.bulk, L2 evict-first) per row, issued by lanes 0..rows-1 and completing on the
+//     stage's mbarrier; the warp waits on it (bounded), computes, and refills the slot.
+//   * At the end of a tile every warp leaves its partial sums in shared memory; after one CTA
+//     barrier the 8 partials of each (row, token) are added in warp order (deterministic) and
+//     stored.  Partial buffers alternate between tiles, so one barrier per tile suffices.
+//   * Weight copies for the first S stages are issued before waiting on the preceding launch
+//     (programmatic dependent launch); the activation is read only after that wait.
+//   * E4M3 / block-128 inner product on the tensor cores (mma.sync m16n8k16, f16 operands,
+//     f32 accumulation).  E4M3 -> f16 (hardware cvt) and int8 -> f16 are exact and f16 x f16
+//     products are exact in f32, so this is numerically an f32 dot product; the instruction
+//     count per weight is ~5x lower than CUDA-core FMAs, which left the kernel issue-bound.
+//   * Q8_0 inner product with dp4a (exact int32 dot of 32 int8 pairs) on 4-row tiles.
+// Generic path: a plain warp-per-row kernel with byte loads for anything the fast path does not
+// take (unaligned pointers, Q8_0 rows that are not 16-byte aligned).
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <mutex>
+
+#include "memq.h"
+#include "memq_dev.cuh"
+
+namespace memq {
+
+// Device-side fault word (bit 0: a bounded mbarrier wait expired).  Read by memq_device_fault.
+__device__ unsigned int g_memq_fault = 0;
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 4;  // ring depth per warp (reduced if shared memory runs short)
+
+enum Kind : int { kE4M3 = 0, kBlk = 1, kQ80 = 2 };
+
+// Stream-kernel geometry per container.
+//   E4M3 / block-128 (tensor-core inner product): a tile is 32 rows (two m16 MMA row tiles), a
+//   stage holds 4 blocks (128 weights) of every tile row, each row slot padded to 144 bytes so
+//   the 8-byte fragment loads of 8 different rows hit 8 different bank groups.
+//   Q8_0 (dp4a inner product): a tile is 4 rows, a stage holds 32 blocks (1088 bytes) per row,
+//   lane l owns block l.
+template <int KIND>
+struct Geo {
+    static constexpr bool kMma = KIND != kQ80;
+    static constexpr int kBlockBytes = kMma ? 32 : 34;
+    static constexpr int kTileRows = kMma ? 32 : 4;
+    static constexpr int kChunkBlocks = kMma ? 4 : 32;
+    static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
+    static constexpr int kStage = kTileRows * kSlot;
+    static constexpr int kSliceQuantum = kMma ? 1 : 8;  // K-slice granularity in blocks
+};
+
+struct StreamArgs {
+    const uint8_t *w;
+    const float *aux;  // per-tensor scale (E4M3) or grid (block-128); unused for Q8_0
+    const int8_t *qs;
+    const float *d;
+    float *y;
+    int64_t out_f;
+    int64_t row_bytes;
+    int in_f;
+    int nb;     // in_f / 32
+    int gcols;  // ceil(in_f / 128)
+    int stages;
+    uint32_t off_part, off_ring;  // shared-memory layout (bytes); barriers at offset 0
+};
+
+__device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bit); }
+
+// ---------------------------------------------------------------------------------------------
+// E4M3 / block-128 stage: tensor-core inner products.
+//
+// Per 32-weight block and 16-row tile, two m16n8k16 MMAs with A = 16 weight rows (E4M3 decoded
+// to f16 by the hardware cvt) and B = the q8_1 activation of up to 8 tokens (int8 -> f16),
+// accumulating in f32; the 16x8 block result is then scaled by d[token][block] (and the grid
+// entry) into f32 accumulators.  The dot product is order-free, so the K index inside a block is
+// permuted: thread (g, t) = (lane/4, lane%4) supplies physical columns 8t..8t+7 of its rows for
+// MMA slots {2t, 2t+1, 2t+8, 2t+9} (first MMA: 8t..8t+3, second: 8t+4..8t+7), and the B
+// fragment of token g uses exactly the same map.
+// acc[tt][0..3] = rows (tt*16+g, tt*16+g+8) x tokens (2t, 2t+1).
+// ---------------------------------------------------------------------------------------------
+template <int KIND, int M>
+__device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *stage,
+                                          int64_t row0, int64_t row_last, int kb0, int nblk,
+                                          int lane, float (&acc)[2][4]) {
+    using G = Geo<KIND>;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const float *grow[4] = {nullptr, nullptr, nullptr, nullptr};
+    if (KIND == kBlk) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // rows g, g+8, 16+g, 24+g of the tile (clamped)
+            int64_t r = row0 + (i >> 1) * 16 + (i & 1) * 8 + g;
+            r = r > row_last ? row_last : r;
+            grow[i] = a.aux + (r >> 7) * a.gcols;
+        }
+    }
+#pragma unroll 1
+    for (int b = 0; b < nblk; ++b) {
+        const int kb = kb0 + b;
+        uint32_t bq[4] = {0u, 0u, 0u, 0u};
+        if (g < M) {
+            const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(
+                a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+            s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
+            s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
+        }
+        const float dx0 = (2 * t < M) ? __ldg(a.d + (2 * t) * a.nb + kb) : 0.f;
+        const float dx1 = (2 * t + 1 < M) ? __ldg(a.d + (2 * t + 1) * a.nb + kb) : 0.f;
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            const uint8_t *pa = stage + (tt * 16 + g) * G::kSlot + 32 * b + 8 * t;
+            const uint2 wa = lds64(pa);
+            const uint2 wb = lds64(pa + 8 * G::kSlot);
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_f16_16816(c, e4m3x2_to_f16x2(wa.x & 0xffffu), e4m3x2_to_f16x2(wb.x & 0xffffu),
+                          e4m3x2_to_f16x2(wa.x >> 16), e4m3x2_to_f16x2(wb.x >> 16), bq[0], bq[1]);
+            mma_f16_16816(c, e4m3x2_to_f16x2(wa.y & 0xffffu), e4m3x2_to_f16x2(wb.y & 0xffffu),
+                          e4m3x2_to_f16x2(wa.y >> 16), e4m3x2_to_f16x2(wb.y >> 16), bq[2], bq[3]);
+            float k0 = dx0, k1 = dx1, k2 = dx0, k3 = dx1;
+            if (KIND == kBlk) {
+                const float gg = __ldg(grow[2 * tt] + (kb >> 2));
+                const float gg8 = __ldg(grow[2 * tt + 1] + (kb >> 2));
+                k0 *= gg;
+                k1 *= gg;
+                k2 *= gg8;
+                k3 *= gg8;
+            }
+            acc[tt][0] = fmaf(c[0], k0, acc[tt][0]);
+            acc[tt][1] = fmaf(c[1], k1, acc[tt][1]);
+            acc[tt][2] = fmaf(c[2], k2, acc[tt][2]);
+            acc[tt][3] = fmaf(c[3], k3, acc[tt][3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Q8_0 stage: lane l owns block l of the stage for each of the tile's 4 rows.  The block's 32
+// weights start 2 bytes into a 34-byte record, so they are re-aligned from 4-byte shared loads
+// with funnel shifts, then dp4a gives the exact int32 dot product with the activation block.
+// ---------------------------------------------------------------------------------------------
+template <int M>
+__device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *stage, int rc,
+                                          int kb0, int nblk, int lane, float (&acc)[4][M]) {
+    using G = Geo<kQ80>;
+    if (lane >= nblk) return;
+    const int kb = kb0 + lane;
+    uint32_t qw[4][8];
+    float dw[4];
+    const int qstart = 34 * lane + 2;
+    const int abase = qstart & ~3;
+    const uint32_t sh = static_cast<uint32_t>(qstart & 3) * 8u;  // 0 or 16
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        if (rr < rc) {
+            const uint8_t *slot = stage + rr * G::kSlot;
+            uint32_t wv[9];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) wv[i] = lds32(slot + abase + 4 * i);
+            wv[8] = sh ? lds32(slot + abase + 32) : 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qw[rr][i] = __funnelshift_r(wv[i], wv[i + 1], sh);
+            dw[rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(slot + 34 * lane))));
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+        const uint4 *qx = reinterpret_cast<const uint4 *>(a.qs + static_cast<int64_t>(j) * a.in_f + 32 * kb);
+        const uint4 x0 = __ldg(qx);
+        const uint4 x1 = __ldg(qx + 1);
+        const float dj = __ldg(a.d + j * a.nb + kb);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            if (rr < rc) {
+                int s = 0;
+                s = __dp4a(static_cast<int>(qw[rr][0]), static_cast<int>(x0.x), s);
+                s = __dp4a(static_cast<int>(qw[rr][1]), static_cast<int>(x0.y), s);
+                s = __dp4a(static_cast<int>(qw[rr][2]), static_cast<int>(x0.z), s);
+                s = __dp4a(static_cast<int>(qw[rr][3]), static_cast<int>(x0.w), s);
+                s = __dp4a(static_cast<int>(qw[rr][4]), static_cast<int>(x1.x), s);
+                s = __dp4a(static_cast<int>(qw[rr][5]), static_cast<int>(x1.y), s);
+                s = __dp4a(static_cast<int>(qw[rr][6]), static_cast<int>(x1.z), s);
+                s = __dp4a(static_cast<int>(qw[rr][7]), static_cast<int>(x1.w), s);
+                acc[rr][j] = fmaf(static_cast<float>(s), dw[rr] * dj, acc[rr][j]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// The stream kernel (see the file header for the schedule).
+// ---------------------------------------------------------------------------------------------
+template <int KIND, int M>
+__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const StreamArgs a) {
+    using G = Geo<KIND>;
+    constexpr int TR = G::kTileRows;
+    extern __shared__ __align__(128) uint8_t smem[];
+    griddep_launch_dependents();
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = a.stages;
+
+    const int64_t R0 = static_cast<int64_t>(blockIdx.x) * a.out_f / gridDim.x;
+    const int64_t R1 = static_cast<int64_t>(blockIdx.x + 1) * a.out_f / gridDim.x;
+    const int ntiles = static_cast<int>((R1 - R0 + TR - 1) / TR);
+
+    // This warp's K slice, in blocks.
+    const int nq = a.nb / G::kSliceQuantum;
+    const int kb_lo = (warp * nq / kWarps) * G::kSliceQuantum;
+    const int kb_hi = ((warp + 1) * nq / kWarps) * G::kSliceQuantum;
+    const int nch = (kb_hi - kb_lo + G::kChunkBlocks - 1) / G::kChunkBlocks;
+    const int items = ntiles * nch;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
+    uint8_t *ring = smem + a.off_ring + static_cast<size_t>(warp) * S * G::kStage;
+    float *part = reinterpret_cast<float *>(smem + a.off_part);  // [2][kWarps][TR][M]
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    // Producer side: (tile, chunk, stage) of the next item to issue.
+    const uint64_t pol = l2_evict_first_policy();
+    int p_tile = 0, p_ch = 0, p_stage = 0, issued = 0;
+    auto issue_next = [&]() {
+        const int64_t r0 = R0 + static_cast<int64_t>(p_tile) * TR;
+        const int rc = static_cast<int>(R1 - r0 < TR ? R1 - r0 : TR);
+        const int kb = kb_lo + p_ch * G::kChunkBlocks;
+        const int nblk = min(G::kChunkBlocks, kb_hi - kb);
+        const uint32_t bytes = static_cast<uint32_t>(nblk * G::kBlockBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[p_stage], bytes * rc);
+        __syncwarp();
+        if (lane < rc)
+            bulk_g2s(ring + p_stage * G::kStage + lane * G::kSlot,
+                     a.w + (r0 + lane) * a.row_bytes + static_cast<int64_t>(kb) * G::kBlockBytes,
+                     bytes, &bars[p_stage], pol);
+        ++issued;
+        if (++p_ch == nch) {
+            p_ch = 0;
+            ++p_tile;
+        }
+        if (++p_stage == S) p_stage = 0;
+    };
+    // Weights do not depend on the preceding launch: start streaming before waiting for it.
+    while (issued < items && issued < S) issue_next();
+
+    griddep_wait();
+    float scale = 1.0f;
+    if (KIND == kE4M3) scale = __ldg(a.aux);
+
+    bool ok = true;
+    int c_stage = 0;
+    uint32_t c_phase = 0;
+    int consumed = 0;
+    for (int tile = 0; tile < ntiles; ++tile) {
+        const int64_t r0 = R0 + static_cast<int64_t>(tile) * TR;
+        const int rc = static_cast<int>(R1 - r0 < TR ? R1 - r0 : TR);
+        float acc_m[2][4];
+        float acc_q[4][M];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc_m[i][j] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < M; ++j) acc_q[i][j] = 0.f;
+
+        for (int ch = 0; ch < nch; ++ch) {
+            if (ok && !warp_wait_bounded(&bars[c_stage], c_phase)) {
+                // Record the fault, give the copies in flight a bounded chance to land, and stop
+                // streaming; the tile barriers below still run so no warp is stranded.
+                if (lane == 0) fault(1u);
+                int st = c_stage;
+                uint32_t ph = c_phase;
+                for (int j = consumed + 1; j < issued; ++j) {
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                    (void)warp_wait_bounded(&bars[st], ph);
+                }
+                ok = false;
+            }
+            if (ok) {
+                const int kb = kb_lo + ch * G::kChunkBlocks;
+                const int nblk = min(G::kChunkBlocks, kb_hi - kb);
+                const uint8_t *stage = ring + c_stage * G::kStage;
+                if (G::kMma)
+                    mma_stage<KIND, M>(a, stage, r0, R1 - 1, kb, nblk, lane, acc_m);
+                else
+                    q80_stage<M>(a, stage, rc, kb, nblk, lane, acc_q);
+                __syncwarp();
+                ++consumed;
+                if (issued < items) issue_next();  // refills the slot just consumed
+            }
+            if (++c_stage == S) {
+                c_stage = 0;
+                c_phase ^= 1u;
+            }
+        }
+
+        // Per-warp partials of this tile -> shared memory.
+        float *pw = part + ((tile & 1) * kWarps + warp) * TR * M;
+        if (G::kMma) {
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                const int ra = tt * 16 + g, rb = ra + 8;
+                if (2 * t < M) {
+                    pw[ra * M + 2 * t] = acc_m[tt][0];
+                    pw[rb * M + 2 * t] = acc_m[tt][2];
+                }
+                if (2 * t + 1 < M) {
+                    pw[ra * M + 2 * t + 1] = acc_m[tt][1];
+                    pw[rb * M + 2 * t + 1] = acc_m[tt][3];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                for (int j = 0; j < M; ++j) {
+                    const float v = warp_sum(acc_q[rr][j]);
+                    if (lane == 0) pw[rr * M + j] = v;
+                }
+        }
+        __syncthreads();
+        // Sum the 8 warp partials of each (row, token) in warp order and store y.
+        for (int idx = threadIdx.x; idx < rc * M; idx += kThreads) {
+            const int row = idx / M, tok = idx - row * M;
+            const float *pt = part + (tile & 1) * kWarps * TR * M + row * M + tok;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v += pt[w * TR * M];
+            a.y[static_cast<int64_t>(tok) * a.out_f + r0 + row] = v * scale;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Generic kernel: one warp per output row, byte-granular global loads, any alignment.
+// ---------------------------------------------------------------------------------------------
+template <int KIND>
+__global__ void __launch_bounds__(kThreads)
+    gemv_generic_kernel(const uint8_t *__restrict__ w, const float *__restrict__ aux,
+                        const int8_t *__restrict__ qs, const float *__restrict__ d,
+                        float *__restrict__ y, int64_t out_f, int in_f, int m) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (r >= out_f) return;
+    const int nb = in_f / 32;
+    const int gcols = (in_f + 127) / 128;
+    const int64_t row_bytes = (KIND == kQ80) ? static_cast<int64_t>(nb) * 34 : in_f;
+    const uint8_t *wr = w + r * row_bytes;
+    float acc[MEMQ_MAX_M];
+    for (int j = 0; j < MEMQ_MAX_M; ++j) acc[j] = 0.f;
+    for (int kb = lane; kb < nb; kb += 32) {
+        float wf[32];
+        float bscale = 1.0f;
+        if (KIND == kQ80) {
+            const uint8_t *blk = wr + static_cast<int64_t>(kb) * 34;
+            bscale = __half2float(__ushort_as_half(static_cast<unsigned short>(blk[0] | (blk[1] << 8))));
+            for (int t = 0; t < 32; ++t) wf[t] = static_cast<float>(static_cast<int8_t>(blk[2 + t]));
+        } else {
+            for (int t = 0; t < 32; t += 2) {
+                const uint32_t two = wr[32 * kb + t] | (static_cast<uint32_t>(wr[32 * kb + t + 1]) << 8);
+                const uint32_t h2 = e4m3x2_to_f16x2(two);
+                wf[t] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+                wf[t + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+            }
+            if (KIND == kBlk) bscale = aux[(r >> 7) * gcols + (kb >> 2)];
+        }
+        for (int j = 0; j < m; ++j) {
+            const int8_t *qx = qs + static_cast<int64_t>(j) * in_f + 32 * kb;
+            float p = 0.f;
+            for (int t = 0; t < 32; ++t) p = fmaf(wf[t], static_cast<float>(qx[t]), p);
+            acc[j] = fmaf(p, bscale * d[static_cast<int64_t>(j) * nb + kb], acc[j]);
+        }
+    }
+    const float scale = (KIND == kE4M3) ? aux[0] : 1.0f;
+    for (int j = 0; j < m; ++j) {
+        const float v = warp_sum(acc[j]);
+        if (lane == 0) y[static_cast<int64_t>(j) * out_f + r] = v * scale;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+std::atomic<uint32_t> g_attr_set[kMaxDevices][3];  // bit (M-1) per kind: max-smem attribute set
+
+bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+cudaError_t device_info(int &dev, DeviceInfo &info) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaError_t err = cudaSuccess;
+    std::call_once(g_dev_once[dev], [&] {
+        DeviceInfo di;
+        err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err == cudaSuccess)
+            err = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (err == cudaSuccess) g_dev[dev] = di;
+    });
+    if (err != cudaSuccess) return err;
+    info = g_dev[dev];
+    return info.sms > 0 ? cudaSuccess : cudaErrorInvalidDevice;
+}
+
+template <int KIND, int M>
+cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const DeviceInfo &info,
+                          cudaStream_t st) {
+    auto kern = gemv_stream_kernel<KIND, M>;
+    const uint32_t bit = 1u << (M - 1);
+    if (!(g_attr_set[dev][KIND].load(std::memory_order_acquire) & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             info.smem_optin);
+        if (e != cudaSuccess) return e;
+        g_attr_set[dev][KIND].fetch_or(bit, std::memory_order_acq_rel);
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes);
+    if (e != cudaSuccess) return e;
+    per_sm = std::max(per_sm, 1);
+    // One wave of CTAs, never more CTAs than output rows.
+    int64_t grid = static_cast<int64_t>(info.sms) * per_sm;
+    grid = std::min<int64_t>(grid, a.out_f);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int KIND>
+cudaError_t launch_stream_m(int m, StreamArgs a, uint32_t smem, int dev, const DeviceInfo &info,
+                            cudaStream_t st) {
+    switch (m) {
+        case 1: return launch_stream<KIND, 1>(a, smem, dev, info, st);
+        case 2: return launch_stream<KIND, 2>(a, smem, dev, info, st);
+        case 3: return launch_stream<KIND, 3>(a, smem, dev, info, st);
+        case 4: return launch_stream<KIND, 4>(a, smem, dev, info, st);
+        case 5: return launch_stream<KIND, 5>(a, smem, dev, info, st);
+        case 6: return launch_stream<KIND, 6>(a, smem, dev, info, st);
+        case 7: return launch_stream<KIND, 7>(a, smem, dev, info, st);
+        default: return launch_stream<KIND, 8>(a, smem, dev, info, st);
+    }
+}
+
+template <int KIND>
+int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float *d, float *y,
+               int64_t out_f, int64_t in_f, int m, void *stream) {
+    if (m < 1 || m > MEMQ_MAX_M) return MEMQ_ERR_M_RANGE;
+    if (in_f < 32 || (in_f % 32) != 0 || in_f > (1LL << 24)) return MEMQ_ERR_SHAPE;
+    if (out_f < 0 || out_f > (1LL << 31) - 1) return MEMQ_ERR_SHAPE;
+    if (out_f == 0) return MEMQ_OK;  // empty output: nothing to read or write, pointers unused
+    if (!w || !qs || !d || !y || (KIND != kQ80 && !aux)) return MEMQ_ERR_NULL;
+    if (!aligned(d, 4) || !aligned(y, 4) || (aux && !aligned(aux, 4))) return MEMQ_ERR_ALIGN;
+
+    int dev = 0;
+    DeviceInfo info;
+    if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const int nb = static_cast<int>(in_f / 32);
+    const int64_t row_bytes = (KIND == kQ80) ? static_cast<int64_t>(nb) * 34 : in_f;
+    using G = Geo<KIND>;
+
+    // Fast-path eligibility and shared-memory plan: barriers, two tile-partial buffers, and
+    // kWarps rings of S stages.
+    bool fast = aligned(w, 16) && aligned(qs, KIND == kQ80 ? 16 : 8) && (row_bytes % 16) == 0 &&
+                (KIND != kQ80 || (nb % 8) == 0);
+    StreamArgs a = {};
+    uint32_t smem = 0;
+    if (fast) {
+        const uint32_t part = align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128);
+        int S = kStages;
+        for (; S >= 2; --S) {
+            const uint32_t bars = align_up(static_cast<uint32_t>(kWarps * S * 8), 128);
+            smem = bars + part + static_cast<uint32_t>(kWarps * S * G::kStage);
+            if (smem <= static_cast<uint32_t>(info.smem_optin)) break;
+        }
+        if (S < 2) {
+            fast = false;
+        } else {
+            a.stages = S;
+            a.off_part = align_up(static_cast<uint32_t>(kWarps * S * 8), 128);
+            a.off_ring = a.off_part + part;
+        }
+    }
+
+    cudaError_t e;
+    if (fast) {
+        a.w = w;
+        a.aux = aux;
+        a.qs = qs;
+        a.d = d;
+        a.y = y;
+        a.out_f = out_f;
+        a.row_bytes = row_bytes;
+        a.in_f = static_cast<int>(in_f);
+        a.nb = nb;
+        a.gcols = static_cast<int>((in_f + 127) / 128);
+        e = launch_stream_m<KIND>(m, a, smem, dev, info, st);
+    } else {
+        const int64_t blocks = (out_f + kWarps - 1) / kWarps;
+        gemv_generic_kernel<KIND><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(
+            w, aux, qs, d, y, out_f, static_cast<int>(in_f), m);
+        e = cudaGetLastError();
+    }
+    return e == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace memq
+
+extern "C" int memq_gemv_e4m3(const uint8_t *w, const float *w_scale, const int8_t *qs,
+                              const float *d, float *y, int64_t out_f, int64_t in_f, int m,
+                              void *stream) {
+    return memq::gemv_entry<memq::kE4M3>(w, w_scale, qs, d, y, out_f, in_f, m, stream);
+}
+
+extern "C" int memq_gemv_e4m3_blk128(const uint8_t *w, const float *grid, const int8_t *qs,
+                                     const float *d, float *y, int64_t out_f, int64_t in_f, int m,
+                                     void *stream) {
+    return memq::gemv_entry<memq::kBlk>(w, grid, qs, d, y, out_f, in_f, m, stream);
+}
+
+extern "C" int memq_gemv_q8_0(const void *w, const int8_t *qs, const float *d, float *y,
+                              int64_t out_f, int64_t in_f, int m, void *stream) {
+    return memq::gemv_entry<memq::kQ80>(static_cast<const uint8_t *>(w), nullptr, qs, d, y, out_f,
+                                        in_f, m, stream);
+}
+
+extern "C" int memq_device_fault(void *stream, uint32_t *fault_out) {
+    if (!fault_out) return MEMQ_ERR_NULL;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MEMQ_ERR_DEVICE;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, memq::g_memq_fault, sizeof(v)) != cudaSuccess) return MEMQ_ERR_DEVICE;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(memq::g_memq_fault, &zero, sizeof(zero)) != cudaSuccess) return MEMQ_ERR_DEVICE;
+    *fault_out = v;
+    return MEMQ_OK;
+}
+
+extern "C" const char *memq_status_string(int status) {
+    switch (status) {
+        case MEMQ_OK: return "ok";
+        case MEMQ_ERR_NULL: return "a required pointer is NULL";
+        case MEMQ_ERR_SHAPE: return "a size is out of range or not a multiple of 32";
+        case MEMQ_ERR_ALIGN: return "a pointer breaks its documented alignment";
+        case MEMQ_ERR_M_RANGE: return "m is outside [1, 8]";
+        case MEMQ_ERR_LAUNCH: return "the CUDA launch failed";
+        case MEMQ_ERR_DEVICE: return "the device fault word could not be read";
+        default: return "unknown memq status";
+    }
+}
+
+extern "C" int memq_version(void) { return (1 << 16) | 0; }

@@ -1,0 +1,79 @@
+"""The C ABI library on the CPU: it loads, exports every entry point the headers declare, and
+rejects bad arguments before touching CUDA.  No compute call is made here."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_decode_memq_gb300 import build
+    try:
+        build.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+    import quantized_decode_memq_gb300 as m
+    return m.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(memq_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
+                     "memq_gemv_q8_0", "memq_status_string", "memq_device_fault",
+                     "memq_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    import quantized_decode_memq_gb300 as m
+    assert m.memq_status_string(0) == "ok"
+    for s in m.Status:
+        assert m.memq_status_string(int(s))
+    assert m.memq_status_string(99) == "unknown memq status"
+    assert m.memq_version() >> 16 == 1
+
+
+def test_validation_rejects_before_any_cuda_call(lib):
+    import quantized_decode_memq_gb300 as m
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: every call below fails validation first
+    assert lib.memq_gemv_e4m3(None, fake, fake, fake, fake, 4, 64, 1, None) == m.Status.ERR_NULL
+    assert lib.memq_gemv_e4m3(fake, fake, fake, fake, fake, 4, 64, 0, None) == m.Status.ERR_M_RANGE
+    assert lib.memq_gemv_e4m3_blk128(fake, fake, fake, fake, fake, 4, 40, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_gemv_q8_0(fake, fake, fake, fake, -3, 64, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_gemv_q8_0(fake, fake, P(0x1002), fake, 4, 64, 1, None) == m.Status.ERR_ALIGN
+    assert lib.memq_rmsnorm_q8_1(fake, fake, None, fake, fake, 33, 1, 1e-6, None) == m.Status.ERR_SHAPE
+    assert lib.memq_rmsnorm_q8_1(fake, None, None, fake, fake, 64, 1, 1e-6, None) == m.Status.ERR_NULL
+    assert lib.memq_rmsnorm_q8_1(P(0x1004), fake, None, fake, fake, 64, 1, 1e-6, None) == m.Status.ERR_ALIGN
+    # empty problems are valid no-ops and launch nothing, even with NULL pointers
+    assert lib.memq_rmsnorm_q8_1(None, None, None, None, None, 64, 0, 1e-6, None) == m.Status.OK
+    assert lib.memq_gemv_q8_0(None, None, None, None, 0, 64, 1, None) == m.Status.OK
+    assert lib.memq_device_fault(None, None) == m.Status.ERR_NULL
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import quantized_decode_memq_gb300._binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        b.lib()
