@@ -48,14 +48,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Waits for phase `parity` of `bar` to complete; the thread is suspended (not spinning) until
+// the phase completes or about 1 ms passes, whichever comes first.  Returns whether it completed.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
@@ -98,30 +100,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 }
 
 // ---------------------------------------------------------------------------------------------
-// Shared-memory loads
+// Shared-memory loads.  Plain C++ loads (not volatile asm), so the compiler can interleave
+// independent blocks while still ordering them after the barrier waits, which clobber memory.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint4 lds128(const void *p) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(smem_u32(p)));
-    return v;
-}
-__device__ __forceinline__ uint2 lds64(const void *p) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32(const void *p) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds16(const void *p) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)));
-    return v;
-}
+__device__ __forceinline__ uint4 lds128(const void *p) { return *static_cast<const uint4 *>(p); }
+__device__ __forceinline__ uint2 lds64(const void *p) { return *static_cast<const uint2 *>(p); }
+__device__ __forceinline__ uint32_t lds32(const void *p) { return *static_cast<const uint32_t *>(p); }
+__device__ __forceinline__ uint32_t lds16(const void *p) { return *static_cast<const uint16_t *>(p); }
 
 // ---------------------------------------------------------------------------------------------
 // Numeric helpers
@@ -133,6 +118,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     uint32_t out;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(static_cast<unsigned short>(two_codes)));
     return out;
+}
+
+// Four E4M3 codes (one 32-bit word, low byte first) -> f16x2 {c0,c1} and {c2,c3}; the word is
+// split into its two 16-bit halves inside PTX so no shift or mask is needed.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w4, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w4));
 }
 
 // Four int8 (one 32-bit word, low byte first) -> two f16x2 {q0,q1}, {q2,q3}, exactly: each byte
@@ -152,8 +148,7 @@ __device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t q4, uint32_t &lo, uint3
 __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
                                               uint32_t a2, uint32_t a3, uint32_t b0,
                                               uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));

@@ -6,7 +6,7 @@
 //
 // Fast path ("stream" kernel), one skeleton for all three containers:
 //   * CTA c owns output rows [R0, R1), an equal share (+-1 row) of out_f, so every SM streams
-//     the same number of weight bytes.  Its rows are processed in tiles; the K dimension of
+//     the same number of weight bytes (two CTAs of 8 warps per SM).  Its rows are processed in tiles; the K dimension of
 //     every tile is split into 8 equal slices, one per warp, so all warps stream every tile.
 //   * Each warp runs its own S-stage ring of shared-memory slots.  A stage is one chunk of the
 //     warp's K slice for all rows of the tile, filled with one 1-D bulk asynchronous copy
@@ -19,8 +19,9 @@
 //     (programmatic dependent launch); the activation is read only after that wait.
 //   * E4M3 / block-128 inner product on the tensor cores (mma.sync m16n8k16, f16 operands,
 //     f32 accumulation).  E4M3 -> f16 (hardware cvt) and int8 -> f16 are exact and f16 x f16
-//     products are exact in f32, so this is numerically an f32 dot product; the instruction
-//     count per weight is ~5x lower than CUDA-core FMAs, which left the kernel issue-bound.
+//     products are exact in f32, so this is numerically an f32 dot product.  A CUDA-core FMA
+//     version of this loop was measured issue-bound (61% issue-active at 35% of DRAM
+//     bandwidth); the MMA form needs a fraction of the instructions per weight.
 //   * Q8_0 inner product with dp4a (exact int32 dot of 32 int8 pairs) on 4-row tiles.
 // Generic path: a plain warp-per-row kernel with byte loads for anything the fast path does not
 // take (unaligned pointers, Q8_0 rows that are not 16-byte aligned).
@@ -42,24 +43,25 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;  // ring depth per warp (reduced if shared memory runs short)
 
 enum Kind : int { kE4M3 = 0, kBlk = 1, kQ80 = 2 };
 
 // Stream-kernel geometry per container.
-//   E4M3 / block-128 (tensor-core inner product): a tile is 32 rows (two m16 MMA row tiles), a
+//   E4M3 / block-128 (tensor-core inner product): a tile is 16 rows (one m16 MMA row tile), a
 //   stage holds 4 blocks (128 weights) of every tile row, each row slot padded to 144 bytes so
 //   the 8-byte fragment loads of 8 different rows hit 8 different bank groups.
 //   Q8_0 (dp4a inner product): a tile is 4 rows, a stage holds 32 blocks (1088 bytes) per row,
 //   lane l owns block l.
+// Both rings are sized so that two 8-warp CTAs fit on one SM (16 warps, ~100 KB in flight).
 template <int KIND>
 struct Geo {
     static constexpr bool kMma = KIND != kQ80;
     static constexpr int kBlockBytes = kMma ? 32 : 34;
-    static constexpr int kTileRows = kMma ? 32 : 4;
+    static constexpr int kTileRows = kMma ? 16 : 4;
     static constexpr int kChunkBlocks = kMma ? 4 : 32;
     static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
     static constexpr int kStage = kTileRows * kSlot;
+    static constexpr int kStages = kMma ? 4 : 3;
     static constexpr int kSliceQuantum = kMma ? 1 : 8;  // K-slice granularity in blocks
 };
 
@@ -75,7 +77,7 @@ struct StreamArgs {
     int nb;     // in_f / 32
     int gcols;  // ceil(in_f / 128)
     int stages;
-    uint32_t off_part, off_ring;  // shared-memory layout (bytes); barriers at offset 0
+    uint32_t off_part, off_bfrag, off_ring;  // shared-memory layout (bytes); barriers at 0
 };
 
 __device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bit); }
@@ -83,66 +85,75 @@ __device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bi
 // ---------------------------------------------------------------------------------------------
 // E4M3 / block-128 stage: tensor-core inner products.
 //
-// Per 32-weight block and 16-row tile, two m16n8k16 MMAs with A = 16 weight rows (E4M3 decoded
-// to f16 by the hardware cvt) and B = the q8_1 activation of up to 8 tokens (int8 -> f16),
-// accumulating in f32; the 16x8 block result is then scaled by d[token][block] (and the grid
-// entry) into f32 accumulators.  The dot product is order-free, so the K index inside a block is
-// permuted: thread (g, t) = (lane/4, lane%4) supplies physical columns 8t..8t+7 of its rows for
-// MMA slots {2t, 2t+1, 2t+8, 2t+9} (first MMA: 8t..8t+3, second: 8t+4..8t+7), and the B
-// fragment of token g uses exactly the same map.
-// acc[tt][0..3] = rows (tt*16+g, tt*16+g+8) x tokens (2t, 2t+1).
+// Per 32-weight block, two m16n8k16 MMAs with A = the tile's 16 weight rows (E4M3 decoded to
+// f16 by the hardware cvt) and B = the q8_1 activation of up to 8 tokens (int8 -> f16), both
+// exact, accumulating in f32; the 16x8 block result is then scaled by d[token][block] (and the
+// grid entry) into f32 accumulators.  The dot product is order-free, so the K index inside a
+// block is permuted: thread (g, t) = (lane/4, lane%4) supplies physical columns 8t..8t+7 of its
+// rows for MMA slots {2t, 2t+1, 2t+8, 2t+9} (first MMA: 8t..8t+3, second: 8t+4..8t+7), and the
+// B fragment of token g uses exactly the same map.  The B fragments come precomputed from
+// shared memory (PRE_B) or are converted from the int8 activation in global memory.
+// acc[0..3] = rows (g, g+8) x tokens (2t, 2t+1) of the tile.
 // ---------------------------------------------------------------------------------------------
-template <int KIND, int M>
+template <int KIND, int M, bool PRE_B, bool FULL>
 __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *stage,
-                                          int64_t row0, int64_t row_last, int kb0, int nblk,
-                                          int lane, float (&acc)[2][4]) {
+                                          const uint4 *bfrag, int64_t row0, int64_t row_last,
+                                          int kb0, int nblk, int lane, float (&acc)[4]) {
     using G = Geo<KIND>;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const float *grow[4] = {nullptr, nullptr, nullptr, nullptr};
+    const float *grow0 = nullptr, *grow8 = nullptr;
     if (KIND == kBlk) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {  // rows g, g+8, 16+g, 24+g of the tile (clamped)
-            int64_t r = row0 + (i >> 1) * 16 + (i & 1) * 8 + g;
-            r = r > row_last ? row_last : r;
-            grow[i] = a.aux + (r >> 7) * a.gcols;
-        }
+        const int64_t r0 = row0 + g > row_last ? row_last : row0 + g;
+        const int64_t r8 = row0 + g + 8 > row_last ? row_last : row0 + g + 8;
+        grow0 = a.aux + (r0 >> 7) * a.gcols;
+        grow8 = a.aux + (r8 >> 7) * a.gcols;
     }
-#pragma unroll 1
-    for (int b = 0; b < nblk; ++b) {
-        const int kb = kb0 + b;
-        uint32_t bq[4] = {0u, 0u, 0u, 0u};
-        if (g < M) {
-            const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(
-                a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
-            s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
-            s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
-        }
-        const float dx0 = (2 * t < M) ? __ldg(a.d + (2 * t) * a.nb + kb) : 0.f;
-        const float dx1 = (2 * t + 1 < M) ? __ldg(a.d + (2 * t + 1) * a.nb + kb) : 0.f;
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
-            const uint8_t *pa = stage + (tt * 16 + g) * G::kSlot + 32 * b + 8 * t;
-            const uint2 wa = lds64(pa);
-            const uint2 wb = lds64(pa + 8 * G::kSlot);
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_f16_16816(c, e4m3x2_to_f16x2(wa.x & 0xffffu), e4m3x2_to_f16x2(wb.x & 0xffffu),
-                          e4m3x2_to_f16x2(wa.x >> 16), e4m3x2_to_f16x2(wb.x >> 16), bq[0], bq[1]);
-            mma_f16_16816(c, e4m3x2_to_f16x2(wa.y & 0xffffu), e4m3x2_to_f16x2(wb.y & 0xffffu),
-                          e4m3x2_to_f16x2(wa.y >> 16), e4m3x2_to_f16x2(wb.y >> 16), bq[2], bq[3]);
-            float k0 = dx0, k1 = dx1, k2 = dx0, k3 = dx1;
+    for (int b = 0; b < G::kChunkBlocks; ++b) {
+        if (FULL || b < nblk) {
+            const int kb = kb0 + b;
+            uint32_t bq[4] = {0u, 0u, 0u, 0u};
+            if (g < M) {
+                if (PRE_B) {
+                    const uint4 v = bfrag[(kb * M + g) * 4 + t];
+                    bq[0] = v.x;
+                    bq[1] = v.y;
+                    bq[2] = v.z;
+                    bq[3] = v.w;
+                } else {
+                    const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(
+                        a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+                    s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
+                    s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
+                }
+            }
+            float k0 = (2 * t < M) ? __ldg(a.d + (2 * t) * a.nb + kb) : 0.f;
+            float k1 = (2 * t + 1 < M) ? __ldg(a.d + (2 * t + 1) * a.nb + kb) : 0.f;
+            float k2 = k0, k3 = k1;
             if (KIND == kBlk) {
-                const float gg = __ldg(grow[2 * tt] + (kb >> 2));
-                const float gg8 = __ldg(grow[2 * tt + 1] + (kb >> 2));
+                const float gg = __ldg(grow0 + (kb >> 2));
+                const float gg8 = __ldg(grow8 + (kb >> 2));
                 k0 *= gg;
                 k1 *= gg;
                 k2 *= gg8;
                 k3 *= gg8;
             }
-            acc[tt][0] = fmaf(c[0], k0, acc[tt][0]);
-            acc[tt][1] = fmaf(c[1], k1, acc[tt][1]);
-            acc[tt][2] = fmaf(c[2], k2, acc[tt][2]);
-            acc[tt][3] = fmaf(c[3], k3, acc[tt][3]);
+            const uint8_t *pa = stage + g * G::kSlot + 32 * b + 8 * t;
+            const uint2 wa = lds64(pa);
+            const uint2 wb = lds64(pa + 8 * G::kSlot);
+            uint32_t a0, a1, a2, a3;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            e4m3x4_to_f16x2x2(wa.x, a0, a2);
+            e4m3x4_to_f16x2x2(wb.x, a1, a3);
+            mma_f16_16816(c, a0, a1, a2, a3, bq[0], bq[1]);
+            e4m3x4_to_f16x2x2(wa.y, a0, a2);
+            e4m3x4_to_f16x2x2(wb.y, a1, a3);
+            mma_f16_16816(c, a0, a1, a2, a3, bq[2], bq[3]);
+            acc[0] = fmaf(c[0], k0, acc[0]);
+            acc[1] = fmaf(c[1], k1, acc[1]);
+            acc[2] = fmaf(c[2], k2, acc[2]);
+            acc[3] = fmaf(c[3], k3, acc[3]);
         }
     }
 }
@@ -203,8 +214,8 @@ __device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *st
 // ---------------------------------------------------------------------------------------------
 // The stream kernel (see the file header for the schedule).
 // ---------------------------------------------------------------------------------------------
-template <int KIND, int M>
-__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const StreamArgs a) {
+template <int KIND, int M, bool PRE_B>
+__global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamArgs a) {
     using G = Geo<KIND>;
     constexpr int TR = G::kTileRows;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -228,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const StreamAr
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
     uint8_t *ring = smem + a.off_ring + static_cast<size_t>(warp) * S * G::kStage;
     float *part = reinterpret_cast<float *>(smem + a.off_part);  // [2][kWarps][TR][M]
+    uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);  // [nb][M][4] (PRE_B)
 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -263,6 +275,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const StreamAr
     griddep_wait();
     float scale = 1.0f;
     if (KIND == kE4M3) scale = __ldg(a.aux);
+    if (PRE_B) {
+        // f16 MMA B fragments of the whole activation, once per CTA: entry (kb, g, t) holds
+        // q[g][32kb + 8t .. 8t+7] as four f16x2 registers.
+        const int n = a.nb * M * 4;
+        for (int i = threadIdx.x; i < n; i += kThreads) {
+            const int t = i & 3;
+            const int g = (i >> 2) % M;
+            const int kb = (i >> 2) / M;
+            const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(
+                a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+            uint4 v;
+            s8x4_to_f16x2x2(qv.x, v.x, v.y);
+            s8x4_to_f16x2x2(qv.y, v.z, v.w);
+            bfrag[i] = v;
+        }
+        __syncthreads();
+    }
 
     bool ok = true;
     int c_stage = 0;
@@ -271,12 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const StreamAr
     for (int tile = 0; tile < ntiles; ++tile) {
         const int64_t r0 = R0 + static_cast<int64_t>(tile) * TR;
         const int rc = static_cast<int>(R1 - r0 < TR ? R1 - r0 : TR);
-        float acc_m[2][4];
+        float acc_m[4] = {0.f, 0.f, 0.f, 0.f};
         float acc_q[4][M];
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc_m[i][j] = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -302,9 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const StreamAr
                 const int kb = kb_lo + ch * G::kChunkBlocks;
                 const int nblk = min(G::kChunkBlocks, kb_hi - kb);
                 const uint8_t *stage = ring + c_stage * G::kStage;
-                if (G::kMma)
-                    mma_stage<KIND, M>(a, stage, r0, R1 - 1, kb, nblk, lane, acc_m);
-                else
+                if (G::kMma) {
+                    if (nblk == G::kChunkBlocks)
+                        mma_stage<KIND, M, PRE_B, true>(a, stage, bfrag, r0, R1 - 1, kb, nblk, lane, acc_m);
+                    else
+                        mma_stage<KIND, M, PRE_B, false>(a, stage, bfrag, r0, R1 - 1, kb, nblk, lane, acc_m);
+                } else
                     q80_stage<M>(a, stage, rc, kb, nblk, lane, acc_q);
                 __syncwarp();
                 ++consumed;
@@ -320,17 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const StreamAr
         float *pw = part + ((tile & 1) * kWarps + warp) * TR * M;
         if (G::kMma) {
             const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-                const int ra = tt * 16 + g, rb = ra + 8;
-                if (2 * t < M) {
-                    pw[ra * M + 2 * t] = acc_m[tt][0];
-                    pw[rb * M + 2 * t] = acc_m[tt][2];
-                }
-                if (2 * t + 1 < M) {
-                    pw[ra * M + 2 * t + 1] = acc_m[tt][1];
-                    pw[rb * M + 2 * t + 1] = acc_m[tt][3];
-                }
+            if (2 * t < M) {
+                pw[g * M + 2 * t] = acc_m[0];
+                pw[(g + 8) * M + 2 * t] = acc_m[2];
+            }
+            if (2 * t + 1 < M) {
+                pw[g * M + 2 * t + 1] = acc_m[1];
+                pw[(g + 8) * M + 2 * t + 1] = acc_m[3];
             }
         } else {
 #pragma unroll
@@ -406,13 +430,14 @@ __global__ void __launch_bounds__(kThreads)
 // ---------------------------------------------------------------------------------------------
 struct DeviceInfo {
     int sms = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;  // per CTA
+    int smem_sm = 0;     // per SM
 };
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
-std::atomic<uint32_t> g_attr_set[kMaxDevices][3];  // bit (M-1) per kind: max-smem attribute set
+std::atomic<uint32_t> g_attr_set[kMaxDevices][3];  // bit per (M, PRE_B): attribute set
 
 bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -427,6 +452,8 @@ cudaError_t device_info(int &dev, DeviceInfo &info) {
         err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (err == cudaSuccess)
             err = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (err == cudaSuccess)
+            err = cudaDeviceGetAttribute(&di.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         if (err == cudaSuccess) g_dev[dev] = di;
     });
     if (err != cudaSuccess) return err;
@@ -434,11 +461,11 @@ cudaError_t device_info(int &dev, DeviceInfo &info) {
     return info.sms > 0 ? cudaSuccess : cudaErrorInvalidDevice;
 }
 
-template <int KIND, int M>
+template <int KIND, int M, bool PRE_B>
 cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const DeviceInfo &info,
                           cudaStream_t st) {
-    auto kern = gemv_stream_kernel<KIND, M>;
-    const uint32_t bit = 1u << (M - 1);
+    auto kern = gemv_stream_kernel<KIND, M, PRE_B>;
+    const uint32_t bit = 1u << ((M - 1) + (PRE_B ? 8 : 0));
     if (!(g_attr_set[dev][KIND].load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              info.smem_optin);
@@ -465,18 +492,18 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int KIND>
+template <int KIND, bool PRE_B>
 cudaError_t launch_stream_m(int m, StreamArgs a, uint32_t smem, int dev, const DeviceInfo &info,
                             cudaStream_t st) {
     switch (m) {
-        case 1: return launch_stream<KIND, 1>(a, smem, dev, info, st);
-        case 2: return launch_stream<KIND, 2>(a, smem, dev, info, st);
-        case 3: return launch_stream<KIND, 3>(a, smem, dev, info, st);
-        case 4: return launch_stream<KIND, 4>(a, smem, dev, info, st);
-        case 5: return launch_stream<KIND, 5>(a, smem, dev, info, st);
-        case 6: return launch_stream<KIND, 6>(a, smem, dev, info, st);
-        case 7: return launch_stream<KIND, 7>(a, smem, dev, info, st);
-        default: return launch_stream<KIND, 8>(a, smem, dev, info, st);
+        case 1: return launch_stream<KIND, 1, PRE_B>(a, smem, dev, info, st);
+        case 2: return launch_stream<KIND, 2, PRE_B>(a, smem, dev, info, st);
+        case 3: return launch_stream<KIND, 3, PRE_B>(a, smem, dev, info, st);
+        case 4: return launch_stream<KIND, 4, PRE_B>(a, smem, dev, info, st);
+        case 5: return launch_stream<KIND, 5, PRE_B>(a, smem, dev, info, st);
+        case 6: return launch_stream<KIND, 6, PRE_B>(a, smem, dev, info, st);
+        case 7: return launch_stream<KIND, 7, PRE_B>(a, smem, dev, info, st);
+        default: return launch_stream<KIND, 8, PRE_B>(a, smem, dev, info, st);
     }
 }
 
@@ -499,26 +526,37 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
     const int64_t row_bytes = (KIND == kQ80) ? static_cast<int64_t>(nb) * 34 : in_f;
     using G = Geo<KIND>;
 
-    // Fast-path eligibility and shared-memory plan: barriers, two tile-partial buffers, and
-    // kWarps rings of S stages.
+    // Fast-path eligibility and shared-memory plan: barriers, two tile-partial buffers, the
+    // precomputed B fragments (E4M3 / block-128, when they still leave room for two CTAs per
+    // SM), and kWarps rings of S stages.
     bool fast = aligned(w, 16) && aligned(qs, KIND == kQ80 ? 16 : 8) && (row_bytes % 16) == 0 &&
                 (KIND != kQ80 || (nb % 8) == 0);
     StreamArgs a = {};
     uint32_t smem = 0;
+    bool pre_b = false;
     if (fast) {
+        const uint32_t two_per_sm = static_cast<uint32_t>(info.smem_sm / 2 - 1024);
         const uint32_t part = align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128);
-        int S = kStages;
+        const uint32_t bfrag = G::kMma ? align_up(static_cast<uint32_t>(nb * m * 64), 128) : 0u;
+        int S = G::kStages;
+        uint32_t bars = 0, ring = 0;
         for (; S >= 2; --S) {
-            const uint32_t bars = align_up(static_cast<uint32_t>(kWarps * S * 8), 128);
-            smem = bars + part + static_cast<uint32_t>(kWarps * S * G::kStage);
-            if (smem <= static_cast<uint32_t>(info.smem_optin)) break;
+            bars = align_up(static_cast<uint32_t>(kWarps * S * 8), 128);
+            ring = static_cast<uint32_t>(kWarps * S * G::kStage);
+            if (bars + part + ring <= static_cast<uint32_t>(info.smem_optin)) break;
         }
         if (S < 2) {
             fast = false;
         } else {
+            const uint32_t base = bars + part + ring;
+            pre_b = G::kMma && bfrag > 0 &&
+                    (base + bfrag <= two_per_sm ||
+                     (base > two_per_sm && base + bfrag <= static_cast<uint32_t>(info.smem_optin)));
             a.stages = S;
-            a.off_part = align_up(static_cast<uint32_t>(kWarps * S * 8), 128);
-            a.off_ring = a.off_part + part;
+            a.off_part = bars;
+            a.off_bfrag = bars + part;
+            a.off_ring = a.off_bfrag + (pre_b ? bfrag : 0u);
+            smem = a.off_ring + ring;
         }
     }
 
@@ -534,7 +572,12 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
         a.in_f = static_cast<int>(in_f);
         a.nb = nb;
         a.gcols = static_cast<int>((in_f + 127) / 128);
-        e = launch_stream_m<KIND>(m, a, smem, dev, info, st);
+        if constexpr (G::kMma) {
+            e = pre_b ? launch_stream_m<KIND, true>(m, a, smem, dev, info, st)
+                      : launch_stream_m<KIND, false>(m, a, smem, dev, info, st);
+        } else {
+            e = launch_stream_m<KIND, false>(m, a, smem, dev, info, st);
+        }
     } else {
         const int64_t blocks = (out_f + kWarps - 1) / kWarps;
         gemv_generic_kernel<KIND><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(
