@@ -6,23 +6,26 @@
 //
 // Fast path ("stream" kernel), one skeleton for all three containers:
 //   * CTA c owns output rows [R0, R1), an equal share (+-1 row) of out_f, so every SM streams
-//     the same number of weight bytes (two CTAs of 8 warps per SM).  Its rows are processed in tiles; the K dimension of
-//     every tile is split into 8 equal slices, one per warp, so all warps stream every tile.
-//   * Each warp runs its own S-stage ring of shared-memory slots.  A stage is one chunk of the
-//     warp's K slice for all rows of the tile, filled with one 1-D bulk asynchronous copy
-//     (cp.async.bulk, L2 evict-first) per row, issued by lanes 0..rows-1 and completing on the
-//     stage's mbarrier; the warp waits on it (bounded), computes, and refills the slot.
-//   * At the end of a tile every warp leaves its partial sums in shared memory; after one CTA
-//     barrier the 8 partials of each (row, token) are added in warp order (deterministic) and
-//     stored.  Partial buffers alternate between tiles, so one barrier per tile suffices.
-//   * Weight copies for the first S stages are issued before waiting on the preceding launch
-//     (programmatic dependent launch); the activation is read only after that wait.
-//   * E4M3 / block-128 inner product on the tensor cores (mma.sync m16n8k16, f16 operands,
-//     f32 accumulation).  E4M3 -> f16 (hardware cvt) and int8 -> f16 are exact and f16 x f16
-//     products are exact in f32, so this is numerically an f32 dot product.  A CUDA-core FMA
-//     version of this loop was measured issue-bound (61% issue-active at 35% of DRAM
-//     bandwidth); the MMA form needs a fraction of the instructions per weight.
-//   * Q8_0 inner product with dp4a (exact int32 dot of 32 int8 pairs) on 4-row tiles.
+//     the same number of weight bytes.  The CTA walks its rows tile by tile and each tile's K
+//     dimension chunk by chunk (32 blocks = 1 KB of E4M3, 1088 B of Q8_0, per row).
+//   * One producer warp fills a shared ring of S stages: a stage is one chunk of every row of
+//     the tile, loaded with one 1-D bulk asynchronous copy (cp.async.bulk, L2 evict-first) per
+//     row that completes on the stage's "full" mbarrier.  Eight consumer warps wait on it
+//     (bounded), compute, and release the stage on its "empty" mbarrier.  Copies are 1 KB each:
+//     the bulk-copy instruction is issued per row, so large rows pieces keep its cost per byte
+//     low.
+//   * E4M3 / block-128: 16-row tiles; consumer warp w takes blocks 4w..4w+3 of every stage and
+//     computes them on the tensor cores (mma.sync m16n8k16, f16 operands, f32 accumulation):
+//     E4M3 -> f16 (hardware cvt) and int8 -> f16 are exact and f16 x f16 products are exact in
+//     f32, so this is numerically an f32 dot product.  At the end of a tile each warp leaves its
+//     partial sums in shared memory; after one barrier among the consumers the 8 partials of each
+//     (row, token) are added in warp order (deterministic) and stored.  (A CUDA-core FMA version
+//     of this loop measured issue-bound: 61% issue-active at 35% of DRAM bandwidth.)
+//   * Q8_0: 8-row tiles; consumer warp w owns row w of the tile, lane l owns block l of every
+//     stage, and dp4a gives the exact int32 dot product of each block.
+//   * The producer never reads what the preceding launch writes, so it starts streaming at once;
+//     the consumers wait for the preceding launch (programmatic dependent launch) before they
+//     read the activation.
 // Generic path: a plain warp-per-row kernel with byte loads for anything the fast path does not
 // take (unaligned pointers, Q8_0 rows that are not 16-byte aligned).
 #include <algorithm>
@@ -41,28 +44,27 @@ __device__ unsigned int g_memq_fault = 0;
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 8;                    // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
+constexpr int kConsumerThreads = kWarps * 32;
+constexpr int kBarConsumers = 1;             // named barrier id used by the consumer warps
 
 enum Kind : int { kE4M3 = 0, kBlk = 1, kQ80 = 2 };
 
-// Stream-kernel geometry per container.
-//   E4M3 / block-128 (tensor-core inner product): a tile is 16 rows (one m16 MMA row tile), a
-//   stage holds 4 blocks (128 weights) of every tile row, each row slot padded to 144 bytes so
-//   the 8-byte fragment loads of 8 different rows hit 8 different bank groups.
-//   Q8_0 (dp4a inner product): a tile is 4 rows, a stage holds 32 blocks (1088 bytes) per row,
-//   lane l owns block l.
-// Both rings are sized so that two 8-warp CTAs fit on one SM (16 warps, ~100 KB in flight).
+// Stream-kernel geometry per container.  A stage holds 32 blocks of every tile row.
+//   E4M3 / block-128: 16-row tiles (one m16 MMA row tile); row slots padded to 1040 bytes so the
+//   8-byte fragment loads of 8 different rows fall in distinct bank groups.
+//   Q8_0: 8-row tiles, 1088-byte row slots (34-byte blocks).
 template <int KIND>
 struct Geo {
     static constexpr bool kMma = KIND != kQ80;
     static constexpr int kBlockBytes = kMma ? 32 : 34;
-    static constexpr int kTileRows = kMma ? 16 : 4;
-    static constexpr int kChunkBlocks = kMma ? 4 : 32;
+    static constexpr int kTileRows = kMma ? 16 : 8;
+    static constexpr int kChunkBlocks = 32;
     static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
     static constexpr int kStage = kTileRows * kSlot;
-    static constexpr int kStages = kMma ? 4 : 3;
-    static constexpr int kSliceQuantum = kMma ? 1 : 8;  // K-slice granularity in blocks
+    static constexpr int kStages = 4;
+    static constexpr int kWarpBlocks = kChunkBlocks / kWarps;  // E4M3: blocks per warp per stage
 };
 
 struct StreamArgs {
@@ -110,7 +112,7 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
         grow8 = a.aux + (r8 >> 7) * a.gcols;
     }
 #pragma unroll
-    for (int b = 0; b < G::kChunkBlocks; ++b) {
+    for (int b = 0; b < G::kWarpBlocks; ++b) {
         if (FULL || b < nblk) {
             const int kb = kb0 + b;
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
@@ -159,61 +161,65 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
 }
 
 // ---------------------------------------------------------------------------------------------
-// Q8_0 stage: lane l owns block l of the stage for each of the tile's 4 rows.  The block's 32
-// weights start 2 bytes into a 34-byte record, so they are re-aligned from 4-byte shared loads
-// with funnel shifts, then dp4a gives the exact int32 dot product with the activation block.
+// Q8_0 stage: the warp's row, lane l owns block l.  The block's 32 weights start 2 bytes into a
+// 34-byte record, so they are re-aligned from 4-byte shared loads with funnel shifts; dp4a then
+// gives the exact int32 dot product with the activation block.
 // ---------------------------------------------------------------------------------------------
 template <int M>
-__device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *stage, int rc,
-                                          int kb0, int nblk, int lane, float (&acc)[4][M]) {
-    using G = Geo<kQ80>;
+__device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *slot, int kb0,
+                                          int nblk, int lane, float (&acc)[M]) {
     if (lane >= nblk) return;
     const int kb = kb0 + lane;
-    uint32_t qw[4][8];
-    float dw[4];
     const int qstart = 34 * lane + 2;
     const int abase = qstart & ~3;
     const uint32_t sh = static_cast<uint32_t>(qstart & 3) * 8u;  // 0 or 16
+    uint32_t wv[9];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-        if (rr < rc) {
-            const uint8_t *slot = stage + rr * G::kSlot;
-            uint32_t wv[9];
+    for (int i = 0; i < 8; ++i) wv[i] = lds32(slot + abase + 4 * i);
+    wv[8] = sh ? lds32(slot + abase + 32) : 0u;
+    uint32_t qw[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) wv[i] = lds32(slot + abase + 4 * i);
-            wv[8] = sh ? lds32(slot + abase + 32) : 0u;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) qw[rr][i] = __funnelshift_r(wv[i], wv[i + 1], sh);
-            dw[rr] = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(slot + 34 * lane))));
-        }
-    }
+    for (int i = 0; i < 8; ++i) qw[i] = __funnelshift_r(wv[i], wv[i + 1], sh);
+    const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(slot + 34 * lane))));
 #pragma unroll
     for (int j = 0; j < M; ++j) {
         const uint4 *qx = reinterpret_cast<const uint4 *>(a.qs + static_cast<int64_t>(j) * a.in_f + 32 * kb);
         const uint4 x0 = __ldg(qx);
         const uint4 x1 = __ldg(qx + 1);
         const float dj = __ldg(a.d + j * a.nb + kb);
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            if (rr < rc) {
-                int s = 0;
-                s = __dp4a(static_cast<int>(qw[rr][0]), static_cast<int>(x0.x), s);
-                s = __dp4a(static_cast<int>(qw[rr][1]), static_cast<int>(x0.y), s);
-                s = __dp4a(static_cast<int>(qw[rr][2]), static_cast<int>(x0.z), s);
-                s = __dp4a(static_cast<int>(qw[rr][3]), static_cast<int>(x0.w), s);
-                s = __dp4a(static_cast<int>(qw[rr][4]), static_cast<int>(x1.x), s);
-                s = __dp4a(static_cast<int>(qw[rr][5]), static_cast<int>(x1.y), s);
-                s = __dp4a(static_cast<int>(qw[rr][6]), static_cast<int>(x1.z), s);
-                s = __dp4a(static_cast<int>(qw[rr][7]), static_cast<int>(x1.w), s);
-                acc[rr][j] = fmaf(static_cast<float>(s), dw[rr] * dj, acc[rr][j]);
-            }
-        }
+        int s = 0;
+        s = __dp4a(static_cast<int>(qw[0]), static_cast<int>(x0.x), s);
+        s = __dp4a(static_cast<int>(qw[1]), static_cast<int>(x0.y), s);
+        s = __dp4a(static_cast<int>(qw[2]), static_cast<int>(x0.z), s);
+        s = __dp4a(static_cast<int>(qw[3]), static_cast<int>(x0.w), s);
+        s = __dp4a(static_cast<int>(qw[4]), static_cast<int>(x1.x), s);
+        s = __dp4a(static_cast<int>(qw[5]), static_cast<int>(x1.y), s);
+        s = __dp4a(static_cast<int>(qw[6]), static_cast<int>(x1.z), s);
+        s = __dp4a(static_cast<int>(qw[7]), static_cast<int>(x1.w), s);
+        acc[j] = fmaf(static_cast<float>(s), dw * dj, acc[j]);
     }
 }
 
 // ---------------------------------------------------------------------------------------------
 // The stream kernel (see the file header for the schedule).
 // ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void named_barrier_consumers() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarConsumers), "n"(kConsumerThreads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Single-thread bounded wait (the producer's lane 0).
+__device__ __forceinline__ bool thread_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
 template <int KIND, int M, bool PRE_B>
 __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamArgs a) {
     using G = Geo<KIND>;
@@ -228,50 +234,61 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
     const int64_t R0 = static_cast<int64_t>(blockIdx.x) * a.out_f / gridDim.x;
     const int64_t R1 = static_cast<int64_t>(blockIdx.x + 1) * a.out_f / gridDim.x;
     const int ntiles = static_cast<int>((R1 - R0 + TR - 1) / TR);
-
-    // This warp's K slice, in blocks.
-    const int nq = a.nb / G::kSliceQuantum;
-    const int kb_lo = (warp * nq / kWarps) * G::kSliceQuantum;
-    const int kb_hi = ((warp + 1) * nq / kWarps) * G::kSliceQuantum;
-    const int nch = (kb_hi - kb_lo + G::kChunkBlocks - 1) / G::kChunkBlocks;
+    const int nch = (a.nb + G::kChunkBlocks - 1) / G::kChunkBlocks;
     const int items = ntiles * nch;
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
-    uint8_t *ring = smem + a.off_ring + static_cast<size_t>(warp) * S * G::kStage;
-    float *part = reinterpret_cast<float *>(smem + a.off_part);  // [2][kWarps][TR][M]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + S;
+    uint8_t *ring = smem + a.off_ring;
+    float *part = reinterpret_cast<float *>(smem + a.off_part);    // [2][kWarps][TR][M]
     uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);  // [nb][M][4] (PRE_B)
 
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
         mbar_init_fence();
     }
-    __syncwarp();
+    __syncthreads();
 
-    // Producer side: (tile, chunk, stage) of the next item to issue.
-    const uint64_t pol = l2_evict_first_policy();
-    int p_tile = 0, p_ch = 0, p_stage = 0, issued = 0;
-    auto issue_next = [&]() {
-        const int64_t r0 = R0 + static_cast<int64_t>(p_tile) * TR;
-        const int rc = static_cast<int>(R1 - r0 < TR ? R1 - r0 : TR);
-        const int kb = kb_lo + p_ch * G::kChunkBlocks;
-        const int nblk = min(G::kChunkBlocks, kb_hi - kb);
-        const uint32_t bytes = static_cast<uint32_t>(nblk * G::kBlockBytes);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[p_stage], bytes * rc);
-        __syncwarp();
-        if (lane < rc)
-            bulk_g2s(ring + p_stage * G::kStage + lane * G::kSlot,
-                     a.w + (r0 + lane) * a.row_bytes + static_cast<int64_t>(kb) * G::kBlockBytes,
-                     bytes, &bars[p_stage], pol);
-        ++issued;
-        if (++p_ch == nch) {
-            p_ch = 0;
-            ++p_tile;
+    if (warp == kWarps) {
+        // ------------------------------- producer warp ---------------------------------------
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            int tile = 0, ch = 0, s = 0;
+            uint32_t eph = 0;  // parity of the empty-barrier phase awaited before a reuse
+            for (int it = 0; it < items; ++it) {
+                if (it >= S && !thread_wait_bounded(&empty[s], eph)) {
+                    fault(2u);
+                    break;
+                }
+                const int64_t r0 = R0 + static_cast<int64_t>(tile) * TR;
+                const int rc = static_cast<int>(R1 - r0 < TR ? R1 - r0 : TR);
+                const int kb = ch * G::kChunkBlocks;
+                const int nblk = min(G::kChunkBlocks, a.nb - kb);
+                const uint32_t bytes = static_cast<uint32_t>(nblk * G::kBlockBytes);
+                mbar_arrive_expect_tx(&full[s], bytes * rc);
+                const uint8_t *src = a.w + r0 * a.row_bytes + static_cast<int64_t>(kb) * G::kBlockBytes;
+                uint8_t *dst = ring + s * G::kStage;
+                for (int rr = 0; rr < rc; ++rr)
+                    bulk_g2s(dst + rr * G::kSlot, src + rr * a.row_bytes, bytes, &full[s], pol);
+                if (++ch == nch) {
+                    ch = 0;
+                    ++tile;
+                }
+                // Use k of a stage (items kS..kS+S-1) waits for phase k-1 of its empty barrier:
+                // parity 0 for k = 1, then alternating, so flip on every wrap after the second.
+                if (++s == S) {
+                    s = 0;
+                    if (it >= 2 * S - 1) eph ^= 1u;
+                }
+            }
         }
-        if (++p_stage == S) p_stage = 0;
-    };
-    // Weights do not depend on the preceding launch: start streaming before waiting for it.
-    while (issued < items && issued < S) issue_next();
+        return;
+    }
 
+    // --------------------------------- consumer warps ------------------------------------------
     griddep_wait();
     float scale = 1.0f;
     if (KIND == kE4M3) scale = __ldg(a.aux);
@@ -279,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
         // f16 MMA B fragments of the whole activation, once per CTA: entry (kb, g, t) holds
         // q[g][32kb + 8t .. 8t+7] as four f16x2 registers.
         const int n = a.nb * M * 4;
-        for (int i = threadIdx.x; i < n; i += kThreads) {
+        for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
             const int t = i & 3;
             const int g = (i >> 2) % M;
             const int kb = (i >> 2) / M;
@@ -290,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
             s8x4_to_f16x2x2(qv.y, v.z, v.w);
             bfrag[i] = v;
         }
-        __syncthreads();
+        named_barrier_consumers();
     }
 
     bool ok = true;
@@ -301,42 +318,44 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
         const int64_t r0 = R0 + static_cast<int64_t>(tile) * TR;
         const int rc = static_cast<int>(R1 - r0 < TR ? R1 - r0 : TR);
         float acc_m[4] = {0.f, 0.f, 0.f, 0.f};
-        float acc_q[4][M];
+        float acc_q[M];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < M; ++j) acc_q[i][j] = 0.f;
+        for (int j = 0; j < M; ++j) acc_q[j] = 0.f;
 
         for (int ch = 0; ch < nch; ++ch) {
-            if (ok && !warp_wait_bounded(&bars[c_stage], c_phase)) {
-                // Record the fault, give the copies in flight a bounded chance to land, and stop
-                // streaming; the tile barriers below still run so no warp is stranded.
+            if (ok && !warp_wait_bounded(&full[c_stage], c_phase)) {
+                // Record the fault, give the copies that may be in flight a bounded chance to
+                // land, and stop consuming; the tile barriers below still run.
                 if (lane == 0) fault(1u);
                 int st = c_stage;
                 uint32_t ph = c_phase;
-                for (int j = consumed + 1; j < issued; ++j) {
+                for (int j = consumed + 1; j < min(items, consumed + S); ++j) {
                     if (++st == S) {
                         st = 0;
                         ph ^= 1u;
                     }
-                    (void)warp_wait_bounded(&bars[st], ph);
+                    (void)warp_wait_bounded(&full[st], ph);
                 }
                 ok = false;
             }
             if (ok) {
-                const int kb = kb_lo + ch * G::kChunkBlocks;
-                const int nblk = min(G::kChunkBlocks, kb_hi - kb);
+                const int kbc = ch * G::kChunkBlocks;
+                const int nblk = min(G::kChunkBlocks, a.nb - kbc);
                 const uint8_t *stage = ring + c_stage * G::kStage;
                 if (G::kMma) {
-                    if (nblk == G::kChunkBlocks)
-                        mma_stage<KIND, M, PRE_B, true>(a, stage, bfrag, r0, R1 - 1, kb, nblk, lane, acc_m);
-                    else
-                        mma_stage<KIND, M, PRE_B, false>(a, stage, bfrag, r0, R1 - 1, kb, nblk, lane, acc_m);
-                } else
-                    q80_stage<M>(a, stage, rc, kb, nblk, lane, acc_q);
+                    const int kb0 = kbc + warp * G::kWarpBlocks;
+                    const int n = min(G::kWarpBlocks, nblk - warp * G::kWarpBlocks);
+                    const uint8_t *st = stage + warp * G::kWarpBlocks * 32;
+                    if (n == G::kWarpBlocks)
+                        mma_stage<KIND, M, PRE_B, true>(a, st, bfrag, r0, R1 - 1, kb0, n, lane, acc_m);
+                    else if (n > 0)
+                        mma_stage<KIND, M, PRE_B, false>(a, st, bfrag, r0, R1 - 1, kb0, n, lane, acc_m);
+                } else if (warp < rc) {
+                    q80_stage<M>(a, stage + warp * G::kSlot, kbc, nblk, lane, acc_q);
+                }
                 __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[c_stage]);
                 ++consumed;
-                if (issued < items) issue_next();  // refills the slot just consumed
             }
             if (++c_stage == S) {
                 c_stage = 0;
@@ -344,9 +363,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
             }
         }
 
-        // Per-warp partials of this tile -> shared memory.
-        float *pw = part + ((tile & 1) * kWarps + warp) * TR * M;
         if (G::kMma) {
+            // Per-warp partials of this tile -> shared memory; then sum the 8 warp partials of
+            // each (row, token) in warp order and store y.
+            float *pw = part + ((tile & 1) * kWarps + warp) * TR * M;
             const int g = lane >> 2, t = lane & 3;
             if (2 * t < M) {
                 pw[g * M + 2 * t] = acc_m[0];
@@ -356,24 +376,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
                 pw[g * M + 2 * t + 1] = acc_m[1];
                 pw[(g + 8) * M + 2 * t + 1] = acc_m[3];
             }
-        } else {
+            named_barrier_consumers();
+            for (int idx = threadIdx.x; idx < rc * M; idx += kConsumerThreads) {
+                const int row = idx / M, tok = idx - row * M;
+                const float *pt = part + (tile & 1) * kWarps * TR * M + row * M + tok;
+                float v = 0.f;
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr)
+                for (int w = 0; w < kWarps; ++w) v += pt[w * TR * M];
+                a.y[static_cast<int64_t>(tok) * a.out_f + r0 + row] = v * scale;
+            }
+        } else if (warp < rc) {
 #pragma unroll
-                for (int j = 0; j < M; ++j) {
-                    const float v = warp_sum(acc_q[rr][j]);
-                    if (lane == 0) pw[rr * M + j] = v;
-                }
-        }
-        __syncthreads();
-        // Sum the 8 warp partials of each (row, token) in warp order and store y.
-        for (int idx = threadIdx.x; idx < rc * M; idx += kThreads) {
-            const int row = idx / M, tok = idx - row * M;
-            const float *pt = part + (tile & 1) * kWarps * TR * M + row * M + tok;
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += pt[w * TR * M];
-            a.y[static_cast<int64_t>(tok) * a.out_f + r0 + row] = v * scale;
+            for (int j = 0; j < M; ++j) {
+                const float v = warp_sum(acc_q[j]);
+                if (lane == 0) a.y[static_cast<int64_t>(j) * a.out_f + r0 + warp] = v;
+            }
         }
     }
 }
@@ -381,13 +398,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
 // ---------------------------------------------------------------------------------------------
 // Generic kernel: one warp per output row, byte-granular global loads, any alignment.
 // ---------------------------------------------------------------------------------------------
+constexpr int kGenericWarps = 8;
+
 template <int KIND>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kGenericWarps * 32)
     gemv_generic_kernel(const uint8_t *__restrict__ w, const float *__restrict__ aux,
                         const int8_t *__restrict__ qs, const float *__restrict__ d,
                         float *__restrict__ y, int64_t out_f, int in_f, int m) {
     const int lane = threadIdx.x & 31;
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kGenericWarps + (threadIdx.x >> 5);
     if (r >= out_f) return;
     const int nb = in_f / 32;
     const int gcols = (in_f + 127) / 128;
@@ -536,13 +555,13 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
     bool pre_b = false;
     if (fast) {
         const uint32_t two_per_sm = static_cast<uint32_t>(info.smem_sm / 2 - 1024);
-        const uint32_t part = align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128);
+        const uint32_t part = G::kMma ? align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128) : 0u;
         const uint32_t bfrag = G::kMma ? align_up(static_cast<uint32_t>(nb * m * 64), 128) : 0u;
         int S = G::kStages;
         uint32_t bars = 0, ring = 0;
         for (; S >= 2; --S) {
-            bars = align_up(static_cast<uint32_t>(kWarps * S * 8), 128);
-            ring = static_cast<uint32_t>(kWarps * S * G::kStage);
+            bars = align_up(static_cast<uint32_t>(2 * S * 8), 128);
+            ring = static_cast<uint32_t>(S * G::kStage);
             if (bars + part + ring <= static_cast<uint32_t>(info.smem_optin)) break;
         }
         if (S < 2) {
@@ -579,8 +598,8 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
             e = launch_stream_m<KIND, false>(m, a, smem, dev, info, st);
         }
     } else {
-        const int64_t blocks = (out_f + kWarps - 1) / kWarps;
-        gemv_generic_kernel<KIND><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(
+        const int64_t blocks = (out_f + kGenericWarps - 1) / kGenericWarps;
+        gemv_generic_kernel<KIND><<<static_cast<unsigned>(blocks), kGenericWarps * 32, 0, st>>>(
             w, aux, qs, d, y, out_f, static_cast<int>(in_f), m);
         e = cudaGetLastError();
     }
