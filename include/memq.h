@@ -85,8 +85,8 @@ int memq_rmsnorm_q8_1(const float *x, const float *w, float *z, int8_t *qs, floa
  *   y        device, f32 [m][out_f]
  *   in_f % 32 == 0, 32 <= in_f <= 2^24; 1 <= m <= MEMQ_MAX_M; out_f >= 0, where out_f == 0
  *   is a no-op that accepts NULL pointers.
- * The fast path wants w 16-byte and qs 8-byte aligned; other alignments take a slower generic
- * kernel with the same results contract.
+ * The fast path wants w and qs 16-byte aligned; other alignments take a slower generic kernel
+ * with the same results contract.
  */
 int memq_gemv_e4m3(const uint8_t *w, const float *w_scale, const int8_t *qs, const float *d,
                    float *y, int64_t out_f, int64_t in_f, int m, void *stream);

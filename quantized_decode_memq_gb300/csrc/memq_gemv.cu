@@ -63,7 +63,8 @@ struct Geo {
     static constexpr int kChunkBlocks = 32;
     static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
     static constexpr int kStage = kTileRows * kSlot;
-    static constexpr int kStages = 4;
+    static constexpr int kMinStages = 3;
+    static constexpr int kMaxStages = 8;
     static constexpr int kWarpBlocks = kChunkBlocks / kWarps;  // E4M3: blocks per warp per stage
 };
 
@@ -79,7 +80,16 @@ struct StreamArgs {
     int nb;     // in_f / 32
     int gcols;  // ceil(in_f / 128)
     int stages;
-    uint32_t off_part, off_bfrag, off_ring;  // shared-memory layout (bytes); barriers at 0
+    int grid_rows;  // block-128: grid rows staged per CTA (bound)
+    // Shared-memory layout (bytes); barriers at 0.
+    uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_ring;
+};
+
+// Where the consumers read the activation from.
+enum ActMode : int {
+    kActGlobal = 0,  // qs and d straight from global memory (L1/L2)
+    kActSmem = 1,    // qs (int8) and d staged in shared memory once per CTA
+    kActFrag = 2,    // E4M3 / block-128: f16 MMA B fragments and d staged in shared memory
 };
 
 __device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bit); }
@@ -94,22 +104,28 @@ __device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bi
 // block is permuted: thread (g, t) = (lane/4, lane%4) supplies physical columns 8t..8t+7 of its
 // rows for MMA slots {2t, 2t+1, 2t+8, 2t+9} (first MMA: 8t..8t+3, second: 8t+4..8t+7), and the
 // B fragment of token g uses exactly the same map.  The B fragments come precomputed from
-// shared memory (PRE_B) or are converted from the int8 activation in global memory.
+// shared memory (kActFrag) or are converted from the int8 activation (kActSmem, kActGlobal).
 // acc[0..3] = rows (g, g+8) x tokens (2t, 2t+1) of the tile.
 // ---------------------------------------------------------------------------------------------
-template <int KIND, int M, bool PRE_B, bool FULL>
+template <int KIND, int M, int MODE, bool FULL>
 __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *stage,
-                                          const uint4 *bfrag, int64_t row0, int64_t row_last,
-                                          int kb0, int nblk, int lane, float (&acc)[4]) {
+                                          const uint8_t *sm, int64_t row0, int64_t row_last,
+                                          int64_t grow_base, int kb0, int nblk, int lane,
+                                          float (&acc)[4]) {
     using G = Geo<KIND>;
     const int g = lane >> 2;
     const int t = lane & 3;
+    const uint4 *bfrag = reinterpret_cast<const uint4 *>(sm + a.off_bfrag);
+    const int8_t *s_qs = reinterpret_cast<const int8_t *>(sm + a.off_qs);
+    const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
     const float *grow0 = nullptr, *grow8 = nullptr;
     if (KIND == kBlk) {
+        // Grid rows of this thread's two tile rows, from the CTA's staged grid rows.
         const int64_t r0 = row0 + g > row_last ? row_last : row0 + g;
         const int64_t r8 = row0 + g + 8 > row_last ? row_last : row0 + g + 8;
-        grow0 = a.aux + (r0 >> 7) * a.gcols;
-        grow8 = a.aux + (r8 >> 7) * a.gcols;
+        const float *s_grid = reinterpret_cast<const float *>(sm + a.off_grid);
+        grow0 = s_grid + ((r0 >> 7) - grow_base) * a.gcols;
+        grow8 = s_grid + ((r8 >> 7) - grow_base) * a.gcols;
     }
 #pragma unroll
     for (int b = 0; b < G::kWarpBlocks; ++b) {
@@ -117,25 +133,33 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
             const int kb = kb0 + b;
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
             if (g < M) {
-                if (PRE_B) {
+                if (MODE == kActFrag) {
                     const uint4 v = bfrag[(kb * M + g) * 4 + t];
                     bq[0] = v.x;
                     bq[1] = v.y;
                     bq[2] = v.z;
                     bq[3] = v.w;
                 } else {
-                    const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(
-                        a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+                    const uint2 qv = MODE == kActSmem
+                                         ? lds64(s_qs + g * a.in_f + 32 * kb + 8 * t)
+                                         : __ldg(reinterpret_cast<const uint2 *>(
+                                               a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
                     s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
                     s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
                 }
             }
-            float k0 = (2 * t < M) ? __ldg(a.d + (2 * t) * a.nb + kb) : 0.f;
-            float k1 = (2 * t + 1 < M) ? __ldg(a.d + (2 * t + 1) * a.nb + kb) : 0.f;
+            float k0 = 0.f, k1 = 0.f;
+            if (MODE == kActGlobal) {
+                if (2 * t < M) k0 = __ldg(a.d + (2 * t) * a.nb + kb);
+                if (2 * t + 1 < M) k1 = __ldg(a.d + (2 * t + 1) * a.nb + kb);
+            } else {
+                if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
+                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
+            }
             float k2 = k0, k3 = k1;
             if (KIND == kBlk) {
-                const float gg = __ldg(grow0 + (kb >> 2));
-                const float gg8 = __ldg(grow8 + (kb >> 2));
+                const float gg = grow0[kb >> 2];
+                const float gg8 = grow8[kb >> 2];
                 k0 *= gg;
                 k1 *= gg;
                 k2 *= gg8;
@@ -165,9 +189,10 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
 // 34-byte record, so they are re-aligned from 4-byte shared loads with funnel shifts; dp4a then
 // gives the exact int32 dot product with the activation block.
 // ---------------------------------------------------------------------------------------------
-template <int M>
-__device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *slot, int kb0,
-                                          int nblk, int lane, float (&acc)[M]) {
+template <int M, int MODE>
+__device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *slot,
+                                          const uint8_t *sm, int kb0, int nblk, int lane,
+                                          float (&acc)[M]) {
     if (lane >= nblk) return;
     const int kb = kb0 + lane;
     const int qstart = 34 * lane + 2;
@@ -181,12 +206,22 @@ __device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *sl
 #pragma unroll
     for (int i = 0; i < 8; ++i) qw[i] = __funnelshift_r(wv[i], wv[i + 1], sh);
     const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(slot + 34 * lane))));
+    const int8_t *s_qs = reinterpret_cast<const int8_t *>(sm + a.off_qs);
+    const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
 #pragma unroll
     for (int j = 0; j < M; ++j) {
-        const uint4 *qx = reinterpret_cast<const uint4 *>(a.qs + static_cast<int64_t>(j) * a.in_f + 32 * kb);
-        const uint4 x0 = __ldg(qx);
-        const uint4 x1 = __ldg(qx + 1);
-        const float dj = __ldg(a.d + j * a.nb + kb);
+        uint4 x0, x1;
+        float dj;
+        if (MODE == kActSmem) {
+            x0 = lds128(s_qs + j * a.in_f + 32 * kb);
+            x1 = lds128(s_qs + j * a.in_f + 32 * kb + 16);
+            dj = s_d[j * a.nb + kb];
+        } else {
+            const uint4 *qx = reinterpret_cast<const uint4 *>(a.qs + static_cast<int64_t>(j) * a.in_f + 32 * kb);
+            x0 = __ldg(qx);
+            x1 = __ldg(qx + 1);
+            dj = __ldg(a.d + j * a.nb + kb);
+        }
         int s = 0;
         s = __dp4a(static_cast<int>(qw[0]), static_cast<int>(x0.x), s);
         s = __dp4a(static_cast<int>(qw[1]), static_cast<int>(x0.y), s);
@@ -220,7 +255,7 @@ __device__ __forceinline__ bool thread_wait_bounded(uint64_t *bar, uint32_t pari
     return true;
 }
 
-template <int KIND, int M, bool PRE_B>
+template <int KIND, int M, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamArgs a) {
     using G = Geo<KIND>;
     constexpr int TR = G::kTileRows;
@@ -240,8 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + S;
     uint8_t *ring = smem + a.off_ring;
-    float *part = reinterpret_cast<float *>(smem + a.off_part);    // [2][kWarps][TR][M]
-    uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);  // [nb][M][4] (PRE_B)
+    float *part = reinterpret_cast<float *>(smem + a.off_part);  // [2][kWarps][TR][M]
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -292,9 +326,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
     griddep_wait();
     float scale = 1.0f;
     if (KIND == kE4M3) scale = __ldg(a.aux);
-    if (PRE_B) {
-        // f16 MMA B fragments of the whole activation, once per CTA: entry (kb, g, t) holds
+    // Stage the activation (per MODE) and the block-128 grid rows this CTA touches.
+    if (MODE == kActFrag) {
+        // f16 MMA B fragments of the whole activation: entry (kb, g, t) holds
         // q[g][32kb + 8t .. 8t+7] as four f16x2 registers.
+        uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);
         const int n = a.nb * M * 4;
         for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
             const int t = i & 3;
@@ -307,8 +343,26 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
             s8x4_to_f16x2x2(qv.y, v.z, v.w);
             bfrag[i] = v;
         }
-        named_barrier_consumers();
     }
+    if (MODE == kActSmem) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.qs);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem + a.off_qs);
+        const int n16 = M * a.in_f / 16;
+        for (int i = threadIdx.x; i < n16; i += kConsumerThreads) dst[i] = __ldg(src + i);
+    }
+    if (MODE != kActGlobal) {
+        float *dst = reinterpret_cast<float *>(smem + a.off_d);
+        for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldg(a.d + i);
+    }
+    const int64_t grow_base = R0 >> 7;
+    if (KIND == kBlk) {
+        float *dst = reinterpret_cast<float *>(smem + a.off_grid);
+        const int nrows = static_cast<int>(((R1 - 1) >> 7) - grow_base + 1);
+        const int n = nrows * a.gcols;
+        for (int i = threadIdx.x; i < n; i += kConsumerThreads)
+            dst[i] = __ldg(a.aux + grow_base * a.gcols + i);
+    }
+    named_barrier_consumers();
 
     bool ok = true;
     int c_stage = 0;
@@ -347,11 +401,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
                     const int n = min(G::kWarpBlocks, nblk - warp * G::kWarpBlocks);
                     const uint8_t *st = stage + warp * G::kWarpBlocks * 32;
                     if (n == G::kWarpBlocks)
-                        mma_stage<KIND, M, PRE_B, true>(a, st, bfrag, r0, R1 - 1, kb0, n, lane, acc_m);
+                        mma_stage<KIND, M, MODE, true>(a, st, smem, r0, R1 - 1, grow_base, kb0, n, lane, acc_m);
                     else if (n > 0)
-                        mma_stage<KIND, M, PRE_B, false>(a, st, bfrag, r0, R1 - 1, kb0, n, lane, acc_m);
+                        mma_stage<KIND, M, MODE, false>(a, st, smem, r0, R1 - 1, grow_base, kb0, n, lane, acc_m);
                 } else if (warp < rc) {
-                    q80_stage<M>(a, stage + warp * G::kSlot, kbc, nblk, lane, acc_q);
+                    q80_stage<M, MODE>(a, stage + warp * G::kSlot, smem, kbc, nblk, lane, acc_q);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[c_stage]);
@@ -456,7 +510,7 @@ struct DeviceInfo {
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
-std::atomic<uint32_t> g_attr_set[kMaxDevices][3];  // bit per (M, PRE_B): attribute set
+std::atomic<uint32_t> g_attr_set[kMaxDevices][3];  // bit per (M, mode): attribute set
 
 bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -480,19 +534,47 @@ cudaError_t device_info(int &dev, DeviceInfo &info) {
     return info.sms > 0 ? cudaSuccess : cudaErrorInvalidDevice;
 }
 
-template <int KIND, int M, bool PRE_B>
+template <int KIND, int M, int MODE>
 cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const DeviceInfo &info,
                           cudaStream_t st) {
-    auto kern = gemv_stream_kernel<KIND, M, PRE_B>;
-    const uint32_t bit = 1u << ((M - 1) + (PRE_B ? 8 : 0));
+    auto kern = gemv_stream_kernel<KIND, M, MODE>;
+    const uint32_t bit = 1u << ((M - 1) + 8 * MODE);
     if (!(g_attr_set[dev][KIND].load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              info.smem_optin);
         if (e != cudaSuccess) return e;
         g_attr_set[dev][KIND].fetch_or(bit, std::memory_order_acq_rel);
     }
+    // Ring depth: as many stages as fit when the CTAs that registers allow per SM share its
+    // shared memory (more stages = more weight bytes in flight), at least kMinStages.
+    using G = Geo<KIND>;
+    const uint32_t fixed = smem_bytes;  // everything except the ring and its barriers
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, kern, kThreads, fixed + G::kMinStages * (G::kStage + 16) + 128);
+    if (e != cudaSuccess) return e;
+    per_sm = std::max(per_sm, 1);
+    int S = G::kMinStages;
+    for (int s = G::kMaxStages; s >= G::kMinStages; --s) {
+        const uint32_t need = fixed + align_up(static_cast<uint32_t>(2 * s * 8), 128) +
+                              static_cast<uint32_t>(s * G::kStage);
+        if (need <= static_cast<uint32_t>(info.smem_optin) &&
+            static_cast<int64_t>(need + 1024) * per_sm <= info.smem_sm) {
+            S = s;
+            break;
+        }
+    }
+    const uint32_t bars = align_up(static_cast<uint32_t>(2 * S * 8), 128);
+    // Shift every region past the barriers.
+    a.stages = S;
+    a.off_part += bars;
+    a.off_grid += bars;
+    a.off_bfrag += bars;
+    a.off_qs += bars;
+    a.off_d += bars;
+    a.off_ring += bars;
+    smem_bytes = fixed + bars + static_cast<uint32_t>(S * G::kStage);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes);
     if (e != cudaSuccess) return e;
     per_sm = std::max(per_sm, 1);
     // One wave of CTAs, never more CTAs than output rows.
@@ -511,18 +593,18 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int KIND, bool PRE_B>
+template <int KIND, int MODE>
 cudaError_t launch_stream_m(int m, StreamArgs a, uint32_t smem, int dev, const DeviceInfo &info,
                             cudaStream_t st) {
     switch (m) {
-        case 1: return launch_stream<KIND, 1, PRE_B>(a, smem, dev, info, st);
-        case 2: return launch_stream<KIND, 2, PRE_B>(a, smem, dev, info, st);
-        case 3: return launch_stream<KIND, 3, PRE_B>(a, smem, dev, info, st);
-        case 4: return launch_stream<KIND, 4, PRE_B>(a, smem, dev, info, st);
-        case 5: return launch_stream<KIND, 5, PRE_B>(a, smem, dev, info, st);
-        case 6: return launch_stream<KIND, 6, PRE_B>(a, smem, dev, info, st);
-        case 7: return launch_stream<KIND, 7, PRE_B>(a, smem, dev, info, st);
-        default: return launch_stream<KIND, 8, PRE_B>(a, smem, dev, info, st);
+        case 1: return launch_stream<KIND, 1, MODE>(a, smem, dev, info, st);
+        case 2: return launch_stream<KIND, 2, MODE>(a, smem, dev, info, st);
+        case 3: return launch_stream<KIND, 3, MODE>(a, smem, dev, info, st);
+        case 4: return launch_stream<KIND, 4, MODE>(a, smem, dev, info, st);
+        case 5: return launch_stream<KIND, 5, MODE>(a, smem, dev, info, st);
+        case 6: return launch_stream<KIND, 6, MODE>(a, smem, dev, info, st);
+        case 7: return launch_stream<KIND, 7, MODE>(a, smem, dev, info, st);
+        default: return launch_stream<KIND, 8, MODE>(a, smem, dev, info, st);
     }
 }
 
@@ -545,37 +627,53 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
     const int64_t row_bytes = (KIND == kQ80) ? static_cast<int64_t>(nb) * 34 : in_f;
     using G = Geo<KIND>;
 
-    // Fast-path eligibility and shared-memory plan: barriers, two tile-partial buffers, the
-    // precomputed B fragments (E4M3 / block-128, when they still leave room for two CTAs per
-    // SM), and kWarps rings of S stages.
-    bool fast = aligned(w, 16) && aligned(qs, KIND == kQ80 ? 16 : 8) && (row_bytes % 16) == 0 &&
+    // Fast-path eligibility and shared-memory plan.  Fixed part: barriers, tile partials
+    // (E4M3 / block-128), the CTA's grid rows (block-128), and an S-stage ring.  Activation:
+    // staged in shared memory when that still leaves room for two CTAs per SM -- as f16 MMA
+    // fragments (E4M3 / block-128) or as int8 + scales -- else read from global memory.
+    bool fast = aligned(w, 16) && aligned(qs, 16) && (row_bytes % 16) == 0 &&
                 (KIND != kQ80 || (nb % 8) == 0);
     StreamArgs a = {};
     uint32_t smem = 0;
-    bool pre_b = false;
+    int mode = kActGlobal;
     if (fast) {
         const uint32_t two_per_sm = static_cast<uint32_t>(info.smem_sm / 2 - 1024);
         const uint32_t part = G::kMma ? align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128) : 0u;
-        const uint32_t bfrag = G::kMma ? align_up(static_cast<uint32_t>(nb * m * 64), 128) : 0u;
-        int S = G::kStages;
-        uint32_t bars = 0, ring = 0;
-        for (; S >= 2; --S) {
-            bars = align_up(static_cast<uint32_t>(2 * S * 8), 128);
-            ring = static_cast<uint32_t>(S * G::kStage);
-            if (bars + part + ring <= static_cast<uint32_t>(info.smem_optin)) break;
-        }
-        if (S < 2) {
+        // Grid rows one CTA can touch: rows per CTA at one CTA per SM, over 128, plus two.
+        const int64_t rows_cta = (out_f + info.sms - 1) / info.sms;
+        const int grid_rows = static_cast<int>(rows_cta / 128 + 2);
+        const int gcols = static_cast<int>((in_f + 127) / 128);
+        const uint32_t gridb = KIND == kBlk ? align_up(static_cast<uint32_t>(grid_rows * gcols * 4), 128) : 0u;
+        const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * 64), 128);
+        const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
+        const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
+        const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
+        const uint32_t base = part + gridb + ring_min;
+        if (base > static_cast<uint32_t>(info.smem_optin)) {
             fast = false;
         } else {
-            const uint32_t base = bars + part + ring;
-            pre_b = G::kMma && bfrag > 0 &&
-                    (base + bfrag <= two_per_sm ||
-                     (base > two_per_sm && base + bfrag <= static_cast<uint32_t>(info.smem_optin)));
-            a.stages = S;
-            a.off_part = bars;
-            a.off_bfrag = bars + part;
-            a.off_ring = a.off_bfrag + (pre_b ? bfrag : 0u);
-            smem = a.off_ring + ring;
+            uint32_t actb = 0;
+            if (G::kMma && base + frag + db <= two_per_sm) {
+                mode = kActFrag;
+                actb = frag + db;
+            } else if (base + qsb + db <= two_per_sm) {
+                mode = kActSmem;
+                actb = qsb + db;
+            }
+            (void)actb;
+            // Offsets without the barrier block; launch_stream shifts them once S is known.
+            a.grid_rows = grid_rows;
+            a.off_part = 0;
+            a.off_grid = a.off_part + part;
+            uint32_t off = a.off_grid + gridb;
+            a.off_bfrag = off;
+            if (mode == kActFrag) off += frag;
+            a.off_qs = off;
+            if (mode == kActSmem) off += qsb;
+            a.off_d = off;
+            if (mode != kActGlobal) off += db;
+            a.off_ring = off;
+            smem = off;  // fixed part; the ring is added in launch_stream
         }
     }
 
@@ -592,10 +690,12 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
         a.nb = nb;
         a.gcols = static_cast<int>((in_f + 127) / 128);
         if constexpr (G::kMma) {
-            e = pre_b ? launch_stream_m<KIND, true>(m, a, smem, dev, info, st)
-                      : launch_stream_m<KIND, false>(m, a, smem, dev, info, st);
+            e = mode == kActFrag  ? launch_stream_m<KIND, kActFrag>(m, a, smem, dev, info, st)
+                : mode == kActSmem ? launch_stream_m<KIND, kActSmem>(m, a, smem, dev, info, st)
+                                   : launch_stream_m<KIND, kActGlobal>(m, a, smem, dev, info, st);
         } else {
-            e = launch_stream_m<KIND, false>(m, a, smem, dev, info, st);
+            e = mode == kActSmem ? launch_stream_m<KIND, kActSmem>(m, a, smem, dev, info, st)
+                                 : launch_stream_m<KIND, kActGlobal>(m, a, smem, dev, info, st);
         }
     } else {
         const int64_t blocks = (out_f + kGenericWarps - 1) / kGenericWarps;
