@@ -37,7 +37,8 @@ if ROOT not in sys.path:
 METRIC = "m=1 quantized GEMV achieved HBM GB/s (DRAM-cold) and % of GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 
-# Workloads by name: (container, out_f, in_f, m, rotated copies)
+# Workloads by name: (container, out_f, in_f, m, rotated copies).  Any other name of the form
+# <e4m3|blk128|q8_0>_<out_f>x<in_f>_m<m> is accepted too (copies sized to twice the L2).
 WORKLOADS = {
     "q8_0_4096x4096_m1": ("q8_0", 4096, 4096, 1, 16),
     "e4m3_1024x4096_m1": ("e4m3", 1024, 4096, 1, 64),
@@ -46,6 +47,23 @@ WORKLOADS = {
     "q8_0_17408x5120_m1": ("q8_0", 17408, 5120, 1, 4),
 }
 DEFAULT_WORKLOAD = "q8_0_4096x4096_m1"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse_workload(name: str):
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    try:
+        kind, shape, mtag = name.split("_") if not name.startswith("q8_0") else \
+            ("q8_0",) + tuple(name[len("q8_0_"):].split("_"))
+        out_f, in_f = (int(v) for v in shape.split("x"))
+        m = int(mtag.lstrip("m"))
+    except ValueError:
+        raise SystemExit(f"unknown workload {name!r}")
+    kind = {"e4m3": "e4m3", "blk128": "blk", "q8_0": "q8_0"}[kind]
+    wbytes = gemv_bytes(kind, out_f, in_f, m)
+    copies = max(4, -(-2 * L2_BYTES // wbytes))
+    return kind, out_f, in_f, m, copies
 
 
 # ------------------------------------------------------------------------------------------
@@ -236,9 +254,19 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     from quantized_decode_memq_gb300 import build
     build.build()
-    kind, out_f, in_f, m, copies = WORKLOADS[args.workload]
+    kind, out_f, in_f, m, copies = parse_workload(args.workload)
     wl = DecodeStep(kind, out_f, in_f, m, copies, dev)
     stream = torch.cuda.Stream(device=dev)
+    if args.ncu_launches:
+        # Profiling entry: one producer launch, then N GEMV launches over the rotated copies.
+        with torch.cuda.stream(stream):
+            wl.producer()
+            for i in range(args.ncu_launches):
+                wl.gemv(i)
+        stream.synchronize()
+        assert wl.memq.memq_device_fault(stream) == 0
+        print(json.dumps({"ncu_launches": args.ncu_launches, "workload": args.workload}))
+        return
 
     # Eager warm-up of every launch shape (sets kernel attributes outside any capture).
     with torch.cuda.stream(stream):
@@ -481,7 +509,7 @@ def run_reference(args, world, rank):
         return
     import oracle
     oracle.build()
-    kind, out_f, in_f, m, copies = WORKLOADS[args.workload]
+    kind, out_f, in_f, m, copies = parse_workload(args.workload)
     x, wn, w, aux = _oracle_inputs(kind, out_f, in_f, m)
     t0 = time.perf_counter()
     _oracle_step(oracle, kind, x, wn, w, aux, in_f, rows=np.arange(min(out_f, 256)))
@@ -530,12 +558,15 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="one of %s, or <e4m3|blk128|q8_0>_<out_f>x<in_f>_m<m>" % sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMV launch from an ncu capture of this kernel")
+    ap.add_argument("--ncu-launches", type=int, default=0,
+                    help="profiling entry: run one producer and N GEMV launches, no timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
