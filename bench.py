@@ -172,6 +172,25 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def profiled_traffic(workload: str):
+    """DRAM bytes per GEMV launch from the committed ncu capture of this workload, or None when
+    there is none or the kernel sources changed since it was taken."""
+    import glob
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemv_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "quantized_decode_memq_gb300", "csrc", "*.cu*"))):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("kernel_sources_sha256"):
+        return None
+    return rec.get("dram_bytes_per_launch", {}).get(workload)
+
+
 def measured_peak_hbm():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -350,7 +369,7 @@ def run_ours(args, world, rank, local):
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": args.traffic,
+            "traffic": args.traffic if args.traffic is not None else profiled_traffic(args.workload),
             "kernel": f"gemv_stream_kernel<{kind}, m={m}>",
             "bytes_per_launch": wl.gemv_bytes,
             "launch_us": round(gemv_s * 1e6, 3),
