@@ -10,8 +10,10 @@ Printed (rank 0, one JSON line):
   value       whole-step throughput: algorithmic bytes of the step (GEMV weights + scales +
               activation, plus the producer's x, w, qs, d) / device time per step, inputs
               resident in HBM; K steps replayed from CUDA graphs, timed with CUDA events.
-  roofline    the GEMV alone: algorithmic bytes per launch / mean launch duration (CUDA events
-              around each launch, DRAM-cold), against the measured HBM copy bandwidth.
+  roofline    the dominant kernel (the GEMV): algorithmic bytes per launch / average launch
+              duration in a decode loop (graph of back-to-back launches over the rotated
+              copies, DRAM-cold), against the measured HBM copy bandwidth; the one-launch-at-a-
+              time figure is reported beside it.
   e2e         the same metric through the public API with host buffers: per step the
               activation row is copied host->device from pinned memory, the chain runs, the
               result y is copied device->host and the host waits for it.
@@ -210,13 +212,14 @@ def measured_peak_hbm():
 class DecodeStep:
     """Producer + GEMV with rotated weight copies, all buffers preallocated on the device."""
 
-    def __init__(self, kind, out_f, in_f, m, copies, device, seed=0x51ED0002):
+    def __init__(self, kind, out_f, in_f, m, copies, device, seed=0x51ED0002, fused=True):
         import torch
         import quantized_decode_memq_gb300 as memq
         from quantized_decode_memq_gb300 import synth
         self.memq = memq
         self.kind, self.out_f, self.in_f, self.m, self.copies = kind, out_f, in_f, m, copies
         self.device = device
+        self.fused_step = fused
         x, wn = synth.activation_rows(in_f, m)
         self.x_host = x
         self.x = torch.from_numpy(x).to(device)
@@ -252,9 +255,26 @@ class DecodeStep:
         else:
             self.memq.memq_gemv_e4m3(self.w[c], self.aux[c], self.qs, self.d, y=self.y)
 
+    def fused(self, i):
+        """The whole decode step in one launch (RMSNorm -> q8_1 inside the GEMV)."""
+        c = i % self.copies
+        memq = self.memq
+        if self.kind == "q8_0":
+            memq.memq_rmsnorm_q8_1_gemv_q8_0(self.x, self.wn, self.w[c], 1e-6, qs=self.qs, d=self.d,
+                                             y=self.y)
+        elif self.kind == "blk":
+            memq.memq_rmsnorm_q8_1_gemv_e4m3_blk128(self.x, self.wn, self.w[c], self.aux[c], 1e-6,
+                                                    qs=self.qs, d=self.d, y=self.y)
+        else:
+            memq.memq_rmsnorm_q8_1_gemv_e4m3(self.x, self.wn, self.w[c], self.aux[c], 1e-6,
+                                             qs=self.qs, d=self.d, y=self.y)
+
     def step(self, i):
-        self.producer()
-        self.gemv(i)
+        if self.fused_step:
+            self.fused(i)
+        else:
+            self.producer()
+            self.gemv(i)
 
 
 def capture(fn, n, stream):
@@ -274,14 +294,15 @@ def run_ours(args, world, rank, local):
     from quantized_decode_memq_gb300 import build
     build.build()
     kind, out_f, in_f, m, copies = parse_workload(args.workload)
-    wl = DecodeStep(kind, out_f, in_f, m, copies, dev)
+    fused = args.step == "fused"
+    wl = DecodeStep(kind, out_f, in_f, m, copies, dev, fused=fused)
     stream = torch.cuda.Stream(device=dev)
     if args.ncu_launches:
         # Profiling entry: one producer launch, then N GEMV launches over the rotated copies.
         with torch.cuda.stream(stream):
             wl.producer()
             for i in range(args.ncu_launches):
-                wl.gemv(i)
+                wl.step(i) if fused else wl.gemv(i)
         stream.synchronize()
         assert wl.memq.memq_device_fault(stream) == 0
         print(json.dumps({"ncu_launches": args.ncu_launches, "workload": args.workload}))
@@ -328,12 +349,18 @@ def run_ours(args, world, rank, local):
     value = units / t_max / 1e9
     ms_per_step = t_max / K * 1e3
 
-    # Roofline: the GEMV alone, one launch at a time, DRAM-cold (rotated copies).
-    gemv_s = time_gemv_launches(wl, stream, n=max(64, 4 * copies))
-    achieved = wl.gemv_bytes / gemv_s / 1e9
+    # Roofline: the dominant kernel -- the fused decode-step kernel (whole step's bytes) or the
+    # GEMV (GEMV bytes) -- one launch at a time, DRAM-cold (rotated copies).
+    launch_fn = wl.fused if fused else wl.gemv
+    launch_bytes = wl.step_bytes if fused else wl.gemv_bytes
+    # Average launch duration of the kernel in a decode loop: a CUDA graph of back-to-back
+    # launches over the rotated copies (each launch reads its own weights from DRAM), CUDA
+    # events around the replays.  Also reported: one launch at a time, event-bracketed, which
+    # adds the launch and teardown latency outside the kernel's execution.
+    b2b_s = time_gemv_back_to_back(wl, stream, n=16 * copies, fn=launch_fn)
+    achieved = launch_bytes / b2b_s / 1e9
+    gemv_s = time_gemv_launches(wl, stream, n=max(64, 4 * copies), fn=launch_fn)
     peak, peak_kind = measured_peak_hbm()
-    # Back-to-back GEMVs (graph of rotated launches, programmatic overlap between them).
-    b2b_s = time_gemv_back_to_back(wl, stream, n=16 * copies)
 
     e2e = time_e2e(wl, stream, steps=min(K, args.e2e_steps))
     e2e_t, e2e_units = aggregate(e2e["elapsed"], float(e2e["steps"] * wl.step_bytes))
@@ -352,8 +379,10 @@ def run_ours(args, world, rank, local):
         "dtype": "int8" if kind == "q8_0" else "fp8",
         "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: fused RMSNorm->q8_1 (1x{in_f} f32) then "
+            "workload": f"{args.workload}: RMSNorm->q8_1 ({m}x{in_f} f32) then "
                         f"{kind} GEMV out_f={out_f} in_f={in_f} m={m}",
+            "step": "one fused launch (memq_rmsnorm_q8_1_gemv_*)" if fused else
+                    "two launches (memq_rmsnorm_q8_1 + memq_gemv_*)",
             "weight_copies": copies,
             "rotation_bytes": copies * (wl.gemv_bytes - m * (in_f + in_f // 8)),
             "l2": "inputs larger than L2: each step reads the next of the rotated weight "
@@ -370,13 +399,14 @@ def run_ours(args, world, rank, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": args.traffic if args.traffic is not None else profiled_traffic(args.workload),
-            "kernel": f"gemv_stream_kernel<{kind}, m={m}>",
-            "bytes_per_launch": wl.gemv_bytes,
-            "launch_us": round(gemv_s * 1e6, 3),
+            "kernel": f"gemv_stream_kernel<{kind}, m={m}, fused={fused}>",
+            "bytes_per_launch": launch_bytes,
+            "launch_us": round(b2b_s * 1e6, 3),
+            "launch_timing": "average period of back-to-back launches in a CUDA graph",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                            else "fallback 6.8 TB/s",
-            "back_to_back_us": round(b2b_s * 1e6, 3),
-            "back_to_back_gbs": round(wl.gemv_bytes / b2b_s / 1e9, 2),
+            "isolated_launch_us": round(gemv_s * 1e6, 3),
+            "isolated_gbs": round(launch_bytes / gemv_s / 1e9, 2),
         },
         "e2e": {
             "value": round(e2e_units / e2e_t / 1e9, 3),
@@ -386,7 +416,7 @@ def run_ours(args, world, rank, local):
             "steps": e2e["steps"],
             "us_per_step": round(e2e_t / e2e["steps"] * 1e6, 2),
         },
-        "gpu_launches": 2 * K,
+        "gpu_launches": (1 if fused else 2) * K,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -395,16 +425,17 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def time_gemv_launches(wl, stream, n):
-    """Mean duration of n individually bracketed GEMV launches (rotated copies)."""
+def time_gemv_launches(wl, stream, n, fn=None):
+    """Mean duration of n individually bracketed launches of fn (rotated copies)."""
     import torch
+    fn = fn or wl.gemv
     try:
         evs = [(torch.cuda.Event(enable_timing=True, external=True),
                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
 
         def body(i):
             evs[i][0].record(stream)
-            wl.gemv(i)
+            fn(i)
             evs[i][1].record(stream)
         with torch.cuda.stream(stream):
             g = capture(body, n, stream)
@@ -422,17 +453,17 @@ def time_gemv_launches(wl, stream, n):
                 b = torch.cuda.Event(enable_timing=True)
                 torch.cuda._sleep(200000)
                 a.record(stream)
-                wl.gemv(i)
+                fn(i)
                 b.record(stream)
                 stream.synchronize()
                 res.append(a.elapsed_time(b))
         return float(np.mean(res[3:] if len(res) > 8 else res)) / 1e3
 
 
-def time_gemv_back_to_back(wl, stream, n):
+def time_gemv_back_to_back(wl, stream, n, fn=None):
     import torch
     with torch.cuda.stream(stream):
-        g = capture(wl.gemv, n, stream)
+        g = capture(fn or wl.gemv, n, stream)
         g.replay()
         stream.synchronize()
         a = torch.cuda.Event(enable_timing=True)
@@ -584,6 +615,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMV launch from an ncu capture of this kernel")
+    ap.add_argument("--step", choices=["fused", "split"], default="split",
+                    help="decode step as one fused launch or as producer + GEMV launches")
     ap.add_argument("--ncu-launches", type=int, default=0,
                     help="profiling entry: run one producer and N GEMV launches, no timing")
     args = ap.parse_args(argv)

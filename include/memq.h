@@ -115,13 +115,40 @@ int memq_gemv_e4m3_blk128(const uint8_t *w, const float *grid, const int8_t *qs,
 int memq_gemv_q8_0(const void *w, const int8_t *qs, const float *d, float *y, int64_t out_f,
                    int64_t in_f, int m, void *stream);
 
+/*
+ * Fused decode step: memq_rmsnorm_q8_1 on the m rows of x followed by the GEMV on the resulting
+ * q8_1 activation, as one launch.  Every CTA of the GEMV quantizes x itself (same arithmetic
+ * as memq_rmsnorm_q8_1) while its weight stream is already in flight, so the producer's latency
+ * leaves the critical path (the "two launches -> one" of q8_fuse_gate.rs, module doc, carried
+ * one stage further into the GEMV of gemv_e4m3_bench.rs).
+ *   x    device, f32 [m][in_f], 16-byte aligned;  wn  device, f32 [in_f], 16-byte aligned
+ *   eps  >= 0
+ *   qs, d  device outputs: the q8_1 activation (int8 [m][in_f], f32 [m][in_f/32]); required
+ *   z      device output f32 [m][in_f] (16-byte aligned) or NULL
+ *   y      device output f32 [m][out_f]
+ *   Weight arguments as the matching GEMV.  in_f <= MEMQ_MAX_NCOLS.  When the single-launch
+ *   plan does not apply (alignment, shared memory) the call makes the same two launches as
+ *   memq_rmsnorm_q8_1 + memq_gemv_*, with the same outputs.  out_f == 0 only produces qs / d / z.
+ */
+int memq_rmsnorm_q8_1_gemv_e4m3(const float *x, const float *wn, float eps, const uint8_t *w,
+                                const float *w_scale, int8_t *qs, float *d, float *z, float *y,
+                                int64_t out_f, int64_t in_f, int m, void *stream);
+int memq_rmsnorm_q8_1_gemv_e4m3_blk128(const float *x, const float *wn, float eps,
+                                       const uint8_t *w, const float *grid, int8_t *qs, float *d,
+                                       float *z, float *y, int64_t out_f, int64_t in_f, int m,
+                                       void *stream);
+int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps, const void *w,
+                                int8_t *qs, float *d, float *z, float *y, int64_t out_f,
+                                int64_t in_f, int m, void *stream);
+
 /* Human-readable name of a memq_status value (static storage; never NULL). */
 const char *memq_status_string(int status);
 
 /*
  * memq_device_fault -- read and clear the current device's fault word.
  * Synchronizes `stream`, then stores the word in *fault_out (0 = no fault) and resets it.
- * Bit 0: a bounded wait on a shared-memory barrier in a GEMV kernel expired.
+ * Bit 0: a GEMV consumer's bounded wait on a shared-memory barrier expired; bit 1: the GEMV
+ * producer's.  The kernel that gave up wrote nothing more and returned.
  * Returns MEMQ_ERR_NULL for a NULL fault_out, MEMQ_ERR_DEVICE if the copy fails.
  */
 int memq_device_fault(void *stream, uint32_t *fault_out);

@@ -8,7 +8,8 @@ raises.
 
 Stage 1 -- ``memq_rmsnorm_q8_1``: q8_fuse_gate.rs (memra-engine 0.125.0), the fused
 ``rms_norm_zq8_f32`` producer.  Stage 2 -- ``memq_gemv_e4m3``, ``memq_gemv_e4m3_blk128``,
-``memq_gemv_q8_0``: gemv_e4m3_bench.rs, the E4M3 / block-128 / Q8_0 arms.
+``memq_gemv_q8_0``: gemv_e4m3_bench.rs, the E4M3 / block-128 / Q8_0 arms.  The fused decode
+step ``memq_rmsnorm_q8_1_gemv_*`` runs both stages in one launch.
 """
 from __future__ import annotations
 
@@ -24,6 +25,9 @@ from ._binding import (  # noqa: F401
     memq_gemv_e4m3_blk128,
     memq_gemv_q8_0,
     memq_rmsnorm_q8_1,
+    memq_rmsnorm_q8_1_gemv_e4m3,
+    memq_rmsnorm_q8_1_gemv_e4m3_blk128,
+    memq_rmsnorm_q8_1_gemv_q8_0,
     memq_status_string,
     memq_version,
 )

@@ -54,12 +54,20 @@ def lib() -> ctypes.CDLL:
             L.memq_gemv_e4m3.argtypes = [P, P, P, P, P, I64, I64, I32, P]
             L.memq_gemv_e4m3_blk128.argtypes = [P, P, P, P, P, I64, I64, I32, P]
             L.memq_gemv_q8_0.argtypes = [P, P, P, P, I64, I64, I32, P]
+            L.memq_rmsnorm_q8_1_gemv_e4m3.argtypes = [P, P, ctypes.c_float, P, P, P, P, P, P,
+                                                      I64, I64, I32, P]
+            L.memq_rmsnorm_q8_1_gemv_e4m3_blk128.argtypes = [P, P, ctypes.c_float, P, P, P, P,
+                                                             P, P, I64, I64, I32, P]
+            L.memq_rmsnorm_q8_1_gemv_q8_0.argtypes = [P, P, ctypes.c_float, P, P, P, P, P, I64,
+                                                      I64, I32, P]
             L.memq_device_fault.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             L.memq_status_string.argtypes = [I32]
             L.memq_status_string.restype = ctypes.c_char_p
             L.memq_version.argtypes = []
             for name in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
-                         "memq_gemv_q8_0", "memq_device_fault", "memq_version"):
+                         "memq_gemv_q8_0", "memq_rmsnorm_q8_1_gemv_e4m3",
+                         "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
+                         "memq_device_fault", "memq_version"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -190,6 +198,78 @@ def memq_gemv_q8_0(w: torch.Tensor, qs: torch.Tensor, d: torch.Tensor, *, y=None
                               _stream(stream))
     _check("memq_gemv_q8_0", rc)
     return y
+
+
+def _fused_outputs(x2, m, in_f, out_f, qs, d, z, y, want_z):
+    dev = x2.device
+    if qs is None:
+        qs = torch.empty((m, in_f), dtype=torch.int8, device=dev)
+    if d is None:
+        d = torch.empty((m, in_f // 32), dtype=torch.float32, device=dev)
+    if z is None and want_z:
+        z = torch.empty((m, in_f), dtype=torch.float32, device=dev)
+    _cuda("qs", qs, torch.int8, (m, in_f))
+    _cuda("d", d, torch.float32, (m, in_f // 32))
+    if z is not None:
+        _cuda("z", z, torch.float32, (m, in_f))
+    y = _out(y, m, out_f, dev)
+    return qs, d, z, y
+
+
+def _fused_in(x, wn, in_f):
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    _cuda("x", x2, torch.float32)
+    if x2.shape[1] != in_f:
+        raise ValueError(f"x has {x2.shape[1]} columns, expected in_f={in_f}")
+    _cuda("wn", wn, torch.float32, (in_f,))
+    return x2, x2.shape[0]
+
+
+def memq_rmsnorm_q8_1_gemv_e4m3(x, wn, w, w_scale, eps: float = 1e-6, *, qs=None, d=None, z=None,
+                                y=None, want_z: bool = False, stream=None):
+    """Fused decode step, E4M3 weights.  Returns (y, qs, d, z)."""
+    _cuda("w", w, torch.uint8)
+    out_f, in_f = w.shape
+    _cuda("w_scale", w_scale, torch.float32, (1,))
+    x2, m = _fused_in(x, wn, in_f)
+    qs, d, z, y = _fused_outputs(x2, m, in_f, out_f, qs, d, z, y, want_z)
+    rc = lib().memq_rmsnorm_q8_1_gemv_e4m3(_ptr(x2), _ptr(wn), ctypes.c_float(eps), _ptr(w),
+                                           _ptr(w_scale), _ptr(qs), _ptr(d), _ptr(z), _ptr(y),
+                                           out_f, in_f, m, _stream(stream))
+    _check("memq_rmsnorm_q8_1_gemv_e4m3", rc)
+    return y, qs, d, z
+
+
+def memq_rmsnorm_q8_1_gemv_e4m3_blk128(x, wn, w, grid, eps: float = 1e-6, *, qs=None, d=None,
+                                       z=None, y=None, want_z: bool = False, stream=None):
+    """Fused decode step, block-128 E4M3 weights.  Returns (y, qs, d, z)."""
+    _cuda("w", w, torch.uint8)
+    out_f, in_f = w.shape
+    _cuda("grid", grid, torch.float32, ((out_f + 127) // 128, (in_f + 127) // 128))
+    x2, m = _fused_in(x, wn, in_f)
+    qs, d, z, y = _fused_outputs(x2, m, in_f, out_f, qs, d, z, y, want_z)
+    rc = lib().memq_rmsnorm_q8_1_gemv_e4m3_blk128(_ptr(x2), _ptr(wn), ctypes.c_float(eps), _ptr(w),
+                                                  _ptr(grid), _ptr(qs), _ptr(d), _ptr(z), _ptr(y),
+                                                  out_f, in_f, m, _stream(stream))
+    _check("memq_rmsnorm_q8_1_gemv_e4m3_blk128", rc)
+    return y, qs, d, z
+
+
+def memq_rmsnorm_q8_1_gemv_q8_0(x, wn, w, eps: float = 1e-6, *, qs=None, d=None, z=None, y=None,
+                                want_z: bool = False, stream=None):
+    """Fused decode step, Q8_0 weights.  Returns (y, qs, d, z)."""
+    _cuda("w", w, torch.uint8)
+    out_f, row_bytes = w.shape
+    if row_bytes % 34 != 0:
+        raise ValueError("Q8_0 rows must be a whole number of 34-byte blocks")
+    in_f = row_bytes // 34 * 32
+    x2, m = _fused_in(x, wn, in_f)
+    qs, d, z, y = _fused_outputs(x2, m, in_f, out_f, qs, d, z, y, want_z)
+    rc = lib().memq_rmsnorm_q8_1_gemv_q8_0(_ptr(x2), _ptr(wn), ctypes.c_float(eps), _ptr(w),
+                                           _ptr(qs), _ptr(d), _ptr(z), _ptr(y), out_f, in_f, m,
+                                           _stream(stream))
+    _check("memq_rmsnorm_q8_1_gemv_q8_0", rc)
+    return y, qs, d, z
 
 
 def memq_device_fault(stream=None) -> int:

@@ -1,0 +1,22 @@
+// memq_gemv_blk128.cu -- block-128 scale-grid E4M3 GEMV and its fused decode step.
+// Operation: gemv_e4m3_bench.rs (memra-engine 0.125.0), module doc, "THE BLOCK-128 ARM".
+#include "memq_gemv_kernels.cuh"
+
+extern "C" int memq_gemv_e4m3_blk128(const uint8_t *w, const float *grid, const int8_t *qs,
+                                     const float *d, float *y, int64_t out_f, int64_t in_f, int m,
+                                     void *stream) {
+    return memq::gemv_entry<memq::kBlk>(w, grid, qs, d, y, out_f, in_f, m, stream);
+}
+
+extern "C" int memq_rmsnorm_q8_1_gemv_e4m3_blk128(const float *x, const float *wn, float eps,
+                                                  const uint8_t *w, const float *grid, int8_t *qs,
+                                                  float *d, float *z, float *y, int64_t out_f,
+                                                  int64_t in_f, int m, void *stream) {
+    return memq::fused_entry<memq::kBlk>(x, wn, eps, w, grid, qs, d, z, y, out_f, in_f, m,
+                                         stream);
+}
+
+// Internal: this translation unit's device fault word (not part of the public header).
+int memq_internal_fault_blk128(unsigned int *out, bool clear) {
+    return memq::read_fault(out, clear) == cudaSuccess ? 0 : 1;
+}

@@ -1,4 +1,7 @@
-// memq_gemv.cu -- weight-stream GEMVs against a q8_1 activation, m <= 8 activation rows.
+// memq_gemv_kernels.cuh -- weight-stream GEMVs against a q8_1 activation, m <= 8 activation
+// rows, and the fused RMSNorm -> q8_1 -> GEMV decode step.  Included once per container by
+// memq_gemv_e4m3.cu, memq_gemv_blk128.cu and memq_gemv_q8_0.cu (one translation unit each, so
+// they compile in parallel).
 //
 // Operations: gemv_e4m3_bench.rs (memra-engine 0.125.0), module doc -- "THE COMPARISON" (arm
 // E4M3: raw E4M3 bytes, one per-tensor scale; arm Q8_0: ggml block_q8_0, 34 B per 32 weights)
@@ -28,7 +31,10 @@
 //     read the activation.
 // Generic path: a plain warp-per-row kernel with byte loads for anything the fast path does not
 // take (unaligned pointers, Q8_0 rows that are not 16-byte aligned).
+#pragma once
+
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -39,10 +45,11 @@
 
 namespace memq {
 
-// Device-side fault word (bit 0: a bounded mbarrier wait expired).  Read by memq_device_fault.
-__device__ unsigned int g_memq_fault = 0;
-
 namespace {
+
+// Device-side fault word of this translation unit (bit 0: a consumer's bounded mbarrier wait
+// expired; bit 1: the producer's).  memq_device_fault reads and clears all of them.
+__device__ unsigned int g_memq_fault = 0;
 
 constexpr int kWarps = 8;                    // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
@@ -64,6 +71,9 @@ struct Geo {
     static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
     static constexpr int kStage = kTileRows * kSlot;
     static constexpr int kMinStages = 3;
+    // Register budget: three CTAs (27 warps) per SM.  One producer thread per CTA sustains only
+    // part of an SM's share of HBM bandwidth, so more CTAs per SM stream faster.
+    static constexpr int kMinCtasPerSm = 3;
     static constexpr int kMaxStages = 8;
     static constexpr int kWarpBlocks = kChunkBlocks / kWarps;  // E4M3: blocks per warp per stage
 };
@@ -81,8 +91,14 @@ struct StreamArgs {
     int gcols;  // ceil(in_f / 128)
     int stages;
     int grid_rows;  // block-128: grid rows staged per CTA (bound)
+    // Fused decode step only: the f32 activation rows and RMSNorm weight the prologue
+    // quantizes, and where CTA 0 publishes the q8_1 activation (z optional).
+    const float *x;
+    const float *wn;
+    float eps;
+    float *z_out;
     // Shared-memory layout (bytes); barriers at 0.
-    uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_ring;
+    uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_red, off_ring;
 };
 
 // Where the consumers read the activation from.
@@ -93,6 +109,11 @@ enum ActMode : int {
 };
 
 __device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bit); }
+
+__device__ __forceinline__ void named_barrier_consumers() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarConsumers), "n"(kConsumerThreads) : "memory");
+}
+
 
 // ---------------------------------------------------------------------------------------------
 // E4M3 / block-128 stage: tensor-core inner products.
@@ -236,12 +257,111 @@ __device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *sl
 }
 
 // ---------------------------------------------------------------------------------------------
-// The stream kernel (see the file header for the schedule).
+// Fused decode step: every CTA quantizes the m activation rows itself (the RMSNorm -> q8_1
+// producer of memq_rmsnorm_q8_1 with the same per-element arithmetic: f32 per-thread sum of
+// squares, f64 across threads, IEEE f32 divide / square root, z = (x*r)*w, 8-lane block amax,
+// d = amax/127, qs = round(z/d)) into shared memory, while its producer warp already streams
+// weights.  The values are identical in every CTA; CTA 0 also writes them to qs/d (and z).
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void named_barrier_consumers() {
-    asm volatile("bar.sync %0, %1;" ::"n"(kBarConsumers), "n"(kConsumerThreads) : "memory");
+__device__ __forceinline__ int8_t quant_q8(float z, float dd) {
+    return dd != 0.0f ? static_cast<int8_t>(roundf(__fdiv_rn(z, dd))) : static_cast<int8_t>(0);
 }
 
+template <int M>
+__device__ __forceinline__ void fused_quantize(const StreamArgs &a, int8_t *s_qs, float *s_d,
+                                               double *s_red, float *s_r) {
+    const int tid = threadIdx.x;  // consumer threads 0..255
+    const int lane = tid & 31, warp = tid >> 5;
+    const int nf4 = a.in_f >> 2;
+    const bool publish = blockIdx.x == 0;
+    const float4 *w4 = reinterpret_cast<const float4 *>(a.wn);
+    // Rows up to kKeep * 1024 wide keep x in registers between the two passes (one read per
+    // CTA); wider rows read it twice (the second read hits L1).
+    constexpr int kKeep = 8;
+    const bool keep = nf4 <= kKeep * kConsumerThreads;
+    for (int j = 0; j < M; ++j) {
+        const float4 *xr = reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(j) * a.in_f);
+        float4 xk[kKeep];
+        float ss = 0.f;
+        if (keep) {
+#pragma unroll
+            for (int v = 0; v < kKeep; ++v) {
+                const int f = tid + v * kConsumerThreads;
+                xk[v] = f < nf4 ? __ldg(xr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int v = 0; v < kKeep; ++v) {
+                ss = fmaf(xk[v].x, xk[v].x, ss);
+                ss = fmaf(xk[v].y, xk[v].y, ss);
+                ss = fmaf(xk[v].z, xk[v].z, ss);
+                ss = fmaf(xk[v].w, xk[v].w, ss);
+            }
+        } else {
+            for (int f = tid; f < nf4; f += kConsumerThreads) {
+                const float4 v = __ldg(xr + f);
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+            }
+        }
+        const double s = warp_sum(static_cast<double>(ss));
+        if (lane == 0) s_red[warp] = s;
+        named_barrier_consumers();
+        if (warp == 0) {
+            double t = lane < kWarps ? s_red[lane] : 0.0;
+            t = warp_sum(t);
+            if (lane == 0)
+                *s_r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(
+                    __fdiv_rn(static_cast<float>(t), static_cast<float>(a.in_f)), a.eps)));
+        }
+        named_barrier_consumers();
+        const float r = *s_r;
+        for (int f0 = 0, v = 0; f0 < nf4; f0 += kConsumerThreads, ++v) {
+            const int f = f0 + tid;
+            const bool act = f < nf4;
+            float4 xv = make_float4(0.f, 0.f, 0.f, 0.f), wv = xv;
+            if (keep) {
+#pragma unroll
+                for (int u = 0; u < kKeep; ++u)
+                    if (u == v) xv = xk[u];
+            }
+            if (act) {
+                if (!keep) xv = __ldg(xr + f);
+                wv = __ldg(w4 + f);
+            }
+            float4 zz;
+            zz.x = __fmul_rn(__fmul_rn(xv.x, r), wv.x);
+            zz.y = __fmul_rn(__fmul_rn(xv.y, r), wv.y);
+            zz.z = __fmul_rn(__fmul_rn(xv.z, r), wv.z);
+            zz.w = __fmul_rn(__fmul_rn(xv.w, r), wv.w);
+            float am = fmaxf(fmaxf(fabsf(zz.x), fabsf(zz.y)), fmaxf(fabsf(zz.z), fabsf(zz.w)));
+            am = fmaxf(am, __shfl_xor_sync(kFullMask, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(kFullMask, am, 2));
+            am = fmaxf(am, __shfl_xor_sync(kFullMask, am, 4));
+            const float dd = __fdiv_rn(am, 127.0f);
+            if (act) {
+                const uint32_t packed =
+                    static_cast<uint32_t>(static_cast<uint8_t>(quant_q8(zz.x, dd))) |
+                    static_cast<uint32_t>(static_cast<uint8_t>(quant_q8(zz.y, dd))) << 8 |
+                    static_cast<uint32_t>(static_cast<uint8_t>(quant_q8(zz.z, dd))) << 16 |
+                    static_cast<uint32_t>(static_cast<uint8_t>(quant_q8(zz.w, dd))) << 24;
+                reinterpret_cast<uint32_t *>(s_qs + j * a.in_f)[f] = packed;
+                if ((tid & 7) == 0) s_d[j * a.nb + (f >> 3)] = dd;
+                if (publish) {
+                    reinterpret_cast<uint32_t *>(const_cast<int8_t *>(a.qs) + static_cast<int64_t>(j) * a.in_f)[f] = packed;
+                    if ((tid & 7) == 0) const_cast<float *>(a.d)[j * a.nb + (f >> 3)] = dd;
+                    if (a.z_out) reinterpret_cast<float4 *>(a.z_out + static_cast<int64_t>(j) * a.in_f)[f] = zz;
+                }
+            }
+        }
+        named_barrier_consumers();  // s_red / s_r are reused by the next row
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// The stream kernel (see the file header for the schedule).
+// ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -255,8 +375,8 @@ __device__ __forceinline__ bool thread_wait_bounded(uint64_t *bar, uint32_t pari
     return true;
 }
 
-template <int KIND, int M, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamArgs a) {
+template <int KIND, int M, int MODE, bool FUSE>
+__global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm) gemv_stream_kernel(const StreamArgs a) {
     using G = Geo<KIND>;
     constexpr int TR = G::kTileRows;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -326,7 +446,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
     griddep_wait();
     float scale = 1.0f;
     if (KIND == kE4M3) scale = __ldg(a.aux);
-    // Stage the activation (per MODE) and the block-128 grid rows this CTA touches.
+    // Stage the activation (per MODE) and the block-128 grid rows this CTA touches.  In the
+    // fused decode step the activation is computed here from x instead of read.
+    if (FUSE) {
+        double *s_red = reinterpret_cast<double *>(smem + a.off_red);  // [kWarps] + r
+        fused_quantize<M>(a, reinterpret_cast<int8_t *>(smem + a.off_qs),
+                          reinterpret_cast<float *>(smem + a.off_d), s_red,
+                          reinterpret_cast<float *>(s_red + kWarps));
+    }
     if (MODE == kActFrag) {
         // f16 MMA B fragments of the whole activation: entry (kb, g, t) holds
         // q[g][32kb + 8t .. 8t+7] as four f16x2 registers.
@@ -336,21 +463,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamAr
             const int t = i & 3;
             const int g = (i >> 2) % M;
             const int kb = (i >> 2) / M;
-            const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(
-                a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+            const uint2 qv = FUSE ? lds64(smem + a.off_qs + g * a.in_f + 32 * kb + 8 * t)
+                                  : __ldg(reinterpret_cast<const uint2 *>(
+                                        a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
             uint4 v;
             s8x4_to_f16x2x2(qv.x, v.x, v.y);
             s8x4_to_f16x2x2(qv.y, v.z, v.w);
             bfrag[i] = v;
         }
     }
-    if (MODE == kActSmem) {
+    if (MODE == kActSmem && !FUSE) {
         const uint4 *src = reinterpret_cast<const uint4 *>(a.qs);
         uint4 *dst = reinterpret_cast<uint4 *>(smem + a.off_qs);
         const int n16 = M * a.in_f / 16;
         for (int i = threadIdx.x; i < n16; i += kConsumerThreads) dst[i] = __ldg(src + i);
     }
-    if (MODE != kActGlobal) {
+    if (MODE != kActGlobal && !FUSE) {
         float *dst = reinterpret_cast<float *>(smem + a.off_d);
         for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldg(a.d + i);
     }
@@ -510,7 +638,7 @@ struct DeviceInfo {
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
-std::atomic<uint32_t> g_attr_set[kMaxDevices][3];  // bit per (M, mode): attribute set
+std::atomic<uint64_t> g_attr_set[kMaxDevices];  // bit per (M, mode, fused): attribute set
 
 bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -534,16 +662,16 @@ cudaError_t device_info(int &dev, DeviceInfo &info) {
     return info.sms > 0 ? cudaSuccess : cudaErrorInvalidDevice;
 }
 
-template <int KIND, int M, int MODE>
+template <int KIND, int M, int MODE, bool FUSE>
 cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const DeviceInfo &info,
                           cudaStream_t st) {
-    auto kern = gemv_stream_kernel<KIND, M, MODE>;
-    const uint32_t bit = 1u << ((M - 1) + 8 * MODE);
-    if (!(g_attr_set[dev][KIND].load(std::memory_order_acquire) & bit)) {
+    auto kern = gemv_stream_kernel<KIND, M, MODE, FUSE>;
+    const uint64_t bit = 1ull << ((M - 1) + 8 * MODE + (FUSE ? 24 : 0));
+    if (!(g_attr_set[dev].load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              info.smem_optin);
         if (e != cudaSuccess) return e;
-        g_attr_set[dev][KIND].fetch_or(bit, std::memory_order_acq_rel);
+        g_attr_set[dev].fetch_or(bit, std::memory_order_acq_rel);
     }
     // Ring depth: as many stages as fit when the CTAs that registers allow per SM share its
     // shared memory (more stages = more weight bytes in flight), at least kMinStages.
@@ -572,6 +700,7 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     a.off_bfrag += bars;
     a.off_qs += bars;
     a.off_d += bars;
+    a.off_red += bars;
     a.off_ring += bars;
     smem_bytes = fixed + bars + static_cast<uint32_t>(S * G::kStage);
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes);
@@ -593,110 +722,148 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int KIND, int MODE>
+template <int KIND, int MODE, bool FUSE>
 cudaError_t launch_stream_m(int m, StreamArgs a, uint32_t smem, int dev, const DeviceInfo &info,
                             cudaStream_t st) {
     switch (m) {
-        case 1: return launch_stream<KIND, 1, MODE>(a, smem, dev, info, st);
-        case 2: return launch_stream<KIND, 2, MODE>(a, smem, dev, info, st);
-        case 3: return launch_stream<KIND, 3, MODE>(a, smem, dev, info, st);
-        case 4: return launch_stream<KIND, 4, MODE>(a, smem, dev, info, st);
-        case 5: return launch_stream<KIND, 5, MODE>(a, smem, dev, info, st);
-        case 6: return launch_stream<KIND, 6, MODE>(a, smem, dev, info, st);
-        case 7: return launch_stream<KIND, 7, MODE>(a, smem, dev, info, st);
-        default: return launch_stream<KIND, 8, MODE>(a, smem, dev, info, st);
+        case 1: return launch_stream<KIND, 1, MODE, FUSE>(a, smem, dev, info, st);
+        case 2: return launch_stream<KIND, 2, MODE, FUSE>(a, smem, dev, info, st);
+        case 3: return launch_stream<KIND, 3, MODE, FUSE>(a, smem, dev, info, st);
+        case 4: return launch_stream<KIND, 4, MODE, FUSE>(a, smem, dev, info, st);
+        case 5: return launch_stream<KIND, 5, MODE, FUSE>(a, smem, dev, info, st);
+        case 6: return launch_stream<KIND, 6, MODE, FUSE>(a, smem, dev, info, st);
+        case 7: return launch_stream<KIND, 7, MODE, FUSE>(a, smem, dev, info, st);
+        default: return launch_stream<KIND, 8, MODE, FUSE>(a, smem, dev, info, st);
     }
+}
+
+// Shared-memory plan of the stream kernel.  Fixed part: tile partials (E4M3 / block-128), the
+// CTA's grid rows (block-128) and a ring of at least kMinStages stages (the barrier block and
+// the final ring depth are added at launch).  The activation is staged in shared memory when
+// that still leaves room for kMinCtasPerSm CTAs per SM -- as f16 MMA fragments (E4M3 /
+// block-128) or as int8 + scales -- else read from global memory.  The fused decode step always needs the int8 +
+// scales (it computes them there) and fails the plan if they do not fit.
+template <int KIND>
+bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo &info,
+                 StreamArgs &a, uint32_t &smem, int &mode) {
+    using G = Geo<KIND>;
+    const int nb = static_cast<int>(in_f / 32);
+    // Shared memory one CTA may use and still leave room for kMinCtasPerSm CTAs per SM.
+    const uint32_t two_per_sm = static_cast<uint32_t>(info.smem_sm / G::kMinCtasPerSm - 1024);
+    const uint32_t optin = static_cast<uint32_t>(info.smem_optin);
+    const uint32_t part = G::kMma ? align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128) : 0u;
+    // Grid rows one CTA can touch: rows per CTA at one CTA per SM, over 128, plus two.
+    const int64_t rows_cta = (out_f + info.sms - 1) / info.sms;
+    const int grid_rows = static_cast<int>(rows_cta / 128 + 2);
+    const int gcols = static_cast<int>((in_f + 127) / 128);
+    const uint32_t gridb = KIND == kBlk ? align_up(static_cast<uint32_t>(grid_rows * gcols * 4), 128) : 0u;
+    const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * 64), 128);
+    const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
+    const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
+    const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
+    const uint32_t base = part + gridb + ring_min;
+    bool with_qs = false, with_frag = false;
+    if (fuse) {
+        with_qs = true;
+        if (G::kMma && base + qsb + db + frag <= two_per_sm) {
+            mode = kActFrag;
+            with_frag = true;
+        } else if (base + qsb + db <= optin) {
+            mode = kActSmem;
+        } else {
+            return false;
+        }
+    } else {
+        if (base > optin) return false;
+        if (G::kMma && base + frag + db <= two_per_sm) {
+            mode = kActFrag;
+            with_frag = true;
+        } else if (base + qsb + db <= two_per_sm) {
+            mode = kActSmem;
+            with_qs = true;
+        } else {
+            mode = kActGlobal;
+        }
+    }
+    a.grid_rows = grid_rows;
+    a.off_part = 0;
+    a.off_grid = a.off_part + part;
+    uint32_t off = a.off_grid + gridb;
+    a.off_bfrag = off;
+    if (with_frag) off += frag;
+    a.off_qs = off;
+    if (with_qs) off += qsb;
+    a.off_d = off;
+    if (mode != kActGlobal) off += db;
+    a.off_red = off;
+    if (fuse) off += 128;  // cross-warp reduction scratch of the fused prologue
+    a.off_ring = off;
+    smem = off;  // fixed part; the ring is added in launch_stream
+    return true;
+}
+
+template <int KIND, bool FUSE>
+cudaError_t launch_planned(int m, int mode, StreamArgs a, uint32_t smem, int dev,
+                           const DeviceInfo &info, cudaStream_t st) {
+    if constexpr (Geo<KIND>::kMma) {
+        if (mode == kActFrag) return launch_stream_m<KIND, kActFrag, FUSE>(m, a, smem, dev, info, st);
+    }
+    if (mode == kActSmem) return launch_stream_m<KIND, kActSmem, FUSE>(m, a, smem, dev, info, st);
+    if constexpr (!FUSE) return launch_stream_m<KIND, kActGlobal, false>(m, a, smem, dev, info, st);
+    return cudaErrorInvalidValue;
+}
+
+template <int KIND>
+int check_gemv_args(const uint8_t *w, const float *aux, const int8_t *qs, const float *d,
+                    float *y, int64_t out_f, int64_t in_f, int m) {
+    if (m < 1 || m > MEMQ_MAX_M) return MEMQ_ERR_M_RANGE;
+    if (in_f < 32 || (in_f % 32) != 0 || in_f > (1LL << 24)) return MEMQ_ERR_SHAPE;
+    if (out_f < 0 || out_f > (1LL << 31) - 1) return MEMQ_ERR_SHAPE;
+    if (out_f == 0) return MEMQ_OK;
+    if (!w || !qs || !d || !y || (KIND != kQ80 && !aux)) return MEMQ_ERR_NULL;
+    if (!aligned(d, 4) || !aligned(y, 4) || (aux && !aligned(aux, 4))) return MEMQ_ERR_ALIGN;
+    return -1;  // valid, work to do
+}
+
+template <int KIND>
+StreamArgs base_args(const uint8_t *w, const float *aux, const int8_t *qs, const float *d,
+                     float *y, int64_t out_f, int64_t in_f) {
+    StreamArgs a = {};
+    a.w = w;
+    a.aux = aux;
+    a.qs = qs;
+    a.d = d;
+    a.y = y;
+    a.out_f = out_f;
+    a.row_bytes = (KIND == kQ80) ? in_f / 32 * 34 : in_f;
+    a.in_f = static_cast<int>(in_f);
+    a.nb = static_cast<int>(in_f / 32);
+    a.gcols = static_cast<int>((in_f + 127) / 128);
+    return a;
+}
+
+template <int KIND>
+bool fast_path_ok(const uint8_t *w, const int8_t *qs, int64_t in_f) {
+    const int64_t row_bytes = (KIND == kQ80) ? in_f / 32 * 34 : in_f;
+    return aligned(w, 16) && aligned(qs, 16) && (row_bytes % 16) == 0 &&
+           (KIND != kQ80 || ((in_f / 32) % 8) == 0);
 }
 
 template <int KIND>
 int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float *d, float *y,
                int64_t out_f, int64_t in_f, int m, void *stream) {
-    if (m < 1 || m > MEMQ_MAX_M) return MEMQ_ERR_M_RANGE;
-    if (in_f < 32 || (in_f % 32) != 0 || in_f > (1LL << 24)) return MEMQ_ERR_SHAPE;
-    if (out_f < 0 || out_f > (1LL << 31) - 1) return MEMQ_ERR_SHAPE;
-    if (out_f == 0) return MEMQ_OK;  // empty output: nothing to read or write, pointers unused
-    if (!w || !qs || !d || !y || (KIND != kQ80 && !aux)) return MEMQ_ERR_NULL;
-    if (!aligned(d, 4) || !aligned(y, 4) || (aux && !aligned(aux, 4))) return MEMQ_ERR_ALIGN;
-
+    const int rc = check_gemv_args<KIND>(w, aux, qs, d, y, out_f, in_f, m);
+    if (rc >= 0) return rc;
     int dev = 0;
     DeviceInfo info;
     if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-    const int nb = static_cast<int>(in_f / 32);
-    const int64_t row_bytes = (KIND == kQ80) ? static_cast<int64_t>(nb) * 34 : in_f;
-    using G = Geo<KIND>;
-
-    // Fast-path eligibility and shared-memory plan.  Fixed part: barriers, tile partials
-    // (E4M3 / block-128), the CTA's grid rows (block-128), and an S-stage ring.  Activation:
-    // staged in shared memory when that still leaves room for two CTAs per SM -- as f16 MMA
-    // fragments (E4M3 / block-128) or as int8 + scales -- else read from global memory.
-    bool fast = aligned(w, 16) && aligned(qs, 16) && (row_bytes % 16) == 0 &&
-                (KIND != kQ80 || (nb % 8) == 0);
-    StreamArgs a = {};
+    StreamArgs a = base_args<KIND>(w, aux, qs, d, y, out_f, in_f);
     uint32_t smem = 0;
     int mode = kActGlobal;
-    if (fast) {
-        const uint32_t two_per_sm = static_cast<uint32_t>(info.smem_sm / 2 - 1024);
-        const uint32_t part = G::kMma ? align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128) : 0u;
-        // Grid rows one CTA can touch: rows per CTA at one CTA per SM, over 128, plus two.
-        const int64_t rows_cta = (out_f + info.sms - 1) / info.sms;
-        const int grid_rows = static_cast<int>(rows_cta / 128 + 2);
-        const int gcols = static_cast<int>((in_f + 127) / 128);
-        const uint32_t gridb = KIND == kBlk ? align_up(static_cast<uint32_t>(grid_rows * gcols * 4), 128) : 0u;
-        const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * 64), 128);
-        const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
-        const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
-        const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
-        const uint32_t base = part + gridb + ring_min;
-        if (base > static_cast<uint32_t>(info.smem_optin)) {
-            fast = false;
-        } else {
-            uint32_t actb = 0;
-            if (G::kMma && base + frag + db <= two_per_sm) {
-                mode = kActFrag;
-                actb = frag + db;
-            } else if (base + qsb + db <= two_per_sm) {
-                mode = kActSmem;
-                actb = qsb + db;
-            }
-            (void)actb;
-            // Offsets without the barrier block; launch_stream shifts them once S is known.
-            a.grid_rows = grid_rows;
-            a.off_part = 0;
-            a.off_grid = a.off_part + part;
-            uint32_t off = a.off_grid + gridb;
-            a.off_bfrag = off;
-            if (mode == kActFrag) off += frag;
-            a.off_qs = off;
-            if (mode == kActSmem) off += qsb;
-            a.off_d = off;
-            if (mode != kActGlobal) off += db;
-            a.off_ring = off;
-            smem = off;  // fixed part; the ring is added in launch_stream
-        }
-    }
-
     cudaError_t e;
-    if (fast) {
-        a.w = w;
-        a.aux = aux;
-        a.qs = qs;
-        a.d = d;
-        a.y = y;
-        a.out_f = out_f;
-        a.row_bytes = row_bytes;
-        a.in_f = static_cast<int>(in_f);
-        a.nb = nb;
-        a.gcols = static_cast<int>((in_f + 127) / 128);
-        if constexpr (G::kMma) {
-            e = mode == kActFrag  ? launch_stream_m<KIND, kActFrag>(m, a, smem, dev, info, st)
-                : mode == kActSmem ? launch_stream_m<KIND, kActSmem>(m, a, smem, dev, info, st)
-                                   : launch_stream_m<KIND, kActGlobal>(m, a, smem, dev, info, st);
-        } else {
-            e = mode == kActSmem ? launch_stream_m<KIND, kActSmem>(m, a, smem, dev, info, st)
-                                 : launch_stream_m<KIND, kActGlobal>(m, a, smem, dev, info, st);
-        }
+    if (fast_path_ok<KIND>(w, qs, in_f) && plan_stream<KIND>(out_f, in_f, m, false, info, a, smem, mode)) {
+        e = launch_planned<KIND, false>(m, mode, a, smem, dev, info, st);
     } else {
         const int64_t blocks = (out_f + kGenericWarps - 1) / kGenericWarps;
         gemv_generic_kernel<KIND><<<static_cast<unsigned>(blocks), kGenericWarps * 32, 0, st>>>(
@@ -706,49 +873,55 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
     return e == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
 }
 
+// The fused decode step: RMSNorm -> q8_1 of x (m rows) and the GEMV in one launch when the plan
+// allows it, else memq_rmsnorm_q8_1 followed by the GEMV.  Either way qs / d (and z when given)
+// receive the activation.
+template <int KIND>
+int fused_entry(const float *x, const float *wn, float eps, const uint8_t *w, const float *aux,
+                int8_t *qs, float *d, float *z, float *y, int64_t out_f, int64_t in_f, int m,
+                void *stream) {
+    const int rc = check_gemv_args<KIND>(w, aux, qs, d, y, out_f, in_f, m);
+    if (rc == MEMQ_OK && out_f == 0) {
+        // Nothing to multiply; the activation is still produced.
+    } else if (rc >= 0) {
+        return rc;
+    }
+    if (in_f > MEMQ_MAX_NCOLS) return MEMQ_ERR_SHAPE;
+    if (!(eps >= 0.0f) || eps == INFINITY) return MEMQ_ERR_SHAPE;
+    if (!x || !wn || !qs || !d) return MEMQ_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(wn, 16) || (z && !aligned(z, 16)) || !aligned(qs, 4) ||
+        !aligned(d, 4))
+        return MEMQ_ERR_ALIGN;
+    int dev = 0;
+    DeviceInfo info;
+    if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (out_f > 0 && fast_path_ok<KIND>(w, qs, in_f)) {
+        StreamArgs a = base_args<KIND>(w, aux, qs, d, y, out_f, in_f);
+        a.x = x;
+        a.wn = wn;
+        a.eps = eps;
+        a.z_out = z;
+        uint32_t smem = 0;
+        int mode = kActSmem;
+        if (plan_stream<KIND>(out_f, in_f, m, true, info, a, smem, mode)) {
+            const cudaError_t e = launch_planned<KIND, true>(m, mode, a, smem, dev, info, st);
+            return e == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+        }
+    }
+    const int r = memq_rmsnorm_q8_1(x, wn, z, qs, d, in_f, m, eps, stream);
+    if (r != MEMQ_OK || out_f == 0) return r;
+    return gemv_entry<KIND>(w, aux, qs, d, y, out_f, in_f, m, stream);
+}
+
+// Reads (and optionally clears) this translation unit's device fault word.
+inline cudaError_t read_fault(unsigned int *out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_memq_fault, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_memq_fault, &zero, sizeof(zero));
+}
+
 }  // namespace
 }  // namespace memq
 
-extern "C" int memq_gemv_e4m3(const uint8_t *w, const float *w_scale, const int8_t *qs,
-                              const float *d, float *y, int64_t out_f, int64_t in_f, int m,
-                              void *stream) {
-    return memq::gemv_entry<memq::kE4M3>(w, w_scale, qs, d, y, out_f, in_f, m, stream);
-}
-
-extern "C" int memq_gemv_e4m3_blk128(const uint8_t *w, const float *grid, const int8_t *qs,
-                                     const float *d, float *y, int64_t out_f, int64_t in_f, int m,
-                                     void *stream) {
-    return memq::gemv_entry<memq::kBlk>(w, grid, qs, d, y, out_f, in_f, m, stream);
-}
-
-extern "C" int memq_gemv_q8_0(const void *w, const int8_t *qs, const float *d, float *y,
-                              int64_t out_f, int64_t in_f, int m, void *stream) {
-    return memq::gemv_entry<memq::kQ80>(static_cast<const uint8_t *>(w), nullptr, qs, d, y, out_f,
-                                        in_f, m, stream);
-}
-
-extern "C" int memq_device_fault(void *stream, uint32_t *fault_out) {
-    if (!fault_out) return MEMQ_ERR_NULL;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MEMQ_ERR_DEVICE;
-    unsigned int v = 0;
-    if (cudaMemcpyFromSymbol(&v, memq::g_memq_fault, sizeof(v)) != cudaSuccess) return MEMQ_ERR_DEVICE;
-    const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(memq::g_memq_fault, &zero, sizeof(zero)) != cudaSuccess) return MEMQ_ERR_DEVICE;
-    *fault_out = v;
-    return MEMQ_OK;
-}
-
-extern "C" const char *memq_status_string(int status) {
-    switch (status) {
-        case MEMQ_OK: return "ok";
-        case MEMQ_ERR_NULL: return "a required pointer is NULL";
-        case MEMQ_ERR_SHAPE: return "a size is out of range or not a multiple of 32";
-        case MEMQ_ERR_ALIGN: return "a pointer breaks its documented alignment";
-        case MEMQ_ERR_M_RANGE: return "m is outside [1, 8]";
-        case MEMQ_ERR_LAUNCH: return "the CUDA launch failed";
-        case MEMQ_ERR_DEVICE: return "the device fault word could not be read";
-        default: return "unknown memq status";
-    }
-}
-
-extern "C" int memq_version(void) { return (1 << 16) | 0; }

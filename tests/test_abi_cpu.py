@@ -34,8 +34,9 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
-                     "memq_gemv_q8_0", "memq_status_string", "memq_device_fault",
-                     "memq_version"):
+                     "memq_gemv_q8_0", "memq_rmsnorm_q8_1_gemv_e4m3",
+                     "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
+                     "memq_status_string", "memq_device_fault", "memq_version"):
         assert required in names
 
 
@@ -69,6 +70,12 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.memq_rmsnorm_q8_1(None, None, None, None, None, 64, 0, 1e-6, None) == m.Status.OK
     assert lib.memq_gemv_q8_0(None, None, None, None, 0, 64, 1, None) == m.Status.OK
     assert lib.memq_device_fault(None, None) == m.Status.ERR_NULL
+    # fused decode step: validation before any launch
+    assert lib.memq_rmsnorm_q8_1_gemv_q8_0(None, fake, 1e-6, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_NULL
+    assert lib.memq_rmsnorm_q8_1_gemv_e4m3(fake, fake, 1e-6, fake, fake, fake, fake, None, fake, 4, 64, 9, None) == m.Status.ERR_M_RANGE
+    assert lib.memq_rmsnorm_q8_1_gemv_e4m3_blk128(fake, fake, -1.0, fake, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_rmsnorm_q8_1_gemv_q8_0(fake, fake, 1e-6, fake, fake, fake, None, fake, 4, 65536, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_rmsnorm_q8_1_gemv_q8_0(P(0x1004), fake, 1e-6, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
