@@ -277,6 +277,91 @@ class DecodeStep:
             self.gemv(i)
 
 
+class ProducerStep:
+    """The RMSNorm -> q8_1 producer alone on rows x ncols (z written, as the fused producer of
+    q8_fuse_gate.rs emits it); several input copies when one does not exceed L2."""
+
+    def __init__(self, ncols, rows, device):
+        import torch
+        import quantized_decode_memq_gb300 as memq
+        from quantized_decode_memq_gb300 import synth
+        self.memq = memq
+        self.ncols, self.rows = ncols, rows
+        xb = rows * ncols * 4
+        self.copies = max(1, min(16, -(-2 * L2_BYTES // xb)))
+        x, wn = synth.activation_rows(ncols, rows, page_streams=rows * ncols <= 200000)
+        x0 = torch.from_numpy(x).to(device)
+        self.x = [x0] + [x0.clone() for _ in range(self.copies - 1)]
+        self.wn = torch.from_numpy(wn).to(device)
+        self.z = torch.empty((rows, ncols), dtype=torch.float32, device=device)
+        self.qs = torch.empty((rows, ncols), dtype=torch.int8, device=device)
+        self.d = torch.empty((rows, ncols // 32), dtype=torch.float32, device=device)
+        self.step_bytes = producer_bytes(rows, ncols) + rows * ncols * 4  # + z written
+        self.gemv_bytes = self.step_bytes
+        self.launches_per_step = 1
+
+    def step(self, i):
+        self.memq.memq_rmsnorm_q8_1(self.x[i % self.copies], self.wn, 1e-6, z=self.z, qs=self.qs,
+                                    d=self.d)
+
+
+class StackStep:
+    """One decode token through a synthetic 48-layer stack of block-128 E4M3 GEMVs at m = 1.
+
+    Per layer: norm(5120) -> q; G 5120->6144 and G 5120->5120 on q; norm(5120 output) -> q';
+    G 5120->17408 (gate) and G 5120->17408 (up) on q'; norm(17408 up output) -> q'';
+    G 17408->5120 on q''; its output feeds the next layer.  Every layer has its own copy of the
+    weights and grids (15.6 GB in all), so every GEMV reads DRAM."""
+
+    SHAPES = ((6144, 5120), (5120, 5120), (17408, 5120), (17408, 5120), (5120, 17408))
+
+    def __init__(self, layers, device, seed=0x57AC0000):
+        import torch
+        import quantized_decode_memq_gb300 as memq
+        from quantized_decode_memq_gb300 import synth
+        self.memq = memq
+        self.layers = layers
+        dev = device
+        base_w, base_g = [], []
+        for k, (o, i) in enumerate(self.SHAPES):
+            base_w.append(torch.from_numpy(synth.e4m3_bytes(seed + k, o, i)).to(dev))
+            base_g.append(torch.from_numpy(synth.grid_log2_uniform(seed + 16 + k, o, i)).to(dev))
+        self.w = [[bw.clone() for bw in base_w] for _ in range(layers)]
+        self.g = [[bg.clone() for bg in base_g] for _ in range(layers)]
+        del base_w, base_g
+        self.wn = [torch.from_numpy(synth.uniform_pm4(seed + 32 + k, n)).to(dev)
+                   for k, n in enumerate((5120, 5120, 17408))]
+        x, _ = synth.activation_rows(5120, 1)
+        self.x0 = torch.from_numpy(x).to(dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.y = [torch.empty((1, o), **f32) for (o, _) in self.SHAPES]
+        self.qs = [torch.empty((1, n), dtype=torch.int8, device=dev) for n in (5120, 5120, 17408)]
+        self.d = [torch.empty((1, n // 32), **f32) for n in (5120, 5120, 17408)]
+        self.gemv_bytes = sum(gemv_bytes("blk", o, i, 1) for (o, i) in self.SHAPES)
+        self.step_bytes = layers * (self.gemv_bytes + producer_bytes(1, 5120) * 2 +
+                                    producer_bytes(1, 17408))
+        self.launches_per_step = 8 * layers
+        torch.cuda.synchronize()
+
+    def layer(self, l, x):
+        m = self.memq
+        w, g, y, qs, d = self.w[l], self.g[l], self.y, self.qs, self.d
+        m.memq_rmsnorm_q8_1(x, self.wn[0], 1e-6, qs=qs[0], d=d[0], want_z=False)
+        m.memq_gemv_e4m3_blk128(w[0], g[0], qs[0], d[0], y=y[0])
+        m.memq_gemv_e4m3_blk128(w[1], g[1], qs[0], d[0], y=y[1])
+        m.memq_rmsnorm_q8_1(y[1], self.wn[1], 1e-6, qs=qs[1], d=d[1], want_z=False)
+        m.memq_gemv_e4m3_blk128(w[2], g[2], qs[1], d[1], y=y[2])
+        m.memq_gemv_e4m3_blk128(w[3], g[3], qs[1], d[1], y=y[3])
+        m.memq_rmsnorm_q8_1(y[3], self.wn[2], 1e-6, qs=qs[2], d=d[2], want_z=False)
+        m.memq_gemv_e4m3_blk128(w[4], g[4], qs[2], d[2], y=y[4])
+        return y[4]
+
+    def step(self, i):
+        x = self.x0
+        for l in range(self.layers):
+            x = self.layer(l, x)
+
+
 def capture(fn, n, stream):
     """A CUDA graph of fn(0..n-1) launched on `stream`."""
     import torch
@@ -293,6 +378,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     from quantized_decode_memq_gb300 import build
     build.build()
+    if args.workload.startswith("producer_") or args.workload.startswith("stack"):
+        return run_other(args, world, rank, local, dev)
     kind, out_f, in_f, m, copies = parse_workload(args.workload)
     fused = args.step == "fused"
     wl = DecodeStep(kind, out_f, in_f, m, copies, dev, fused=fused)
@@ -421,6 +508,65 @@ def run_ours(args, world, rank, local):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_other(args, world, rank, local, dev):
+    """Producer sweep (producer_<ncols>x<rows>) and the decode stack (stack<layers>): K steps
+    replayed from a CUDA graph, whole-step algorithmic bytes / device time."""
+    import torch
+    from quantized_decode_memq_gb300 import build
+    build.build()
+    if args.workload.startswith("producer_"):
+        ncols, rows = (int(v) for v in args.workload[len("producer_"):].split("x"))
+        wl = ProducerStep(ncols, rows, dev)
+        per_graph = wl.copies
+        desc = f"{args.workload}: RMSNorm->q8_1 producer, {rows} rows x {ncols} (z written)"
+    else:
+        layers = int(args.workload[len("stack"):] or 48)
+        wl = StackStep(layers, dev)
+        per_graph = 1
+        desc = (f"{args.workload}: one token through {layers} layers of block-128 E4M3 GEMVs "
+                f"(5120->6144, 5120->5120, 5120->17408 x2, 17408->5120) with 3 producers each")
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(per_graph):
+            wl.step(i)
+    stream.synchronize()
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        g = capture(wl.step, per_graph, stream)
+        for _ in range(max(1, -(-W // per_graph))):
+            g.replay()
+    stream.synchronize()
+    reps = max(1, -(-K // per_graph))
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    steps = reps * per_graph
+    t_max, units = aggregate(e0.elapsed_time(e1) / 1e3, float(steps * wl.step_bytes))
+    peak, peak_kind = measured_peak_hbm()
+    value = units / t_max / 1e9
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": W, "ms_per_step": t_max / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if args.workload.startswith("producer_") else "fp8",
+            "data": "synthetic",
+            "config": {"workload": desc, "step_bytes": wl.step_bytes,
+                       "timing": "steps replayed from a CUDA graph, CUDA events"},
+            "pct_of_peak": round(100.0 * value / peak, 2),
+            "gpu_launches": wl.launches_per_step * steps, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

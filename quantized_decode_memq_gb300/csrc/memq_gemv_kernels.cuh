@@ -71,9 +71,10 @@ struct Geo {
     static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
     static constexpr int kStage = kTileRows * kSlot;
     static constexpr int kMinStages = 3;
-    // Register budget: three CTAs (27 warps) per SM.  One producer thread per CTA sustains only
-    // part of an SM's share of HBM bandwidth, so more CTAs per SM stream faster.
-    static constexpr int kMinCtasPerSm = 3;
+    // Register budget: three (E4M3 / block-128) or four (Q8_0) CTAs per SM.  One producer thread
+    // per CTA sustains only part of an SM's share of HBM bandwidth, so more CTAs per SM stream
+    // faster; the tensor-core kernels need more registers per thread than Q8_0's.
+    static constexpr int kMinCtasPerSm = kMma ? 3 : 4;
     static constexpr int kMaxStages = 8;
     static constexpr int kWarpBlocks = kChunkBlocks / kWarps;  // E4M3: blocks per warp per stage
 };

@@ -1,0 +1,74 @@
+"""GPU parity of the decode chain layered like a transformer block, teacher-forced per stage.
+
+Each layer: RMSNorm -> q8_1 on the 5120-wide input; block-128 E4M3 GEMVs 5120->6144 and
+5120->5120 on it; RMSNorm -> q8_1 of the 5120 output; GEMVs 5120->17408 (gate, up) on that;
+RMSNorm -> q8_1 of the 17408 up output; GEMV 17408->5120, whose output feeds the next layer.
+All launches go back to back on one stream, as in a decode step.  Each stage is then checked
+against the oracle fed the GPU's own inputs to that stage (the previous stage's GPU output), so
+one stage's rounding never counts against the next.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import check_gemv, check_producer, sample_rows, to_dev
+from quantized_decode_memq_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+EPS = float(np.float32(1e-6))
+SHAPES = ((6144, 5120), (5120, 5120), (17408, 5120), (17408, 5120), (5120, 17408))
+# (norm input, GEMVs fed by that norm): norm k reads the output of GEMV SRC[k]
+NORMS = ((None, (0, 1)), (1, (2, 3)), (3, (4,)))
+
+
+@pytest.fixture(scope="module")
+def memq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_decode_memq_gb300 import build
+    build.build()
+    import quantized_decode_memq_gb300 as m
+    return m
+
+
+def test_two_layer_chain_teacher_forced(memq, oracle):
+    layers = 2
+    w = [[synth.e4m3_bytes(0x5A00 + 8 * l + k, o, i) for k, (o, i) in enumerate(SHAPES)]
+         for l in range(layers)]
+    g = [[synth.grid_log2_uniform(0x5B00 + 8 * l + k, o, i) for k, (o, i) in enumerate(SHAPES)]
+         for l in range(layers)]
+    wn = [synth.uniform_pm4(0x5C00 + k, n) for k, n in enumerate((5120, 5120, 17408))]
+    x0, _ = synth.activation_rows(5120, 1)
+    wd = [[to_dev(a) for a in row] for row in w]
+    gd = [[to_dev(a) for a in row] for row in g]
+    wnd = [to_dev(a) for a in wn]
+
+    # run every layer back to back, keeping each stage's output for the checks
+    outs = []
+    x = to_dev(x0)
+    for l in range(layers):
+        ys, acts, ins = [None] * 5, [], []
+        for k, (src, gemvs) in enumerate(NORMS):
+            inp = x if src is None else ys[src]
+            ins.append(inp)
+            z, qs, d = memq.memq_rmsnorm_q8_1(inp, wnd[k], EPS)
+            acts.append((z, qs, d))
+            for j in gemvs:
+                ys[j] = memq.memq_gemv_e4m3_blk128(wd[l][j], gd[l][j], qs, d)
+        outs.append((ins, acts, ys))
+        x = ys[4]
+    torch.cuda.synchronize()
+    assert memq.memq_device_fault() == 0
+
+    for l, (ins, acts, ys) in enumerate(outs):
+        for k, (src, gemvs) in enumerate(NORMS):
+            xin = ins[k].cpu().numpy().reshape(1, -1)
+            assert np.all(np.isfinite(xin))
+            z, qs, d = acts[k]
+            check_producer(oracle, xin, wn[k], EPS, z, qs, d)
+            qs_h, d_h = qs.cpu().numpy(), d.cpu().numpy()
+            for j in gemvs:
+                rows = sample_rows(SHAPES[j][0], 128, seed=l * 8 + j)
+                y_ref, s_ref = oracle.gemv_e4m3_blk128(w[l][j], g[l][j], qs_h, d_h, rows=rows)
+                check_gemv(ys[j], y_ref, s_ref, rows=rows)
