@@ -17,6 +17,12 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // has completed and its writes are visible (a no-op when the launch carried no programmatic
 // dependency).  `griddep_launch_dependents` lets the next launch in the stream begin its
 // prologue early; that launch still waits for this grid before reading what it wrote.
+//
+// Because the kernels here release their successor at entry, a launch's lifetime overlaps the
+// end of its predecessor's.  Data the predecessor writes (the activation x, the q8_1 qs / d) is
+// therefore NOT constant over the reader's lifetime and must not go through the non-coherent
+// read-only path (ld.global.nc / __ldg): it is read after griddep_wait with L2-coherent loads
+// (__ldcg).  __ldg stays for true constants (weights, scale grids, the RMSNorm weight).
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
@@ -97,6 +103,22 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Tiled 2-D tensor copy global -> shared (TMA): the box of the tensor map `map` (a generic
+// address of a __grid_constant__ kernel parameter) at element coordinates (x, y), completing
+// on `bar`.  The destination must be 128-byte aligned and x * element size a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *map, int x, int y,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const void *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // ---------------------------------------------------------------------------------------------

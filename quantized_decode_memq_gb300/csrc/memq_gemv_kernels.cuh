@@ -37,6 +37,7 @@
 #include <cmath>
 #include <atomic>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <mutex>
 
@@ -100,6 +101,18 @@ struct StreamArgs {
     float *z_out;
     // Shared-memory layout (bytes); barriers at 0.
     uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_red, off_ring;
+    int use_tma;  // 1: full tiles (and 8-row halves) come as one tensor copy each
+};
+
+// Tensor maps over the weight plane viewed as [out_f rows][row_bytes / 8] 64-bit elements, box
+// = one chunk slot (kSlot bytes, i.e. the 1 KB / 1088 B chunk plus the row padding of the shared
+// layout) x `rows`: `tile` covers a whole tile, `oct` 8 rows.  A box lands in shared memory as
+// rows of kSlot bytes, exactly the ring's stage layout; columns past the end of a row read as
+// zero and rows past out_f too.  The padding columns of a chunk overlap the next chunk of the
+// same row (they are never used).
+struct TmaMaps {
+    CUtensorMap tile;
+    CUtensorMap oct;
 };
 
 // Where the consumers read the activation from.
@@ -164,7 +177,7 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
                 } else {
                     const uint2 qv = MODE == kActSmem
                                          ? lds64(s_qs + g * a.in_f + 32 * kb + 8 * t)
-                                         : __ldg(reinterpret_cast<const uint2 *>(
+                                         : __ldcg(reinterpret_cast<const uint2 *>(
                                                a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
                     s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
                     s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
@@ -172,8 +185,8 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
             }
             float k0 = 0.f, k1 = 0.f;
             if (MODE == kActGlobal) {
-                if (2 * t < M) k0 = __ldg(a.d + (2 * t) * a.nb + kb);
-                if (2 * t + 1 < M) k1 = __ldg(a.d + (2 * t + 1) * a.nb + kb);
+                if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
+                if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
             } else {
                 if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
                 if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
@@ -240,9 +253,9 @@ __device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *sl
             dj = s_d[j * a.nb + kb];
         } else {
             const uint4 *qx = reinterpret_cast<const uint4 *>(a.qs + static_cast<int64_t>(j) * a.in_f + 32 * kb);
-            x0 = __ldg(qx);
-            x1 = __ldg(qx + 1);
-            dj = __ldg(a.d + j * a.nb + kb);
+            x0 = __ldcg(qx);
+            x1 = __ldcg(qx + 1);
+            dj = __ldcg(a.d + j * a.nb + kb);
         }
         int s = 0;
         s = __dp4a(static_cast<int>(qw[0]), static_cast<int>(x0.x), s);
@@ -288,7 +301,7 @@ __device__ __forceinline__ void fused_quantize(const StreamArgs &a, int8_t *s_qs
 #pragma unroll
             for (int v = 0; v < kKeep; ++v) {
                 const int f = tid + v * kConsumerThreads;
-                xk[v] = f < nf4 ? __ldg(xr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xk[v] = f < nf4 ? __ldcg(xr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int v = 0; v < kKeep; ++v) {
@@ -299,7 +312,7 @@ __device__ __forceinline__ void fused_quantize(const StreamArgs &a, int8_t *s_qs
             }
         } else {
             for (int f = tid; f < nf4; f += kConsumerThreads) {
-                const float4 v = __ldg(xr + f);
+                const float4 v = __ldcg(xr + f);
                 ss = fmaf(v.x, v.x, ss);
                 ss = fmaf(v.y, v.y, ss);
                 ss = fmaf(v.z, v.z, ss);
@@ -328,7 +341,7 @@ __device__ __forceinline__ void fused_quantize(const StreamArgs &a, int8_t *s_qs
                     if (u == v) xv = xk[u];
             }
             if (act) {
-                if (!keep) xv = __ldg(xr + f);
+                if (!keep) xv = __ldcg(xr + f);
                 wv = __ldg(w4 + f);
             }
             float4 zz;
@@ -377,7 +390,8 @@ __device__ __forceinline__ bool thread_wait_bounded(uint64_t *bar, uint32_t pari
 }
 
 template <int KIND, int M, int MODE, bool FUSE>
-__global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm) gemv_stream_kernel(const StreamArgs a) {
+__global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
+    gemv_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMaps tm) {
     using G = Geo<KIND>;
     constexpr int TR = G::kTileRows;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -411,6 +425,13 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm) gemv_strea
         // ------------------------------- producer warp ---------------------------------------
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
+            // Tensor copies need 128-byte aligned destinations: every stage base is, given a
+            // 128-byte aligned ring (checked here, else rows are copied one by one).
+            const bool use_tma = a.use_tma && (smem_u32(ring) & 127u) == 0;
+            if (use_tma) {
+                tma_prefetch_map(&tm.tile);
+                if (TR > 8) tma_prefetch_map(&tm.oct);
+            }
             int tile = 0, ch = 0, s = 0;
             uint32_t eph = 0;  // parity of the empty-barrier phase awaited before a reuse
             for (int it = 0; it < items; ++it) {
@@ -423,10 +444,19 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm) gemv_strea
                 const int kb = ch * G::kChunkBlocks;
                 const int nblk = min(G::kChunkBlocks, a.nb - kb);
                 const uint32_t bytes = static_cast<uint32_t>(nblk * G::kBlockBytes);
-                mbar_arrive_expect_tx(&full[s], bytes * rc);
                 const uint8_t *src = a.w + r0 * a.row_bytes + static_cast<int64_t>(kb) * G::kBlockBytes;
                 uint8_t *dst = ring + s * G::kStage;
-                for (int rr = 0; rr < rc; ++rr)
+                // Rows [0, boxed) come as tensor copies (whole tile, or its first 8 rows: both
+                // land 128-byte aligned), the rest row by row.
+                const int boxed = !use_tma ? 0 : rc == TR ? TR : rc >= 8 ? 8 : 0;
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(boxed * G::kSlot) +
+                                                    bytes * static_cast<uint32_t>(rc - boxed));
+                const int tx = kb * G::kBlockBytes / 8;
+                if (boxed == TR)
+                    tma_load_2d(dst, &tm.tile, tx, static_cast<int>(r0), &full[s], pol);
+                else if (boxed == 8)
+                    tma_load_2d(dst, &tm.oct, tx, static_cast<int>(r0), &full[s], pol);
+                for (int rr = boxed; rr < rc; ++rr)
                     bulk_g2s(dst + rr * G::kSlot, src + rr * a.row_bytes, bytes, &full[s], pol);
                 if (++ch == nch) {
                     ch = 0;
@@ -465,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm) gemv_strea
             const int g = (i >> 2) % M;
             const int kb = (i >> 2) / M;
             const uint2 qv = FUSE ? lds64(smem + a.off_qs + g * a.in_f + 32 * kb + 8 * t)
-                                  : __ldg(reinterpret_cast<const uint2 *>(
+                                  : __ldcg(reinterpret_cast<const uint2 *>(
                                         a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
             uint4 v;
             s8x4_to_f16x2x2(qv.x, v.x, v.y);
@@ -477,11 +507,11 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm) gemv_strea
         const uint4 *src = reinterpret_cast<const uint4 *>(a.qs);
         uint4 *dst = reinterpret_cast<uint4 *>(smem + a.off_qs);
         const int n16 = M * a.in_f / 16;
-        for (int i = threadIdx.x; i < n16; i += kConsumerThreads) dst[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < n16; i += kConsumerThreads) dst[i] = __ldcg(src + i);
     }
     if (MODE != kActGlobal && !FUSE) {
         float *dst = reinterpret_cast<float *>(smem + a.off_d);
-        for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldg(a.d + i);
+        for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldcg(a.d + i);
     }
     const int64_t grow_base = R0 >> 7;
     if (KIND == kBlk) {
@@ -663,6 +693,51 @@ cudaError_t device_info(int &dev, DeviceInfo &info) {
     return info.sms > 0 ? cudaSuccess : cudaErrorInvalidDevice;
 }
 
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime once per process (the
+// library does not link the driver API directly).  Null when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Builds the two tensor maps of the weight plane (see TmaMaps) and sets a.use_tma; on any
+// failure the producer copies every row with its own bulk copy instead.
+template <int KIND>
+void make_maps(StreamArgs &a, TmaMaps &tm) {
+    using G = Geo<KIND>;
+    a.use_tma = 0;
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc || a.row_bytes % 16 != 0 || a.out_f > (1ll << 31) - 1) return;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.row_bytes / 8),
+                                static_cast<cuuint64_t>(a.out_f)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.row_bytes)};
+    const cuuint32_t estr[2] = {1, 1};
+    const int heights[2] = {G::kTileRows, 8};
+    CUtensorMap *maps[2] = {&tm.tile, &tm.oct};
+    for (int i = 0; i < 2; ++i) {
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(G::kSlot / 8),
+                                   static_cast<cuuint32_t>(heights[i])};
+        if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(a.w), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return;
+    }
+    a.use_tma = 1;
+}
+
 template <int KIND, int M, int MODE, bool FUSE>
 cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const DeviceInfo &info,
                           cudaStream_t st) {
@@ -720,7 +795,9 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    TmaMaps tm = {};
+    make_maps<KIND>(a, tm);
+    return cudaLaunchKernelEx(&cfg, kern, a, tm);
 }
 
 template <int KIND, int MODE, bool FUSE>

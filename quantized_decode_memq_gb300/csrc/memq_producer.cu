@@ -5,8 +5,9 @@
 // that emits f32 z, int8 qs and one f32 scale per 32-element block.
 //
 // Design (one CTA per row, the row held in registers):
-//   * each thread owns V float4 slices of x (and, up to V = 8, of w), loaded once: x streamed
-//     with an L1 no-allocate load, w through the read-only path since every row shares it;
+//   * each thread owns V float4 slices of x (and, up to V = 8, of w), loaded once: x with an
+//     L2-coherent load (it is typically the previous launch's output, see memq_dev.cuh), w
+//     through the read-only path since every row shares it;
 //   * sum of x^2: f32 per thread, f64 across threads (warp shuffles + a shared-memory step),
 //     then r = 1/sqrt(ss/ncols + eps) with IEEE f32 divide and square root;
 //   * z = (x*r)*w in f32; a 32-element block is 8 consecutive float4 slices, i.e. 8 adjacent
@@ -23,14 +24,6 @@
 
 namespace memq {
 namespace {
-
-__device__ __forceinline__ float4 ld_stream_f4(const float4 *p) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 __device__ __forceinline__ int8_t quant1(float z, float dd) {
     return dd != 0.0f ? static_cast<int8_t>(roundf(__fdiv_rn(z, dd))) : static_cast<int8_t>(0);
@@ -66,7 +59,7 @@ __global__ void __launch_bounds__(V <= 8 ? 256 : 512)
     for (int v = 0; v < V; ++v) {
         const int f = tid + v * nthr;
         if (f < nf4) {
-            xv[v] = ld_stream_f4(xr + f);
+            xv[v] = __ldcg(xr + f);
             if (kKeepW) wv[kKeepW ? v : 0] = __ldg(w4 + f);
         } else {
             xv[v] = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -72,3 +72,33 @@ def test_two_layer_chain_teacher_forced(memq, oracle):
                 rows = sample_rows(SHAPES[j][0], 128, seed=l * 8 + j)
                 y_ref, s_ref = oracle.gemv_e4m3_blk128(w[l][j], g[l][j], qs_h, d_h, rows=rows)
                 check_gemv(ys[j], y_ref, s_ref, rows=rows)
+
+
+def test_repeated_gemv_to_norm_handoff(memq, oracle):
+    """A GEMV followed at once by the RMSNorm of its output, 40 times, launched back to back.
+
+    Every launch releases its successor at entry, so each RMSNorm starts while the GEMV before
+    it is still finishing; it must read the GEMV's final output.  Each z is checked against the
+    oracle on the GEMV output as read back afterwards (both widths of the producer kernel)."""
+    reps = 40
+    w_up = to_dev(synth.e4m3_bytes(0x5D00, 17408, 5120))
+    g_up = to_dev(synth.grid_log2_uniform(0x5D01, 17408, 5120))
+    w_dn = to_dev(synth.e4m3_bytes(0x5D02, 5120, 17408))
+    g_dn = to_dev(synth.grid_log2_uniform(0x5D03, 5120, 17408))
+    wn_up = synth.uniform_pm4(0x5D04, 17408)
+    wn_dn = synth.uniform_pm4(0x5D05, 5120)
+    wn_up_d, wn_dn_d = to_dev(wn_up), to_dev(wn_dn)
+    x0, _ = synth.activation_rows(5120, 1)
+    _, qs, d = memq.memq_rmsnorm_q8_1(to_dev(x0), wn_dn_d, EPS)
+    keep = []
+    for _ in range(reps):
+        y_up = memq.memq_gemv_e4m3_blk128(w_up, g_up, qs, d)
+        z1, qs1, d1 = memq.memq_rmsnorm_q8_1(y_up, wn_up_d, EPS)
+        y_dn = memq.memq_gemv_e4m3_blk128(w_dn, g_dn, qs1, d1)
+        z2, qs, d = memq.memq_rmsnorm_q8_1(y_dn, wn_dn_d, EPS)
+        keep.append((y_up, z1, qs1, d1, y_dn, z2, qs, d))
+    torch.cuda.synchronize()
+    assert memq.memq_device_fault() == 0
+    for y_up, z1, qs1, d1, y_dn, z2, qs2, d2 in keep:
+        check_producer(oracle, y_up.cpu().numpy(), wn_up, EPS, z1, qs1, d1)
+        check_producer(oracle, y_dn.cpu().numpy(), wn_dn, EPS, z2, qs2, d2)
