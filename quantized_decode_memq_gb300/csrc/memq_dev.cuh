@@ -121,6 +121,15 @@ __device__ __forceinline__ void tma_prefetch_map(const void *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// As bulk_g2s, with the default L2 policy.
+__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes,
+                                               uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // Shared-memory loads.  Plain C++ loads (not volatile asm), so the compiler can interleave
 // independent blocks while still ordering them after the barrier waits, which clobber memory.

@@ -67,15 +67,17 @@ template <int KIND>
 struct Geo {
     static constexpr bool kMma = KIND != kQ80;
     static constexpr int kBlockBytes = kMma ? 32 : 34;
-    static constexpr int kTileRows = kMma ? 16 : 8;
+    static constexpr int kTileRows = kMma ? 16 : kWarps;  // Q8_0: one row per consumer warp
     static constexpr int kChunkBlocks = 32;
     static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
     static constexpr int kStage = kTileRows * kSlot;
     static constexpr int kMinStages = 3;
-    // Register budget: three (E4M3 / block-128) or four (Q8_0) CTAs per SM.  One producer thread
-    // per CTA sustains only part of an SM's share of HBM bandwidth, so more CTAs per SM stream
-    // faster; the tensor-core kernels need more registers per thread than Q8_0's.
+    // Register budget: three (E4M3 / block-128) or four (Q8_0) CTAs per SM.  More CTAs per SM
+    // keep more weight bytes in flight per SM; the tensor-core kernels need more registers per
+    // thread than Q8_0's.
     static constexpr int kMinCtasPerSm = kMma ? 3 : 4;
+    // CTAs per SM one launch uses (at most kMinCtasPerSm).
+    static constexpr int kCtasPerLaunch = kMinCtasPerSm;
     static constexpr int kMaxStages = 8;
     static constexpr int kWarpBlocks = kChunkBlocks / kWarps;  // E4M3: blocks per warp per stage
 };
@@ -102,6 +104,7 @@ struct StreamArgs {
     // Shared-memory layout (bytes); barriers at 0.
     uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_red, off_ring;
     int use_tma;  // 1: full tiles (and 8-row halves) come as one tensor copy each
+    int ctas_per_sm;  // host: CTAs per SM the plan sized shared memory for
 };
 
 // Tensor maps over the weight plane viewed as [out_f rows][row_bytes / 8] 64-bit elements, box
@@ -409,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + S;
+    uint64_t *act_bar = full + 2 * S;  // the activation's bulk copies
     uint8_t *ring = smem + a.off_ring;
     float *part = reinterpret_cast<float *>(smem + a.off_part);  // [2][kWarps][TR][M]
 
@@ -417,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
         }
+        mbar_init(act_bar, 1);
         mbar_init_fence();
     }
     __syncthreads();
@@ -474,16 +479,48 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
     }
 
     // --------------------------------- consumer warps ------------------------------------------
-    griddep_wait();
+    // Constants first (the per-tensor scale, the block-128 grid rows this CTA touches): they do
+    // not depend on the preceding launch, so they are staged while it finishes.
     float scale = 1.0f;
     if (KIND == kE4M3) scale = __ldg(a.aux);
-    // Stage the activation (per MODE) and the block-128 grid rows this CTA touches.  In the
-    // fused decode step the activation is computed here from x instead of read.
+    const int64_t grow_base = R0 >> 7;
+    if (KIND == kBlk) {
+        float *dst = reinterpret_cast<float *>(smem + a.off_grid);
+        const int nrows = static_cast<int>(((R1 - 1) >> 7) - grow_base + 1);
+        const int n = nrows * a.gcols;
+        for (int i = threadIdx.x; i < n; i += kConsumerThreads)
+            dst[i] = __ldg(a.aux + grow_base * a.gcols + i);
+    }
+    griddep_wait();
+    bool ok = true;
+    // The activation (written by the preceding launch): qs and d into shared memory with one
+    // bulk copy each (one L2 round trip), or computed here in the fused decode step.
     if (FUSE) {
         double *s_red = reinterpret_cast<double *>(smem + a.off_red);  // [kWarps] + r
         fused_quantize<M>(a, reinterpret_cast<int8_t *>(smem + a.off_qs),
                           reinterpret_cast<float *>(smem + a.off_d), s_red,
                           reinterpret_cast<float *>(s_red + kWarps));
+    } else if (MODE != kActGlobal) {
+        const uint32_t qbytes = static_cast<uint32_t>(M * a.in_f);
+        const uint32_t dbytes = static_cast<uint32_t>(M * a.nb * 4);
+        const bool d_bulk = (dbytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.d) & 15u) == 0;
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(act_bar, qbytes + (d_bulk ? dbytes : 0u));
+            bulk_g2s_plain(smem + a.off_qs, a.qs, qbytes, act_bar);
+            if (d_bulk) bulk_g2s_plain(smem + a.off_d, a.d, dbytes, act_bar);
+        }
+        if (!d_bulk) {
+            float *dst = reinterpret_cast<float *>(smem + a.off_d);
+            for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldcg(a.d + i);
+        }
+        if (!warp_wait_bounded(act_bar, 0)) {
+            // Record the fault; give the activation copy and the ring's first stages a bounded
+            // chance to land before the CTA stops consuming (and eventually exits).
+            if (lane == 0) fault(1u);
+            (void)warp_wait_bounded(act_bar, 0);
+            for (int j = 0; j < min(items, S); ++j) (void)warp_wait_bounded(&full[j], 0);
+            ok = false;
+        }
     }
     if (MODE == kActFrag) {
         // f16 MMA B fragments of the whole activation: entry (kb, g, t) holds
@@ -494,36 +531,15 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
             const int t = i & 3;
             const int g = (i >> 2) % M;
             const int kb = (i >> 2) / M;
-            const uint2 qv = FUSE ? lds64(smem + a.off_qs + g * a.in_f + 32 * kb + 8 * t)
-                                  : __ldcg(reinterpret_cast<const uint2 *>(
-                                        a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+            const uint2 qv = lds64(smem + a.off_qs + g * a.in_f + 32 * kb + 8 * t);
             uint4 v;
             s8x4_to_f16x2x2(qv.x, v.x, v.y);
             s8x4_to_f16x2x2(qv.y, v.z, v.w);
             bfrag[i] = v;
         }
     }
-    if (MODE == kActSmem && !FUSE) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.qs);
-        uint4 *dst = reinterpret_cast<uint4 *>(smem + a.off_qs);
-        const int n16 = M * a.in_f / 16;
-        for (int i = threadIdx.x; i < n16; i += kConsumerThreads) dst[i] = __ldcg(src + i);
-    }
-    if (MODE != kActGlobal && !FUSE) {
-        float *dst = reinterpret_cast<float *>(smem + a.off_d);
-        for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldcg(a.d + i);
-    }
-    const int64_t grow_base = R0 >> 7;
-    if (KIND == kBlk) {
-        float *dst = reinterpret_cast<float *>(smem + a.off_grid);
-        const int nrows = static_cast<int>(((R1 - 1) >> 7) - grow_base + 1);
-        const int n = nrows * a.gcols;
-        for (int i = threadIdx.x; i < n; i += kConsumerThreads)
-            dst[i] = __ldg(a.aux + grow_base * a.gcols + i);
-    }
     named_barrier_consumers();
 
-    bool ok = true;
     int c_stage = 0;
     uint32_t c_phase = 0;
     int consumed = 0;
@@ -757,10 +773,10 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, kern, kThreads, fixed + G::kMinStages * (G::kStage + 16) + 128);
     if (e != cudaSuccess) return e;
-    per_sm = std::max(per_sm, 1);
+    per_sm = std::max(std::min({per_sm, G::kMinCtasPerSm, a.ctas_per_sm}), 1);
     int S = G::kMinStages;
     for (int s = G::kMaxStages; s >= G::kMinStages; --s) {
-        const uint32_t need = fixed + align_up(static_cast<uint32_t>(2 * s * 8), 128) +
+        const uint32_t need = fixed + align_up(static_cast<uint32_t>((2 * s + 1) * 8), 128) +
                               static_cast<uint32_t>(s * G::kStage);
         if (need <= static_cast<uint32_t>(info.smem_optin) &&
             static_cast<int64_t>(need + 1024) * per_sm <= info.smem_sm) {
@@ -768,7 +784,7 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
             break;
         }
     }
-    const uint32_t bars = align_up(static_cast<uint32_t>(2 * S * 8), 128);
+    const uint32_t bars = align_up(static_cast<uint32_t>((2 * S + 1) * 8), 128);
     // Shift every region past the barriers.
     a.stages = S;
     a.off_part += bars;
@@ -783,7 +799,7 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     if (e != cudaSuccess) return e;
     per_sm = std::max(per_sm, 1);
     // One wave of CTAs, never more CTAs than output rows.
-    int64_t grid = static_cast<int64_t>(info.sms) * per_sm;
+    int64_t grid = static_cast<int64_t>(info.sms) * std::min({per_sm, G::kCtasPerLaunch, a.ctas_per_sm});
     grid = std::min<int64_t>(grid, a.out_f);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -816,18 +832,18 @@ cudaError_t launch_stream_m(int m, StreamArgs a, uint32_t smem, int dev, const D
 }
 
 // Shared-memory plan of the stream kernel.  Fixed part: tile partials (E4M3 / block-128), the
-// CTA's grid rows (block-128) and a ring of at least kMinStages stages (the barrier block and
-// the final ring depth are added at launch).  The activation is staged in shared memory when
-// that still leaves room for kMinCtasPerSm CTAs per SM -- as f16 MMA fragments (E4M3 /
-// block-128) or as int8 + scales -- else read from global memory.  The fused decode step always needs the int8 +
-// scales (it computes them there) and fails the plan if they do not fit.
+// CTA's grid rows (block-128), the staged activation, and a ring of at least kMinStages stages
+// (the barrier block and the final ring depth are added at launch).  The activation lives in
+// shared memory -- int8 qs + scales, plus its f16 MMA fragments for E4M3 / block-128 when they
+// also fit -- and the plan takes the largest CTA count per SM (at most kMinCtasPerSm) for which
+// that fits; only an activation too large for one CTA per SM is read from global memory.  The
+// fused decode step always needs the int8 + scales there (it computes them) and fails the plan
+// if they do not fit.
 template <int KIND>
 bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo &info,
                  StreamArgs &a, uint32_t &smem, int &mode) {
     using G = Geo<KIND>;
     const int nb = static_cast<int>(in_f / 32);
-    // Shared memory one CTA may use and still leave room for kMinCtasPerSm CTAs per SM.
-    const uint32_t two_per_sm = static_cast<uint32_t>(info.smem_sm / G::kMinCtasPerSm - 1024);
     const uint32_t optin = static_cast<uint32_t>(info.smem_optin);
     const uint32_t part = G::kMma ? align_up(static_cast<uint32_t>(2 * kWarps * G::kTileRows * m * 4), 128) : 0u;
     // Grid rows one CTA can touch: rows per CTA at one CTA per SM, over 128, plus two.
@@ -838,43 +854,39 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * 64), 128);
     const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
     const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
+    const uint32_t red = fuse ? align_up((kWarps + 1) * 8, 128) : 0u;
     const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
-    const uint32_t base = part + gridb + ring_min;
-    bool with_qs = false, with_frag = false;
-    if (fuse) {
-        with_qs = true;
-        if (G::kMma && base + qsb + db + frag <= two_per_sm) {
+    const uint32_t base = part + gridb + red + ring_min;
+    if (base > optin) return false;
+    int ctas = G::kMinCtasPerSm;
+    mode = kActGlobal;
+    for (int k = G::kMinCtasPerSm; k >= 1; --k) {
+        // Shared memory one CTA may use and still leave room for k CTAs per SM.
+        const uint32_t budget = std::min(optin, static_cast<uint32_t>(info.smem_sm / k - 1024));
+        if (G::kMma && base + qsb + db + frag <= budget) {
             mode = kActFrag;
-            with_frag = true;
-        } else if (base + qsb + db <= optin) {
+        } else if (base + qsb + db <= budget) {
             mode = kActSmem;
         } else {
-            return false;
+            continue;
         }
-    } else {
-        if (base > optin) return false;
-        if (G::kMma && base + frag + db <= two_per_sm) {
-            mode = kActFrag;
-            with_frag = true;
-        } else if (base + qsb + db <= two_per_sm) {
-            mode = kActSmem;
-            with_qs = true;
-        } else {
-            mode = kActGlobal;
-        }
+        ctas = k;
+        break;
     }
+    if (fuse && mode == kActGlobal) return false;
     a.grid_rows = grid_rows;
+    a.ctas_per_sm = ctas;
     a.off_part = 0;
     a.off_grid = a.off_part + part;
     uint32_t off = a.off_grid + gridb;
     a.off_bfrag = off;
-    if (with_frag) off += frag;
+    if (mode == kActFrag) off += frag;
     a.off_qs = off;
-    if (with_qs) off += qsb;
+    if (mode != kActGlobal) off += qsb;
     a.off_d = off;
     if (mode != kActGlobal) off += db;
     a.off_red = off;
-    if (fuse) off += 128;  // cross-warp reduction scratch of the fused prologue
+    off += red;  // cross-warp scratch of the fused prologue
     a.off_ring = off;
     smem = off;  // fixed part; the ring is added in launch_stream
     return true;

@@ -249,3 +249,42 @@ def test_repeat_calls_deterministic_and_no_fault(memq, oracle):
         b = gpu_gemv(memq, kind, w, aux, qs, d)
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     assert memq.memq_device_fault() == 0
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("m", [1, 8])
+def test_graph_back_to_back_launches(memq, oracle, kind, m):
+    """Six GEMVs captured in one CUDA graph and replayed twice, as the benchmark times them:
+    consecutive launches overlap (each releases the next at entry).  Every launch has its own
+    weights and output; each output is checked on sampled rows."""
+    out_f, in_f, n = 17408, 5120, 6
+    qs, d = act(oracle, m, in_f, 77)
+    qs_d, d_d = to_dev(qs), to_dev(d)
+    ws = [weights(kind, out_f, in_f, 900 + i) for i in range(n)]
+    wd = [(to_dev(w), None if aux is None else to_dev(aux)) for w, aux in ws]
+    ys = [torch.full((m, out_f), float("nan"), device="cuda") for _ in range(n)]
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+
+    def launch(i):
+        w, aux = wd[i]
+        if kind == "q8_0":
+            memq.memq_gemv_q8_0(w, qs_d, d_d, y=ys[i])
+        elif kind == "blk":
+            memq.memq_gemv_e4m3_blk128(w, aux, qs_d, d_d, y=ys[i])
+        else:
+            memq.memq_gemv_e4m3(w, aux, qs_d, d_d, y=ys[i])
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for i in range(n):
+            launch(i)
+    with torch.cuda.stream(st):
+        g.replay()
+        g.replay()
+    st.synchronize()
+    assert memq.memq_device_fault() == 0
+    rows = sample_rows(out_f, 64, seed=m)
+    for i, (w, aux) in enumerate(ws):
+        y_ref, s_ref = ref_gemv(oracle, kind, w, aux, qs, d, in_f, rows=rows)
+        check_gemv(ys[i], y_ref, s_ref, rows=rows)
