@@ -315,7 +315,7 @@ class StackStep:
 
     SHAPES = ((6144, 5120), (5120, 5120), (17408, 5120), (17408, 5120), (5120, 17408))
 
-    def __init__(self, layers, device, seed=0x57AC0000):
+    def __init__(self, layers, device, seed=0x57AC0000, fused=False):
         import torch
         import quantized_decode_memq_gb300 as memq
         from quantized_decode_memq_gb300 import synth
@@ -340,7 +340,8 @@ class StackStep:
         self.gemv_bytes = sum(gemv_bytes("blk", o, i, 1) for (o, i) in self.SHAPES)
         self.step_bytes = layers * (self.gemv_bytes + producer_bytes(1, 5120) * 2 +
                                     producer_bytes(1, 17408))
-        self.launches_per_step = 8 * layers
+        self.fused = fused
+        self.launches_per_step = (5 if fused else 8) * layers
         torch.cuda.synchronize()
 
     def layer(self, l, x):
@@ -356,10 +357,22 @@ class StackStep:
         m.memq_gemv_e4m3_blk128(w[4], g[4], qs[2], d[2], y=y[4])
         return y[4]
 
+    def layer_fused(self, l, x):
+        """The same layer with each RMSNorm -> q8_1 fused into the GEMV that first reads it (the
+        fused call publishes qs / d, which the second GEMV on the same activation reads)."""
+        m = self.memq
+        w, g, y, qs, d = self.w[l], self.g[l], self.y, self.qs, self.d
+        m.memq_rmsnorm_q8_1_gemv_e4m3_blk128(x, self.wn[0], w[0], g[0], 1e-6, qs=qs[0], d=d[0], y=y[0])
+        m.memq_gemv_e4m3_blk128(w[1], g[1], qs[0], d[0], y=y[1])
+        m.memq_rmsnorm_q8_1_gemv_e4m3_blk128(y[1], self.wn[1], w[2], g[2], 1e-6, qs=qs[1], d=d[1], y=y[2])
+        m.memq_gemv_e4m3_blk128(w[3], g[3], qs[1], d[1], y=y[3])
+        m.memq_rmsnorm_q8_1_gemv_e4m3_blk128(y[3], self.wn[2], w[4], g[4], 1e-6, qs=qs[2], d=d[2], y=y[4])
+        return y[4]
+
     def step(self, i):
         x = self.x0
         for l in range(self.layers):
-            x = self.layer(l, x)
+            x = self.layer_fused(l, x) if self.fused else self.layer(l, x)
 
 
 def capture(fn, n, stream):
@@ -525,10 +538,13 @@ def run_other(args, world, rank, local, dev):
         desc = f"{args.workload}: RMSNorm->q8_1 producer, {rows} rows x {ncols} (z written)"
     else:
         layers = int(args.workload[len("stack"):] or 48)
-        wl = StackStep(layers, dev)
+        fused = args.step == "fused"
+        wl = StackStep(layers, dev, fused=fused)
         per_graph = 1
         desc = (f"{args.workload}: one token through {layers} layers of block-128 E4M3 GEMVs "
-                f"(5120->6144, 5120->5120, 5120->17408 x2, 17408->5120) with 3 producers each")
+                f"(5120->6144, 5120->5120, 5120->17408 x2, 17408->5120) with 3 RMSNorm->q8_1 "
+                + ("fused into the GEMVs (5 launches per layer)" if fused else
+                   "producers each (8 launches per layer)"))
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for i in range(per_graph):

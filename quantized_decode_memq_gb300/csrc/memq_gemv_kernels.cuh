@@ -858,9 +858,15 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
     const uint32_t base = part + gridb + red + ring_min;
     if (base > optin) return false;
-    int ctas = G::kMinCtasPerSm;
+    // Small problems: fewer CTAs per SM when a CTA would get fewer than kMinRowsPerCta rows
+    // (measured: 1024 x 5120 runs 20-30% faster at one CTA per SM than with 2-3 rows per CTA;
+    // from about 7 rows per CTA up, more CTAs per SM are faster).
+    constexpr int64_t kMinRowsPerCta = 4;
+    const int k_rows = static_cast<int>(std::min<int64_t>(
+        G::kMinCtasPerSm, std::max<int64_t>(1, out_f / (static_cast<int64_t>(info.sms) * kMinRowsPerCta))));
+    int ctas = k_rows;
     mode = kActGlobal;
-    for (int k = G::kMinCtasPerSm; k >= 1; --k) {
+    for (int k = k_rows; k >= 1; --k) {
         // Shared memory one CTA may use and still leave room for k CTAs per SM.
         const uint32_t budget = std::min(optin, static_cast<uint32_t>(info.smem_sm / k - 1024));
         if (G::kMma && base + qsb + db + frag <= budget) {
