@@ -393,6 +393,8 @@ def run_ours(args, world, rank, local):
     build.build()
     if args.workload.startswith("producer_") or args.workload.startswith("stack"):
         return run_other(args, world, rank, local, dev)
+    if args.workload == "c3":
+        return run_c3(args, world, rank, local, dev)
     kind, out_f, in_f, m, copies = parse_workload(args.workload)
     fused = args.step == "fused"
     wl = DecodeStep(kind, out_f, in_f, m, copies, dev, fused=fused)
@@ -521,6 +523,72 @@ def run_ours(args, world, rank, local):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_c3(args, world, rank, local, dev, out_f=17408, in_f=5120, rounds=15):
+    """The three containers on the same 17408 x 5120 shape at m = 1, interleaved: per arm a CUDA
+    graph of back-to-back GEMV launches over its own rotated weight copies; the graphs are
+    replayed in turn (E4M3, block-128, Q8_0) for `rounds` rounds, each replay timed with CUDA
+    events; per arm the median launch period.  Reports the Q8_0 : E4M3 time ratio next to the
+    1.0625 byte ratio."""
+    import torch
+    from quantized_decode_memq_gb300 import build
+    build.build()
+    arms = {}
+    for kind in ("e4m3", "blk", "q8_0"):
+        copies = max(4, -(-2 * L2_BYTES // gemv_bytes(kind, out_f, in_f, 1)))
+        arms[kind] = DecodeStep(kind, out_f, in_f, 1, copies, dev, fused=False)
+    stream = torch.cuda.Stream(device=dev)
+    graphs, n = {}, {}
+    with torch.cuda.stream(stream):
+        for kind, wl in arms.items():
+            wl.producer()
+            for i in range(wl.copies):
+                wl.gemv(i)
+            n[kind] = 8 * wl.copies
+            graphs[kind] = capture(wl.gemv, n[kind], stream)
+            for _ in range(max(1, args.warmup // n[kind] + 1)):
+                graphs[kind].replay()
+    stream.synchronize()
+    times = {k: [] for k in arms}
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(rounds):
+        for kind in arms:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                graphs[kind].replay()
+                e1.record(stream)
+            stream.synchronize()
+            times[kind].append(e0.elapsed_time(e1) * 1e3 / n[kind])
+    clocks = sampler.stop()
+    peak, peak_kind = measured_peak_hbm()
+    res = {}
+    for kind, wl in arms.items():
+        us = float(np.median(times[kind]))
+        gbs = wl.gemv_bytes / us / 1e3
+        res[kind] = {"us": round(us, 3), "gb_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                     "bytes": wl.gemv_bytes, "spread_us": [round(min(times[kind]), 3),
+                                                           round(max(times[kind]), 3)]}
+    tot_bytes = sum(wl.gemv_bytes for wl in arms.values())
+    tot_us = sum(r["us"] for r in res.values())
+    line = {"metric": METRIC, "value": round(tot_bytes / tot_us / 1e3, 2), "unit": "GB/s",
+            "n_gpus": world, "steps": rounds * sum(n.values()), "warmup": args.warmup,
+            "ms_per_step": tot_us / 3 / 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8+int8", "data": "synthetic",
+            "config": {"workload": f"c3: E4M3, block-128 and Q8_0 GEMV {out_f}x{in_f} m=1, "
+                                   f"interleaved arms, rotated weight copies (DRAM-cold)",
+                       "timing": "per arm: median over rounds of the launch period of a graph "
+                                 "of back-to-back launches"},
+            "arms": res,
+            "q8_0_to_e4m3_time_ratio": round(res["q8_0"]["us"] / res["e4m3"]["us"], 4),
+            "byte_ratio": round(arms["q8_0"].gemv_bytes / arms["e4m3"].gemv_bytes, 4),
+            "peak": {"hbm_gbs": peak, "source": peak_kind},
+            "gpu_launches": rounds * sum(n.values()), "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

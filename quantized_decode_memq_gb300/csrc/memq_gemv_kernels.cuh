@@ -57,19 +57,37 @@ constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kConsumerThreads = kWarps * 32;
 constexpr int kBarConsumers = 1;             // named barrier id used by the consumer warps
 
-enum Kind : int { kE4M3 = 0, kBlk = 1, kQ80 = 2 };
+// kQ80T is Q8_0 computed on the tensor cores (taken from kQ80MmaMinM activation rows up); the
+// public Q8_0 entry points choose between kQ80 and kQ80T.
+enum Kind : int { kE4M3 = 0, kBlk = 1, kQ80 = 2, kQ80T = 3 };
+constexpr int kQ80MmaMinM = 3;
+
+constexpr bool is_q80(int kind) { return kind == kQ80 || kind == kQ80T; }
+
+// Which Q8_0 path a call takes.  dp4a reads the activation once per weight row, so from a few
+// activation rows on it is bound by shared-memory bandwidth; the tensor-core path reads it once
+// per 16-row block step but needs 16-row tiles and a larger staged activation.  Measured on
+// GB300 (back-to-back, DRAM-cold): tensor cores win from m = 6 on every shape (17408 x 5120,
+// m = 8: 23 us against 51 us) and from m = 3 when the activation is small enough to keep
+// several CTAs per SM and there are enough rows (17408 x 5120, m = 4: 23 against 30 us); with
+// a 17408-wide activation at m = 3-4, or 1024 rows, dp4a stays faster.
+inline bool q80_on_tensor_cores(int64_t out_f, int64_t in_f, int m) {
+    if (m >= 6) return true;
+    return m >= kQ80MmaMinM && m * in_f <= 40960 && out_f >= 2048;
+}
 
 // Stream-kernel geometry per container.  A stage holds 32 blocks of every tile row.
 //   E4M3 / block-128: 16-row tiles (one m16 MMA row tile); row slots padded to 1040 bytes so the
 //   8-byte fragment loads of 8 different rows fall in distinct bank groups.
-//   Q8_0: 8-row tiles, 1088-byte row slots (34-byte blocks).
+//   Q8_0 (dp4a): 8-row tiles, 1088-byte row slots (34-byte blocks).
+//   Q8_0 (tensor cores): 16-row tiles, row slots padded to 1104 bytes.
 template <int KIND>
 struct Geo {
     static constexpr bool kMma = KIND != kQ80;
-    static constexpr int kBlockBytes = kMma ? 32 : 34;
+    static constexpr int kBlockBytes = is_q80(KIND) ? 34 : 32;
     static constexpr int kTileRows = kMma ? 16 : kWarps;  // Q8_0: one row per consumer warp
     static constexpr int kChunkBlocks = 32;
-    static constexpr int kSlot = kMma ? kChunkBlocks * 32 + 16 : kChunkBlocks * 34;
+    static constexpr int kSlot = kChunkBlocks * kBlockBytes + (kMma ? 16 : 0);
     static constexpr int kStage = kTileRows * kSlot;
     static constexpr int kMinStages = 3;
     // Register budget: three (E4M3 / block-128) or four (Q8_0) CTAs per SM.  More CTAs per SM
@@ -218,6 +236,90 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
             acc[1] = fmaf(c[1], k1, acc[1]);
             acc[2] = fmaf(c[2], k2, acc[2]);
             acc[3] = fmaf(c[3], k3, acc[3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Q8_0 stage on the tensor cores (kQ80T): as mma_stage, with A = the int8 weights of the tile's
+// 16 rows (int8 -> f16 exact).  Every product is an integer of magnitude <= 127^2 and a block's
+// 32 of them sum to < 2^24, so the MMA's f32 block sum is the exact integer dot product -- the
+// same value dp4a gives.  A record is 34 bytes (f16 d_w, then 32 int8); the thread's 8 weight
+// bytes start 2 bytes into it, i.e. 4-byte aligned for odd blocks of the warp and 2 mod 4 for
+// even ones (the stage, its row slots and the warp's 4-block slice are 8-byte aligned), read
+// with two or three 4-byte loads.  The block result of (row, token) is scaled by
+// d_w[row] * d_x[token], in that order, as in the dp4a stage.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint2 q80_weights8(const uint8_t *rec, bool odd) {
+    // rec: the record start + 8t; returns its bytes [2, 10).  `odd` is a constant after the
+    // caller's unrolling.
+    if (odd) {
+        return make_uint2(lds32(rec + 2), lds32(rec + 6));
+    } else {
+        const uint32_t a = lds32(rec), b = lds32(rec + 4), c = lds32(rec + 8);
+        return make_uint2(__funnelshift_r(a, b, 16), __funnelshift_r(b, c, 16));
+    }
+}
+
+template <int M, int MODE, bool FULL>
+__device__ __forceinline__ void mma_stage_q80(const StreamArgs &a, const uint8_t *stage,
+                                              const uint8_t *sm, int kb0, int nblk, int lane,
+                                              float (&acc)[4]) {
+    using G = Geo<kQ80T>;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const uint4 *bfrag = reinterpret_cast<const uint4 *>(sm + a.off_bfrag);
+    const int8_t *s_qs = reinterpret_cast<const int8_t *>(sm + a.off_qs);
+    const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
+    const uint8_t *row0 = stage + g * G::kSlot;
+    const uint8_t *row8 = row0 + 8 * G::kSlot;
+#pragma unroll
+    for (int b = 0; b < G::kWarpBlocks; ++b) {
+        if (FULL || b < nblk) {
+            const int kb = kb0 + b;
+            uint32_t bq[4] = {0u, 0u, 0u, 0u};
+            if (g < M) {
+                if (MODE == kActFrag) {
+                    const uint4 v = bfrag[(kb * M + g) * 4 + t];
+                    bq[0] = v.x;
+                    bq[1] = v.y;
+                    bq[2] = v.z;
+                    bq[3] = v.w;
+                } else {
+                    const uint2 qv = MODE == kActSmem
+                                         ? lds64(s_qs + g * a.in_f + 32 * kb + 8 * t)
+                                         : __ldcg(reinterpret_cast<const uint2 *>(
+                                               a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+                    s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
+                    s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
+                }
+            }
+            float k0 = 0.f, k1 = 0.f;
+            if (MODE == kActGlobal) {
+                if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
+                if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
+            } else {
+                if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
+                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
+            }
+            const uint8_t *r0 = row0 + 34 * b;
+            const uint8_t *r8 = row8 + 34 * b;
+            const float dw0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(r0))));
+            const float dw8 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(r8))));
+            const uint2 wa = q80_weights8(r0 + 8 * t, b & 1);
+            const uint2 wb = q80_weights8(r8 + 8 * t, b & 1);
+            uint32_t a0, a1, a2, a3;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            s8x4_to_f16x2x2(wa.x, a0, a2);
+            s8x4_to_f16x2x2(wb.x, a1, a3);
+            mma_f16_16816(c, a0, a1, a2, a3, bq[0], bq[1]);
+            s8x4_to_f16x2x2(wa.y, a0, a2);
+            s8x4_to_f16x2x2(wb.y, a1, a3);
+            mma_f16_16816(c, a0, a1, a2, a3, bq[2], bq[3]);
+            acc[0] = fmaf(c[0], dw0 * k0, acc[0]);
+            acc[1] = fmaf(c[1], dw0 * k1, acc[1]);
+            acc[2] = fmaf(c[2], dw8 * k0, acc[2]);
+            acc[3] = fmaf(c[3], dw8 * k1, acc[3]);
         }
     }
 }
@@ -571,10 +673,18 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
                 const int kbc = ch * G::kChunkBlocks;
                 const int nblk = min(G::kChunkBlocks, a.nb - kbc);
                 const uint8_t *stage = ring + c_stage * G::kStage;
-                if (G::kMma) {
+                if constexpr (KIND == kQ80T) {
                     const int kb0 = kbc + warp * G::kWarpBlocks;
                     const int n = min(G::kWarpBlocks, nblk - warp * G::kWarpBlocks);
-                    const uint8_t *st = stage + warp * G::kWarpBlocks * 32;
+                    const uint8_t *st = stage + warp * G::kWarpBlocks * G::kBlockBytes;
+                    if (n == G::kWarpBlocks)
+                        mma_stage_q80<M, MODE, true>(a, st, smem, kb0, n, lane, acc_m);
+                    else if (n > 0)
+                        mma_stage_q80<M, MODE, false>(a, st, smem, kb0, n, lane, acc_m);
+                } else if (G::kMma) {
+                    const int kb0 = kbc + warp * G::kWarpBlocks;
+                    const int n = min(G::kWarpBlocks, nblk - warp * G::kWarpBlocks);
+                    const uint8_t *st = stage + warp * G::kWarpBlocks * G::kBlockBytes;
                     if (n == G::kWarpBlocks)
                         mma_stage<KIND, M, MODE, true>(a, st, smem, r0, R1 - 1, grow_base, kb0, n, lane, acc_m);
                     else if (n > 0)
@@ -685,7 +795,7 @@ struct DeviceInfo {
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
-std::atomic<uint64_t> g_attr_set[kMaxDevices];  // bit per (M, mode, fused): attribute set
+std::atomic<uint64_t> g_attr_set[4][kMaxDevices];  // [kind]: bit per (M, mode, fused) set
 
 bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -759,11 +869,11 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
                           cudaStream_t st) {
     auto kern = gemv_stream_kernel<KIND, M, MODE, FUSE>;
     const uint64_t bit = 1ull << ((M - 1) + 8 * MODE + (FUSE ? 24 : 0));
-    if (!(g_attr_set[dev].load(std::memory_order_acquire) & bit)) {
+    if (!(g_attr_set[KIND][dev].load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              info.smem_optin);
         if (e != cudaSuccess) return e;
-        g_attr_set[dev].fetch_or(bit, std::memory_order_acq_rel);
+        g_attr_set[KIND][dev].fetch_or(bit, std::memory_order_acq_rel);
     }
     // Ring depth: as many stages as fit when the CTAs that registers allow per SM share its
     // shared memory (more stages = more weight bytes in flight), at least kMinStages.
@@ -819,15 +929,27 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
 template <int KIND, int MODE, bool FUSE>
 cudaError_t launch_stream_m(int m, StreamArgs a, uint32_t smem, int dev, const DeviceInfo &info,
                             cudaStream_t st) {
-    switch (m) {
-        case 1: return launch_stream<KIND, 1, MODE, FUSE>(a, smem, dev, info, st);
-        case 2: return launch_stream<KIND, 2, MODE, FUSE>(a, smem, dev, info, st);
-        case 3: return launch_stream<KIND, 3, MODE, FUSE>(a, smem, dev, info, st);
-        case 4: return launch_stream<KIND, 4, MODE, FUSE>(a, smem, dev, info, st);
-        case 5: return launch_stream<KIND, 5, MODE, FUSE>(a, smem, dev, info, st);
-        case 6: return launch_stream<KIND, 6, MODE, FUSE>(a, smem, dev, info, st);
-        case 7: return launch_stream<KIND, 7, MODE, FUSE>(a, smem, dev, info, st);
-        default: return launch_stream<KIND, 8, MODE, FUSE>(a, smem, dev, info, st);
+    if constexpr (KIND == kQ80T) {  // only taken from kQ80MmaMinM = 3 rows up
+        switch (m) {
+            case 3: return launch_stream<KIND, 3, MODE, FUSE>(a, smem, dev, info, st);
+            case 4: return launch_stream<KIND, 4, MODE, FUSE>(a, smem, dev, info, st);
+            case 5: return launch_stream<KIND, 5, MODE, FUSE>(a, smem, dev, info, st);
+            case 6: return launch_stream<KIND, 6, MODE, FUSE>(a, smem, dev, info, st);
+            case 7: return launch_stream<KIND, 7, MODE, FUSE>(a, smem, dev, info, st);
+            case 8: return launch_stream<KIND, 8, MODE, FUSE>(a, smem, dev, info, st);
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (m) {
+            case 1: return launch_stream<KIND, 1, MODE, FUSE>(a, smem, dev, info, st);
+            case 2: return launch_stream<KIND, 2, MODE, FUSE>(a, smem, dev, info, st);
+            case 3: return launch_stream<KIND, 3, MODE, FUSE>(a, smem, dev, info, st);
+            case 4: return launch_stream<KIND, 4, MODE, FUSE>(a, smem, dev, info, st);
+            case 5: return launch_stream<KIND, 5, MODE, FUSE>(a, smem, dev, info, st);
+            case 6: return launch_stream<KIND, 6, MODE, FUSE>(a, smem, dev, info, st);
+            case 7: return launch_stream<KIND, 7, MODE, FUSE>(a, smem, dev, info, st);
+            default: return launch_stream<KIND, 8, MODE, FUSE>(a, smem, dev, info, st);
+        }
     }
 }
 
@@ -916,7 +1038,7 @@ int check_gemv_args(const uint8_t *w, const float *aux, const int8_t *qs, const 
     if (in_f < 32 || (in_f % 32) != 0 || in_f > (1LL << 24)) return MEMQ_ERR_SHAPE;
     if (out_f < 0 || out_f > (1LL << 31) - 1) return MEMQ_ERR_SHAPE;
     if (out_f == 0) return MEMQ_OK;
-    if (!w || !qs || !d || !y || (KIND != kQ80 && !aux)) return MEMQ_ERR_NULL;
+    if (!w || !qs || !d || !y || (!is_q80(KIND) && !aux)) return MEMQ_ERR_NULL;
     if (!aligned(d, 4) || !aligned(y, 4) || (aux && !aligned(aux, 4))) return MEMQ_ERR_ALIGN;
     return -1;  // valid, work to do
 }
@@ -931,7 +1053,7 @@ StreamArgs base_args(const uint8_t *w, const float *aux, const int8_t *qs, const
     a.d = d;
     a.y = y;
     a.out_f = out_f;
-    a.row_bytes = (KIND == kQ80) ? in_f / 32 * 34 : in_f;
+    a.row_bytes = is_q80(KIND) ? in_f / 32 * 34 : in_f;
     a.in_f = static_cast<int>(in_f);
     a.nb = static_cast<int>(in_f / 32);
     a.gcols = static_cast<int>((in_f + 127) / 128);
@@ -940,9 +1062,9 @@ StreamArgs base_args(const uint8_t *w, const float *aux, const int8_t *qs, const
 
 template <int KIND>
 bool fast_path_ok(const uint8_t *w, const int8_t *qs, int64_t in_f) {
-    const int64_t row_bytes = (KIND == kQ80) ? in_f / 32 * 34 : in_f;
+    const int64_t row_bytes = is_q80(KIND) ? in_f / 32 * 34 : in_f;
     return aligned(w, 16) && aligned(qs, 16) && (row_bytes % 16) == 0 &&
-           (KIND != kQ80 || ((in_f / 32) % 8) == 0);
+           (!is_q80(KIND) || ((in_f / 32) % 8) == 0);
 }
 
 template <int KIND>
@@ -962,7 +1084,8 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
         e = launch_planned<KIND, false>(m, mode, a, smem, dev, info, st);
     } else {
         const int64_t blocks = (out_f + kGenericWarps - 1) / kGenericWarps;
-        gemv_generic_kernel<KIND><<<static_cast<unsigned>(blocks), kGenericWarps * 32, 0, st>>>(
+        constexpr int GK = KIND == kQ80T ? kQ80 : KIND;
+        gemv_generic_kernel<GK><<<static_cast<unsigned>(blocks), kGenericWarps * 32, 0, st>>>(
             w, aux, qs, d, y, out_f, static_cast<int>(in_f), m);
         e = cudaGetLastError();
     }

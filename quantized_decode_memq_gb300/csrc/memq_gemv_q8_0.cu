@@ -5,16 +5,22 @@
 
 extern "C" int memq_gemv_q8_0(const void *w, const int8_t *qs, const float *d, float *y,
                               int64_t out_f, int64_t in_f, int m, void *stream) {
-    return memq::gemv_entry<memq::kQ80>(static_cast<const uint8_t *>(w), nullptr, qs, d, y, out_f,
-                                        in_f, m, stream);
+    const uint8_t *w8 = static_cast<const uint8_t *>(w);
+    if (memq::q80_on_tensor_cores(out_f, in_f, m))
+        return memq::gemv_entry<memq::kQ80T>(w8, nullptr, qs, d, y, out_f, in_f, m, stream);
+    return memq::gemv_entry<memq::kQ80>(w8, nullptr, qs, d, y, out_f, in_f, m, stream);
 }
 
 extern "C" int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps,
                                            const void *w, int8_t *qs, float *d, float *z,
                                            float *y, int64_t out_f, int64_t in_f, int m,
                                            void *stream) {
-    return memq::fused_entry<memq::kQ80>(x, wn, eps, static_cast<const uint8_t *>(w), nullptr, qs,
-                                         d, z, y, out_f, in_f, m, stream);
+    const uint8_t *w8 = static_cast<const uint8_t *>(w);
+    if (memq::q80_on_tensor_cores(out_f, in_f, m))
+        return memq::fused_entry<memq::kQ80T>(x, wn, eps, w8, nullptr, qs, d, z, y, out_f, in_f, m,
+                                              stream);
+    return memq::fused_entry<memq::kQ80>(x, wn, eps, w8, nullptr, qs, d, z, y, out_f, in_f, m,
+                                         stream);
 }
 
 // Internal: this translation unit's device fault word (not part of the public header).
