@@ -586,6 +586,8 @@ def run_c3(args, world, rank, local, dev, out_f=17408, in_f=5120, rounds=15):
                                  "of back-to-back launches"},
             "arms": res,
             "q8_0_to_e4m3_time_ratio": round(res["q8_0"]["us"] / res["e4m3"]["us"], 4),
+            "q8_0_to_blk128_time_ratio": round(res["q8_0"]["us"] / res["blk"]["us"], 4),
+            "blk128_to_e4m3_time_ratio": round(res["blk"]["us"] / res["e4m3"]["us"], 4),
             "byte_ratio": round(arms["q8_0"].gemv_bytes / arms["e4m3"].gemv_bytes, 4),
             "peak": {"hbm_gbs": peak, "source": peak_kind},
             "gpu_launches": rounds * sum(n.values()), "clocks": clocks}

@@ -71,10 +71,15 @@ def _load():
                                                          P, I64, P, P]
             lib.memq_oracle_gemv_q8_0.argtypes = [P, P, P, I64, I64, ctypes.c_int, P, I64,
                                                   P, P]
+            lib.memq_oracle_silu_mul.argtypes = [P, P, I64, P]
+            lib.memq_oracle_f16_bits.argtypes = [ctypes.c_double]
+            lib.memq_oracle_f16_bits.restype = ctypes.c_uint16
+            lib.memq_oracle_repack_q8_0.argtypes = [P, P, ctypes.c_int, I64, I64, P, P]
             for name in ("memq_oracle_e4m3_table", "memq_oracle_f16_decode",
                          "memq_oracle_rmsnorm", "memq_oracle_quantize_q8_1",
                          "memq_oracle_gemv_e4m3", "memq_oracle_gemv_e4m3_blk128",
-                         "memq_oracle_gemv_q8_0"):
+                         "memq_oracle_gemv_q8_0", "memq_oracle_silu_mul",
+                         "memq_oracle_repack_q8_0"):
                 getattr(lib, name).restype = None
             _lib = lib
     return _lib
@@ -204,3 +209,47 @@ def gemv_q8_0(w: np.ndarray, in_f: int, qs, d, rows=None):
     assert w.shape == (out_f, in_f // 32 * 34)
     qs, d, m = _act_args(qs, d, in_f)
     return _finish(_load().memq_oracle_gemv_q8_0, w, (), qs, d, out_f, in_f, m, rows)
+
+
+# ------------------------------------------------------------------------------------------
+# Next rows: the silu(gate)*up -> q8_1 producer and the E4M3 -> Q8_0 repack
+# ------------------------------------------------------------------------------------------
+
+def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """z = silu(g) * u = g / (1 + exp(-g)) * u in f64 (g, u: f32, same shape)."""
+    g = _c(np.atleast_2d(g), np.float32)
+    u = _c(np.atleast_2d(u), np.float32)
+    assert g.shape == u.shape
+    z = np.empty(g.shape, np.float64)
+    _load().memq_oracle_silu_mul(_ptr(g), _ptr(u), g.size, _ptr(z))
+    return z
+
+
+def silu_mul_q8_1(g: np.ndarray, u: np.ndarray):
+    """The whole silu producer: returns (z f64, d f32, qs int8, ratio f64)."""
+    z = silu_mul(g, u)
+    d, qs, ratio = quantize_q8_1(z)
+    return z, d, qs, ratio
+
+
+def f16_bits(v) -> np.ndarray:
+    """IEEE binary16 bits of f64 values, round to nearest even (scalar or array)."""
+    a = np.asarray(v, np.float64)
+    f = _load().memq_oracle_f16_bits
+    return np.array([f(float(x)) for x in a.reshape(-1)], np.uint16).reshape(a.shape)
+
+
+def repack_q8_0(w: np.ndarray, aux: np.ndarray, grid: bool):
+    """E4M3 weights -> Q8_0 slab (uint8 [out_f, in_f/32*34]) and the f32 d of every block.
+
+    aux: the per-tensor scale (grid=False, shape (1,)) or the block-128 grid (grid=True)."""
+    w = _c(w, np.uint8)
+    out_f, in_f = w.shape
+    aux = _c(aux, np.float32)
+    if grid:
+        assert aux.shape == ((out_f + 127) // 128, (in_f + 127) // 128)
+    out = np.empty((out_f, in_f // 32 * 34), np.uint8)
+    d = np.empty((out_f, in_f // 32), np.float32)
+    _load().memq_oracle_repack_q8_0(_ptr(w), _ptr(aux), int(grid), out_f, in_f, _ptr(out),
+                                    _ptr(d))
+    return out, d

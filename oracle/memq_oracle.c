@@ -26,6 +26,18 @@
  *   memq_oracle_gemv_*   library matmul of independently dequantized operands on small
  *                        shapes, one-hot activations, sign-flip / zero / constant-grid
  *                        identities, and the exact cross-container identity
+ *   memq_oracle_silu_mul the identity silu(x) - silu(-x) = x, silu(0) = 0, a library logistic
+ *                        function, and the q8_1 quantizer's own pins on its output
+ *   memq_oracle_f16_bits all representable binade boundaries and random f32 values vs the
+ *                        float16 conversion of numpy (round to nearest even, subnormals)
+ *   memq_oracle_repack_q8_0  brute-force nearest code over all 255 values, amax -> +-127,
+ *                        constant / zero blocks, dequantization error <= d/2, and the GEMV of
+ *                        the repacked slab against the GEMV of the E4M3 source within the
+ *                        quantization bound
+ *
+ * Also from the pages (SURVEY's "next" rows): q8_fuse_gate.rs, `main` -- the silu(gate)*up ->
+ * q8_1 activation producer named for the 1536-wide expert site; gemv_e4m3_bench.rs, module doc
+ * "QUESTION" -- the ship path that dequantizes FP8 weights to a Q8_0 slab at load ("ARM B'").
  */
 #include <math.h>
 #include <stddef.h>
@@ -223,6 +235,102 @@ void memq_oracle_gemv_q8_0(const uint8_t *w, const int8_t *qs, const float *d, i
             }
             y[j * nrows + t] = acc;
             sabs[j * nrows + t] = s;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * The silu(gate) * up -> q8_1 activation producer (q8_fuse_gate.rs, `main`: the expert-ff site,
+ * "silu/gate*up -> q8_1").  z = silu(g) * u with silu(g) = g / (1 + exp(-g)), in f64; the q8_1
+ * step is memq_oracle_quantize_q8_1 on z.  g, u: [n] f32 -> z: [n] f64.
+ * ------------------------------------------------------------------------------------------- */
+void memq_oracle_silu_mul(const float *g, const float *u, int64_t n, double *z)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double gi = (double)g[i];
+        z[i] = gi / (1.0 + exp(-gi)) * (double)u[i];
+    }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Load-time repack of E4M3 weights into a Q8_0 slab (gemv_e4m3_bench.rs, module doc
+ * "QUESTION": the ship path "dequants FP8 checkpoints to a Q8_0 slab at load").
+ *
+ * The pages fix the two formats but not the arithmetic of the conversion; the reading taken is
+ * the q8_1 rule applied to the dequantized weights, per 32-block of a row:
+ *   W[k] = e4m3(w[k]) * s  (s = the per-tensor scale, or grid[r/128][i/128]),
+ *   amax = max |W|,  d = amax / 127,  stored as f16 (round to nearest, ties to even),
+ *   qs[k] = round(W[k] / d) (ties away from zero), qs = 0 when d = 0.
+ * Floating point decides the integer codes here, so this function takes those decisions in the
+ * precision of the GPU kernel, IEEE f32 (one rounded product, one rounded quotient each); with
+ * -ffp-contract=off the result is the exact f32 evaluation of these formulas.
+ * ------------------------------------------------------------------------------------------- */
+
+/* f64 -> IEEE binary16 bits, round to nearest, ties to even; subnormals; overflow -> inf. */
+uint16_t memq_oracle_f16_bits(double v)
+{
+    uint16_t sign = 0;
+    if (v != v)
+        return 0x7E00;
+    if (v < 0 || (v == 0 && 1.0 / v < 0)) {
+        sign = 0x8000;
+        v = -v;
+    }
+    if (v == 0)
+        return sign;
+    /* exponent of the f16 quantum: 2^(e - 10) for a normal value in [2^e, 2^(e+1)), e >= -14;
+     * subnormals share the quantum 2^-24 */
+    int e = 0;
+    double m = frexp(v, &e); /* v = m * 2^e, m in [0.5, 1) */
+    e -= 1;                  /* v in [2^e, 2^(e+1)) */
+    if (e < -14)
+        e = -14;
+    double q = ldexp(1.0, e - 10);
+    double k = rint(v / q); /* the division by a power of two is exact; rint = ties to even */
+    double r = k * q;
+    (void)m;
+    if (r >= 65536.0)
+        return sign | 0x7C00;
+    /* encode r */
+    if (r < ldexp(1.0, -14))
+        return sign | (uint16_t)k; /* subnormal: r = k * 2^-24 */
+    int er = 0;
+    double mr = frexp(r, &er); /* r = mr * 2^er, mr in [0.5, 1) */
+    er -= 1;
+    uint16_t mant = (uint16_t)((mr * 2.0 - 1.0) * 1024.0);
+    return sign | (uint16_t)((er + 15) << 10) | mant;
+}
+
+/* w: [out_f][in_f] E4M3 bytes; aux: the per-tensor scale (grid = 0, aux[0]) or the f32 grid
+ * [ceil(out_f/128)][ceil(in_f/128)] (grid = 1).  out: [out_f][in_f/32 * 34] bytes (f16 d
+ * little-endian, then 32 int8).  dout (may be NULL): the f32 d of every block. */
+void memq_oracle_repack_q8_0(const uint8_t *w, const float *aux, int grid, int64_t out_f,
+                             int64_t in_f, uint8_t *out, float *dout)
+{
+    int64_t nb = in_f / 32, gcols = (in_f + 127) / 128;
+    for (int64_t r = 0; r < out_f; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            float W[32];
+            float amax = 0.0f;
+            for (int k = 0; k < 32; ++k) {
+                int64_t i = b * 32 + k;
+                float s = grid ? aux[(r / 128) * gcols + i / 128] : aux[0];
+                volatile float p = (float)memq_oracle_e4m3(w[r * in_f + i]) * s;
+                W[k] = p;
+                if (fabsf(W[k]) > amax)
+                    amax = fabsf(W[k]);
+            }
+            volatile float d = amax / 127.0f;
+            uint8_t *blk = out + (r * nb + b) * 34;
+            uint16_t h = memq_oracle_f16_bits((double)d);
+            blk[0] = (uint8_t)(h & 0xFF);
+            blk[1] = (uint8_t)(h >> 8);
+            if (dout)
+                dout[r * nb + b] = d;
+            for (int k = 0; k < 32; ++k) {
+                volatile float t = (d != 0.0f) ? W[k] / d : 0.0f;
+                blk[2 + k] = (uint8_t)(int8_t)roundf(t);
+            }
         }
     }
 }

@@ -39,10 +39,22 @@ MUTATIONS = {
                     "            sabs[j * nrows + t] = s;\n        }\n    }\n}\n\n/* ggml",
                     "s += p;\n            }\n            y[j * nrows + t] = acc;\n"
                     "            sabs[j * nrows + t] = s;\n        }\n    }\n}\n\n/* ggml"),
+    "silu_sign": ("exp(-gi)", "exp(gi)"),
+    "silu_up_dropped": ("(1.0 + exp(-gi)) * (double)u[i];", "(1.0 + exp(-gi));"),
+    "f16_ties_up": ("double k = rint(v / q);", "double k = floor(v / q + 0.5);"),
+    "f16_subnormal_quantum": ("if (e < -14)\n        e = -14;", "if (e < -15)\n        e = -15;"),
+    "repack_grid_col": ("aux[(r / 128) * gcols + i / 128]", "aux[(r / 128) * gcols + i / 256]"),
+    # (No tie-rule mutant for the repack: with E4M3 inputs the only reachable tie is
+    #  W = amax / 2 -> +-63.5, where ties-away and ties-to-even both give +-64.)
+    "repack_divisor": ("amax / 127.0f", "amax / 128.0f"),
+    "repack_scale_dropped": ("(float)memq_oracle_e4m3(w[r * in_f + i]) * s;",
+                             "(float)memq_oracle_e4m3(w[r * in_f + i]);"),
+    "repack_f16_byte_order": ("blk[0] = (uint8_t)(h & 0xFF);\n            blk[1] = (uint8_t)(h >> 8);",
+                              "blk[1] = (uint8_t)(h & 0xFF);\n            blk[0] = (uint8_t)(h >> 8);"),
 }
 
 PIN_TESTS = ["tests/test_oracle_decode.py", "tests/test_oracle_producer.py",
-             "tests/test_oracle_gemv.py"]
+             "tests/test_oracle_gemv.py", "tests/test_oracle_next.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
