@@ -305,6 +305,59 @@ class ProducerStep:
                                     d=self.d)
 
 
+class SiluStep:
+    """The silu(gate) * up -> q8_1 producer on rows x ncols (z written), rotated input copies."""
+
+    def __init__(self, ncols, rows, device):
+        import torch
+        import quantized_decode_memq_gb300 as memq
+        from quantized_decode_memq_gb300 import synth
+        self.memq = memq
+        xb = 2 * rows * ncols * 4
+        self.copies = max(1, min(16, -(-2 * L2_BYTES // xb)))
+        g = torch.from_numpy(synth.uniform_pm4(0x7500, rows * ncols).reshape(rows, ncols)).to(device)
+        u = torch.from_numpy(synth.uniform_pm4(0x7501, rows * ncols).reshape(rows, ncols)).to(device)
+        self.g = [g] + [g.clone() for _ in range(self.copies - 1)]
+        self.u = [u] + [u.clone() for _ in range(self.copies - 1)]
+        self.z = torch.empty((rows, ncols), dtype=torch.float32, device=device)
+        self.qs = torch.empty((rows, ncols), dtype=torch.int8, device=device)
+        self.d = torch.empty((rows, ncols // 32), dtype=torch.float32, device=device)
+        self.step_bytes = rows * ncols * (4 + 4 + 4 + 1) + rows * ncols // 32 * 4
+        self.launches_per_step = 1
+
+    def step(self, i):
+        c = i % self.copies
+        self.memq.memq_silu_mul_q8_1(self.g[c], self.u[c], z=self.z, qs=self.qs, d=self.d)
+
+
+class RepackStep:
+    """E4M3 (per-tensor or block-128) -> Q8_0 slab, rotated source copies."""
+
+    def __init__(self, kind, out_f, in_f, device):
+        import torch
+        import quantized_decode_memq_gb300 as memq
+        from quantized_decode_memq_gb300 import synth
+        self.memq, self.kind = memq, kind
+        src = out_f * in_f
+        self.copies = max(2, min(16, -(-2 * L2_BYTES // src)))
+        w = torch.from_numpy(synth.e4m3_bytes(0x7600, out_f, in_f)).to(device)
+        self.w = [w] + [w.clone() for _ in range(self.copies - 1)]
+        if kind == "blk":
+            self.aux = torch.from_numpy(synth.grid_log2_uniform(0x7601, out_f, in_f)).to(device)
+        else:
+            self.aux = torch.tensor([2.0 ** -4], dtype=torch.float32, device=device)
+        self.out = [torch.empty((out_f, in_f // 32 * 34), dtype=torch.uint8, device=device)
+                    for _ in range(2)]
+        self.step_bytes = src + src // 32 * 34 + self.aux.numel() * 4
+        self.launches_per_step = 1
+
+    def step(self, i):
+        c = i % self.copies
+        fn = (self.memq.memq_repack_e4m3_blk128_q8_0 if self.kind == "blk"
+              else self.memq.memq_repack_e4m3_q8_0)
+        fn(self.w[c], self.aux, out=self.out[i % 2])
+
+
 class StackStep:
     """One decode token through a synthetic 48-layer stack of block-128 E4M3 GEMVs at m = 1.
 
@@ -391,7 +444,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     from quantized_decode_memq_gb300 import build
     build.build()
-    if args.workload.startswith("producer_") or args.workload.startswith("stack"):
+    if args.workload.split("_")[0] in ("producer", "silu", "repack") or args.workload.startswith("stack"):
         return run_other(args, world, rank, local, dev)
     if args.workload == "c3":
         return run_c3(args, world, rank, local, dev)
@@ -606,6 +659,19 @@ def run_other(args, world, rank, local, dev):
         wl = ProducerStep(ncols, rows, dev)
         per_graph = wl.copies
         desc = f"{args.workload}: RMSNorm->q8_1 producer, {rows} rows x {ncols} (z written)"
+    elif args.workload.startswith("silu_"):
+        ncols, rows = (int(v) for v in args.workload[len("silu_"):].split("x"))
+        wl = SiluStep(ncols, rows, dev)
+        per_graph = wl.copies
+        desc = f"{args.workload}: silu(gate) * up -> q8_1 producer, {rows} rows x {ncols} (z written)"
+    elif args.workload.startswith("repack_"):
+        kind, shape = args.workload[len("repack_"):].split("_")
+        kind = "blk" if kind == "blk128" else kind
+        out_f, in_f = (int(v) for v in shape.split("x"))
+        wl = RepackStep(kind, out_f, in_f, dev)
+        per_graph = wl.copies
+        desc = (f"{args.workload}: E4M3 ({'block-128 grid' if kind == 'blk' else 'per-tensor scale'})"
+                f" -> Q8_0 slab, {out_f}x{in_f}, read 1 B + write 1.0625 B per weight")
     else:
         layers = int(args.workload[len("stack"):] or 48)
         fused = args.step == "fused"
@@ -647,7 +713,7 @@ def run_other(args, world, rank, local, dev):
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": steps, "warmup": W, "ms_per_step": t_max / steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if args.workload.startswith("producer_") else "fp8",
+            "dtype": "f32" if args.workload.split("_")[0] in ("producer", "silu") else "fp8",
             "data": "synthetic",
             "config": {"workload": desc, "step_bytes": wl.step_bytes,
                        "timing": "steps replayed from a CUDA graph, CUDA events"},

@@ -8,6 +8,10 @@
  *      memq_gemv_e4m3_blk128  E4M3 weights + f32 block-128 scale grid          (1.0 B/weight)
  *      memq_gemv_q8_0         ggml block_q8_0 weights (f16 scale + 32 int8)     (1.0625 B/weight)
  *
+ * Around them: the fused decode steps memq_rmsnorm_q8_1_gemv_* (stage 1 inside the GEMV
+ * launch), the silu(gate) * up -> q8_1 producer memq_silu_mul_q8_1, and the load-time repack of
+ * E4M3 weights into a Q8_0 slab, memq_repack_e4m3[_blk128]_q8_0.
+ *
  * The operations are the ones defined on the memra-engine 0.125.0 source pages:
  * q8_fuse_gate.rs (module doc: the `rms_norm` -> `quantize_q8_1` chain and the fused
  * `rms_norm_zq8_f32` producer) and gemv_e4m3_bench.rs (module doc, "THE COMPARISON" and "THE
@@ -142,6 +146,43 @@ int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps, cons
                                 int64_t in_f, int m, void *stream);
 
 /* Human-readable name of a memq_status value (static storage; never NULL). */
+/*
+ * memq_silu_mul_q8_1 -- the silu(gate) * up -> q8_1 activation producer.
+ * Named on q8_fuse_gate.rs (`main`: the expert-ff width 1536, the "silu/gate*up -> q8_1"
+ * fusion site).  For each row r < rows and column i < ncols:
+ *     z[r][i] = silu(gate[r][i]) * up[r][i],   silu(g) = g / (1 + exp(-g))   (f32)
+ * then per 32-element block exactly as memq_rmsnorm_q8_1: d = amax/127, qs = round(z/d).
+ *   gate, up  device f32 [rows][ncols], 16-byte aligned (typically the two GEMV outputs)
+ *   z         device f32 [rows][ncols], 16-byte aligned, or NULL to skip writing z
+ *   qs        device int8 [rows][ncols], 4-byte aligned;  d  device f32 [rows][ncols/32]
+ *   ncols     multiple of 32, 32 <= ncols <= 2^30;  rows >= 0 (0 = no-op)
+ * Errors: MEMQ_ERR_SHAPE, MEMQ_ERR_NULL, MEMQ_ERR_ALIGN, MEMQ_ERR_LAUNCH.
+ */
+int memq_silu_mul_q8_1(const float *gate, const float *up, float *z, int8_t *qs, float *d,
+                       int64_t ncols, int64_t rows, void *stream);
+
+/*
+ * memq_repack_e4m3_q8_0 / memq_repack_e4m3_blk128_q8_0 -- load-time conversion of E4M3
+ * weights into a ggml block_q8_0 slab (gemv_e4m3_bench.rs, module doc "QUESTION": the ship
+ * path "dequants FP8 checkpoints to a Q8_0 slab at load", ARM B').  For each row r and 32-block
+ * b of the row, with W[i] = e4m3(w[r][i]) * s in f32 (s = *w_scale, or grid[r/128][i/128]):
+ *     d = max_{i in b} |W[i]| / 127  (f32),  stored as f16 (round to nearest even)
+ *     qs[i] = round(W[i] / d)  (f32 quotient, ties away from zero; 0 when d == 0)
+ * so that out can be passed to memq_gemv_q8_0 in place of (w, scale).  The f32 operations are
+ * IEEE (one rounding each), so the slab is bit-reproducible.
+ *   w        device E4M3 bytes [out_f][in_f], 16-byte aligned
+ *   w_scale  device f32, one value;  grid  device f32 [ceil(out_f/128)][ceil(in_f/128)]
+ *   out      device bytes [out_f][in_f/32 * 34], 16-byte aligned (the slab is contiguous)
+ *   in_f     multiple of 32;  out_f >= 0 (0 = no-op)
+ * NaN weight codes (0x7F / 0xFF) are outside the contract.  Not for the decode loop: it reads
+ * 1 byte and writes 1.0625 bytes per weight, once at load.
+ * Errors: MEMQ_ERR_SHAPE, MEMQ_ERR_NULL, MEMQ_ERR_ALIGN, MEMQ_ERR_LAUNCH.
+ */
+int memq_repack_e4m3_q8_0(const uint8_t *w, const float *w_scale, void *out, int64_t out_f,
+                          int64_t in_f, void *stream);
+int memq_repack_e4m3_blk128_q8_0(const uint8_t *w, const float *grid, void *out, int64_t out_f,
+                                 int64_t in_f, void *stream);
+
 const char *memq_status_string(int status);
 
 /*

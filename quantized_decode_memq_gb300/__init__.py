@@ -9,7 +9,10 @@ raises.
 Stage 1 -- ``memq_rmsnorm_q8_1``: q8_fuse_gate.rs (memra-engine 0.125.0), the fused
 ``rms_norm_zq8_f32`` producer.  Stage 2 -- ``memq_gemv_e4m3``, ``memq_gemv_e4m3_blk128``,
 ``memq_gemv_q8_0``: gemv_e4m3_bench.rs, the E4M3 / block-128 / Q8_0 arms.  The fused decode
-step ``memq_rmsnorm_q8_1_gemv_*`` runs both stages in one launch.
+step ``memq_rmsnorm_q8_1_gemv_*`` runs both stages in one launch.  Around them:
+``memq_silu_mul_q8_1`` (the silu(gate) * up -> q8_1 producer named in q8_fuse_gate.rs, ``main``)
+and ``memq_repack_e4m3[_blk128]_q8_0`` (gemv_e4m3_bench.rs, "QUESTION": E4M3 weights -> a Q8_0
+slab at load).
 """
 from __future__ import annotations
 
@@ -28,6 +31,9 @@ from ._binding import (  # noqa: F401
     memq_rmsnorm_q8_1_gemv_e4m3,
     memq_rmsnorm_q8_1_gemv_e4m3_blk128,
     memq_rmsnorm_q8_1_gemv_q8_0,
+    memq_repack_e4m3_blk128_q8_0,
+    memq_repack_e4m3_q8_0,
+    memq_silu_mul_q8_1,
     memq_status_string,
     memq_version,
 )

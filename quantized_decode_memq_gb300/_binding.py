@@ -60,6 +60,9 @@ def lib() -> ctypes.CDLL:
                                                              P, P, I64, I64, I32, P]
             L.memq_rmsnorm_q8_1_gemv_q8_0.argtypes = [P, P, ctypes.c_float, P, P, P, P, P, I64,
                                                       I64, I32, P]
+            L.memq_silu_mul_q8_1.argtypes = [P, P, P, P, P, I64, I64, P]
+            L.memq_repack_e4m3_q8_0.argtypes = [P, P, P, I64, I64, P]
+            L.memq_repack_e4m3_blk128_q8_0.argtypes = [P, P, P, I64, I64, P]
             L.memq_device_fault.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             L.memq_status_string.argtypes = [I32]
             L.memq_status_string.restype = ctypes.c_char_p
@@ -67,7 +70,8 @@ def lib() -> ctypes.CDLL:
             for name in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
                          "memq_gemv_q8_0", "memq_rmsnorm_q8_1_gemv_e4m3",
                          "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
-                         "memq_device_fault", "memq_version"):
+                         "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
+                         "memq_repack_e4m3_blk128_q8_0", "memq_device_fault", "memq_version"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -278,3 +282,53 @@ def memq_device_fault(stream=None) -> int:
     rc = lib().memq_device_fault(_stream(stream), ctypes.byref(v))
     _check("memq_device_fault", rc)
     return int(v.value)
+
+
+def memq_silu_mul_q8_1(gate: torch.Tensor, up: torch.Tensor, *, z=None, qs=None, d=None,
+                       want_z: bool = True, stream=None):
+    """silu(gate) * up -> q8_1.  gate, up: f32 [rows, ncols] (or [ncols]).
+
+    Returns (z f32 [rows, ncols] or None, qs int8 [rows, ncols], d f32 [rows, ncols/32])."""
+    g2 = gate if gate.dim() == 2 else gate.reshape(1, -1)
+    u2 = up if up.dim() == 2 else up.reshape(1, -1)
+    _cuda("gate", g2, torch.float32)
+    rows, ncols = g2.shape
+    _cuda("up", u2, torch.float32, (rows, ncols))
+    if qs is None:
+        qs = torch.empty((rows, ncols), dtype=torch.int8, device=g2.device)
+    if d is None:
+        d = torch.empty((rows, ncols // 32), dtype=torch.float32, device=g2.device)
+    if z is None and want_z:
+        z = torch.empty((rows, ncols), dtype=torch.float32, device=g2.device)
+    _cuda("qs", qs, torch.int8, (rows, ncols))
+    _cuda("d", d, torch.float32, (rows, ncols // 32))
+    if z is not None:
+        _cuda("z", z, torch.float32, (rows, ncols))
+    rc = lib().memq_silu_mul_q8_1(_ptr(g2), _ptr(u2), _ptr(z), _ptr(qs), _ptr(d), ncols, rows,
+                                  _stream(stream))
+    _check("memq_silu_mul_q8_1", rc)
+    return z, qs, d
+
+
+def _repack(fn: str, w, aux, aux_shape, out, stream):
+    _cuda("w", w, torch.uint8)
+    out_f, in_f = w.shape
+    _cuda("scale" if aux_shape == (1,) else "grid", aux, torch.float32, aux_shape)
+    if out is None:
+        out = torch.empty((out_f, in_f // 32 * 34), dtype=torch.uint8, device=w.device)
+    _cuda("out", out, torch.uint8, (out_f, in_f // 32 * 34))
+    rc = getattr(lib(), fn)(_ptr(w), _ptr(aux), _ptr(out), out_f, in_f, _stream(stream))
+    _check(fn, rc)
+    return out
+
+
+def memq_repack_e4m3_q8_0(w: torch.Tensor, w_scale: torch.Tensor, *, out=None, stream=None):
+    """E4M3 [out_f, in_f] with a per-tensor scale -> Q8_0 slab uint8 [out_f, in_f/32*34]."""
+    return _repack("memq_repack_e4m3_q8_0", w, w_scale, (1,), out, stream)
+
+
+def memq_repack_e4m3_blk128_q8_0(w: torch.Tensor, grid: torch.Tensor, *, out=None, stream=None):
+    """E4M3 [out_f, in_f] with a block-128 grid -> Q8_0 slab uint8 [out_f, in_f/32*34]."""
+    out_f, in_f = w.shape
+    return _repack("memq_repack_e4m3_blk128_q8_0", w, grid,
+                   ((out_f + 127) // 128, (in_f + 127) // 128), out, stream)

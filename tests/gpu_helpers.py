@@ -46,15 +46,21 @@ def check_producer(oracle, x: np.ndarray, w: np.ndarray, eps: float, z_gpu, qs_g
        "near" widens by the propagated z tolerance (127 * 2 * Z_REL relative).
     Returns the number of qs codes that differ from the full-chain oracle.
     """
+    if rows is not None:
+        x = x[rows]
+    z_ref, d_ref, qs_ref, ratio_ref = oracle.rmsnorm_q8_1(x, w, eps)
+    return check_q8_1(oracle, z_ref, d_ref, qs_ref, ratio_ref, z_gpu, qs_gpu, d_gpu, rows)
+
+
+def check_q8_1(oracle, z_ref, d_ref, qs_ref, ratio_ref, z_gpu, qs_gpu, d_gpu, rows=None):
+    """The q8_1 checks of check_producer against an oracle z (f64) and its quantization."""
     z_g = None if z_gpu is None else z_gpu.cpu().numpy().astype(np.float64)
     qs_g = qs_gpu.cpu().numpy()
     d_g = d_gpu.cpu().numpy()
     if rows is not None:
-        x = x[rows]
         z_g = None if z_g is None else z_g[rows]
         qs_g = qs_g[rows]
         d_g = d_g[rows]
-    z_ref, d_ref, qs_ref, ratio_ref = oracle.rmsnorm_q8_1(x, w, eps)
 
     if z_g is not None:
         floor = np.abs(z_ref).max(axis=1, keepdims=True) * 2.0 ** -24

@@ -36,6 +36,8 @@ def test_header_declares_the_boundary():
     for required in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
                      "memq_gemv_q8_0", "memq_rmsnorm_q8_1_gemv_e4m3",
                      "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
+                     "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
+                     "memq_repack_e4m3_blk128_q8_0",
                      "memq_status_string", "memq_device_fault", "memq_version"):
         assert required in names
 
@@ -76,6 +78,16 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.memq_rmsnorm_q8_1_gemv_e4m3_blk128(fake, fake, -1.0, fake, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_SHAPE
     assert lib.memq_rmsnorm_q8_1_gemv_q8_0(fake, fake, 1e-6, fake, fake, fake, None, fake, 4, 65536, 1, None) == m.Status.ERR_SHAPE
     assert lib.memq_rmsnorm_q8_1_gemv_q8_0(P(0x1004), fake, 1e-6, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_ALIGN
+    # silu(gate) * up -> q8_1 producer
+    assert lib.memq_silu_mul_q8_1(fake, fake, None, fake, fake, 48, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_silu_mul_q8_1(None, fake, None, fake, fake, 64, 1, None) == m.Status.ERR_NULL
+    assert lib.memq_silu_mul_q8_1(fake, P(0x1008), None, fake, fake, 64, 1, None) == m.Status.ERR_ALIGN
+    assert lib.memq_silu_mul_q8_1(None, None, None, None, None, 64, 0, None) == m.Status.OK
+    # E4M3 -> Q8_0 repack
+    assert lib.memq_repack_e4m3_q8_0(fake, fake, fake, 4, 40, None) == m.Status.ERR_SHAPE
+    assert lib.memq_repack_e4m3_blk128_q8_0(fake, None, fake, 4, 64, None) == m.Status.ERR_NULL
+    assert lib.memq_repack_e4m3_q8_0(fake, fake, P(0x1002), 4, 64, None) == m.Status.ERR_ALIGN
+    assert lib.memq_repack_e4m3_q8_0(None, None, None, 0, 64, None) == m.Status.OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
