@@ -368,7 +368,7 @@ class StackStep:
 
     SHAPES = ((6144, 5120), (5120, 5120), (17408, 5120), (17408, 5120), (5120, 17408))
 
-    def __init__(self, layers, device, seed=0x57AC0000, fused=False):
+    def __init__(self, layers, device, seed=0x57AC0000, fused=False, grouped=False):
         import torch
         import quantized_decode_memq_gb300 as memq
         from quantized_decode_memq_gb300 import synth
@@ -393,8 +393,8 @@ class StackStep:
         self.gemv_bytes = sum(gemv_bytes("blk", o, i, 1) for (o, i) in self.SHAPES)
         self.step_bytes = layers * (self.gemv_bytes + producer_bytes(1, 5120) * 2 +
                                     producer_bytes(1, 17408))
-        self.fused = fused
-        self.launches_per_step = (5 if fused else 8) * layers
+        self.fused, self.grouped = fused, grouped
+        self.launches_per_step = (5 if fused else 6 if grouped else 8) * layers
         torch.cuda.synchronize()
 
     def layer(self, l, x):
@@ -422,10 +422,28 @@ class StackStep:
         m.memq_rmsnorm_q8_1_gemv_e4m3_blk128(y[3], self.wn[2], w[4], g[4], 1e-6, qs=qs[2], d=d[2], y=y[4])
         return y[4]
 
+    def layer_grouped(self, l, x):
+        """The same layer with the GEMVs that share an activation in one launch each (5120->6144
+        with 5120->5120; gate with up): 6 launches."""
+        m = self.memq
+        w, g, y, qs, d = self.w[l], self.g[l], self.y, self.qs, self.d
+        m.memq_rmsnorm_q8_1(x, self.wn[0], 1e-6, qs=qs[0], d=d[0], want_z=False)
+        m.memq_gemv_e4m3_blk128_group(w[0:2], g[0:2], qs[0], d[0], ys=y[0:2])
+        m.memq_rmsnorm_q8_1(y[1], self.wn[1], 1e-6, qs=qs[1], d=d[1], want_z=False)
+        m.memq_gemv_e4m3_blk128_group(w[2:4], g[2:4], qs[1], d[1], ys=y[2:4])
+        m.memq_rmsnorm_q8_1(y[3], self.wn[2], 1e-6, qs=qs[2], d=d[2], want_z=False)
+        m.memq_gemv_e4m3_blk128(w[4], g[4], qs[2], d[2], y=y[4])
+        return y[4]
+
     def step(self, i):
         x = self.x0
         for l in range(self.layers):
-            x = self.layer_fused(l, x) if self.fused else self.layer(l, x)
+            if self.fused:
+                x = self.layer_fused(l, x)
+            elif self.grouped:
+                x = self.layer_grouped(l, x)
+            else:
+                x = self.layer(l, x)
 
 
 def capture(fn, n, stream):
@@ -674,13 +692,14 @@ def run_other(args, world, rank, local, dev):
                 f" -> Q8_0 slab, {out_f}x{in_f}, read 1 B + write 1.0625 B per weight")
     else:
         layers = int(args.workload[len("stack"):] or 48)
-        fused = args.step == "fused"
-        wl = StackStep(layers, dev, fused=fused)
+        fused, grouped = args.step == "fused", args.step == "group"
+        wl = StackStep(layers, dev, fused=fused, grouped=grouped)
         per_graph = 1
         desc = (f"{args.workload}: one token through {layers} layers of block-128 E4M3 GEMVs "
                 f"(5120->6144, 5120->5120, 5120->17408 x2, 17408->5120) with 3 RMSNorm->q8_1 "
                 + ("fused into the GEMVs (5 launches per layer)" if fused else
-                   "producers each (8 launches per layer)"))
+                   "producers, GEMVs on one activation grouped (6 launches per layer)" if grouped
+                   else "producers each (8 launches per layer)"))
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for i in range(per_graph):
@@ -913,8 +932,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMV launch from an ncu capture of this kernel")
-    ap.add_argument("--step", choices=["fused", "split"], default="split",
-                    help="decode step as one fused launch or as producer + GEMV launches")
+    ap.add_argument("--step", choices=["fused", "split", "group"], default="split",
+                    help="decode step as one fused launch or as producer + GEMV launches; "
+                         "for the stack, 'group' runs the GEMVs that share an activation as one "
+                         "grouped launch")
     ap.add_argument("--ncu-launches", type=int, default=0,
                     help="profiling entry: run one producer and N GEMV launches, no timing")
     args = ap.parse_args(argv)

@@ -147,6 +147,28 @@ int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps, cons
 
 /* Human-readable name of a memq_status value (static storage; never NULL). */
 /*
+ * memq_gemv_*_group -- up to 4 GEMVs of the same container that share one activation (qs, d,
+ * in_f, m), e.g. the gate and up projections, or q and k/v, in ONE launch: the matrices' rows
+ * are split over the CTAs in proportion; every output equals the corresponding single
+ * memq_gemv_* call bit for bit.  w, w_scale / grid, y and out_f are HOST arrays of `count`
+ * entries (device pointers / row counts), read during the call only.  Per matrix the
+ * single-call rules apply; every out_f must be >= 1.  If any matrix is off the fast path (an
+ * unaligned pointer, Q8_0 rows not 16-byte aligned) the call falls back to one launch per
+ * matrix.  Part of the "dual gate+up GEMV sharing one activation read" named among the unfused
+ * sites of q8_fuse_gate.rs (`main`).
+ * Errors: MEMQ_ERR_SHAPE (count outside [1, 4], an empty matrix, a bad size), MEMQ_ERR_NULL,
+ * MEMQ_ERR_ALIGN, MEMQ_ERR_M_RANGE, MEMQ_ERR_LAUNCH.
+ */
+int memq_gemv_e4m3_group(int count, const uint8_t *const *w, const float *const *w_scale,
+                         float *const *y, const int64_t *out_f, const int8_t *qs, const float *d,
+                         int64_t in_f, int m, void *stream);
+int memq_gemv_e4m3_blk128_group(int count, const uint8_t *const *w, const float *const *grid,
+                                float *const *y, const int64_t *out_f, const int8_t *qs,
+                                const float *d, int64_t in_f, int m, void *stream);
+int memq_gemv_q8_0_group(int count, const void *const *w, float *const *y, const int64_t *out_f,
+                         const int8_t *qs, const float *d, int64_t in_f, int m, void *stream);
+
+/*
  * memq_silu_mul_q8_1 -- the silu(gate) * up -> q8_1 activation producer.
  * Named on q8_fuse_gate.rs (`main`: the expert-ff width 1536, the "silu/gate*up -> q8_1"
  * fusion site).  For each row r < rows and column i < ncols:

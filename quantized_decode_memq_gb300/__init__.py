@@ -17,6 +17,7 @@ slab at load).
 from __future__ import annotations
 
 from ._binding import (  # noqa: F401
+    MAX_GROUP,
     MAX_M,
     MAX_NCOLS,
     MemqError,
@@ -26,7 +27,10 @@ from ._binding import (  # noqa: F401
     memq_device_fault,
     memq_gemv_e4m3,
     memq_gemv_e4m3_blk128,
+    memq_gemv_e4m3_blk128_group,
+    memq_gemv_e4m3_group,
     memq_gemv_q8_0,
+    memq_gemv_q8_0_group,
     memq_rmsnorm_q8_1,
     memq_rmsnorm_q8_1_gemv_e4m3,
     memq_rmsnorm_q8_1_gemv_e4m3_blk128,

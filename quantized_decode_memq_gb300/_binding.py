@@ -15,6 +15,7 @@ _lib = None
 
 MAX_M = 8
 MAX_NCOLS = 32768
+MAX_GROUP = 4
 
 
 class Status(enum.IntEnum):
@@ -60,6 +61,11 @@ def lib() -> ctypes.CDLL:
                                                              P, P, I64, I64, I32, P]
             L.memq_rmsnorm_q8_1_gemv_q8_0.argtypes = [P, P, ctypes.c_float, P, P, P, P, P, I64,
                                                       I64, I32, P]
+            PP = ctypes.POINTER(ctypes.c_void_p)
+            PI64 = ctypes.POINTER(ctypes.c_int64)
+            L.memq_gemv_e4m3_group.argtypes = [I32, PP, PP, PP, PI64, P, P, I64, I32, P]
+            L.memq_gemv_e4m3_blk128_group.argtypes = [I32, PP, PP, PP, PI64, P, P, I64, I32, P]
+            L.memq_gemv_q8_0_group.argtypes = [I32, PP, PP, PI64, P, P, I64, I32, P]
             L.memq_silu_mul_q8_1.argtypes = [P, P, P, P, P, I64, I64, P]
             L.memq_repack_e4m3_q8_0.argtypes = [P, P, P, I64, I64, P]
             L.memq_repack_e4m3_blk128_q8_0.argtypes = [P, P, P, I64, I64, P]
@@ -70,7 +76,8 @@ def lib() -> ctypes.CDLL:
             for name in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
                          "memq_gemv_q8_0", "memq_rmsnorm_q8_1_gemv_e4m3",
                          "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
-                         "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
+                         "memq_gemv_e4m3_group", "memq_gemv_e4m3_blk128_group",
+                         "memq_gemv_q8_0_group", "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
                          "memq_repack_e4m3_blk128_q8_0", "memq_device_fault", "memq_version"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -332,3 +339,65 @@ def memq_repack_e4m3_blk128_q8_0(w: torch.Tensor, grid: torch.Tensor, *, out=Non
     out_f, in_f = w.shape
     return _repack("memq_repack_e4m3_blk128_q8_0", w, grid,
                    ((out_f + 127) // 128, (in_f + 127) // 128), out, stream)
+
+
+def _group(fn: str, ws, auxs, qs, d, ys, stream, aux_shape):
+    count = len(ws)
+    if not 1 <= count <= MAX_GROUP:
+        raise ValueError(f"{fn}: 1 to {MAX_GROUP} matrices, got {count}")
+    in_f = ws[0].shape[1] if ws[0].dim() == 2 else None
+    for i, w in enumerate(ws):
+        _cuda(f"w[{i}]", w, torch.uint8)
+    qs2, d2, m = _act(qs, d, in_f)
+    outs = []
+    for i, w in enumerate(ws):
+        out_f = w.shape[0]
+        if auxs is not None:
+            _cuda(f"aux[{i}]", auxs[i], torch.float32, aux_shape(out_f, in_f))
+        y = None if ys is None else ys[i]
+        outs.append(_out(y, m, out_f, w.device))
+    VP = ctypes.c_void_p * count
+    wp = VP(*[w.data_ptr() for w in ws])
+    yp = VP(*[y.data_ptr() for y in outs])
+    of = (ctypes.c_int64 * count)(*[w.shape[0] for w in ws])
+    args = [count, wp]
+    if auxs is not None:
+        args.append(VP(*[a.data_ptr() for a in auxs]))
+    args += [yp, of, _ptr(qs2), _ptr(d2), in_f, m, _stream(stream)]
+    _check(fn, getattr(lib(), fn)(*args))
+    return outs
+
+
+def memq_gemv_e4m3_group(ws, w_scales, qs, d, *, ys=None, stream=None):
+    """Several E4M3 GEMVs sharing one activation, one launch.  Returns [y_i]."""
+    return _group("memq_gemv_e4m3_group", ws, w_scales, qs, d, ys, stream, lambda o, i: (1,))
+
+
+def memq_gemv_e4m3_blk128_group(ws, grids, qs, d, *, ys=None, stream=None):
+    """Several block-128 E4M3 GEMVs sharing one activation, one launch.  Returns [y_i]."""
+    return _group("memq_gemv_e4m3_blk128_group", ws, grids, qs, d, ys, stream,
+                  lambda o, i: ((o + 127) // 128, (i + 127) // 128))
+
+
+def memq_gemv_q8_0_group(ws, qs, d, *, in_f=None, ys=None, stream=None):
+    """Several Q8_0 GEMVs sharing one activation, one launch.  ws: uint8 [out_f, in_f/32*34]."""
+    return _group_q8(ws, qs, d, in_f, ys, stream)
+
+
+def _group_q8(ws, qs, d, in_f, ys, stream):
+    count = len(ws)
+    if not 1 <= count <= MAX_GROUP:
+        raise ValueError(f"memq_gemv_q8_0_group: 1 to {MAX_GROUP} matrices, got {count}")
+    for i, w in enumerate(ws):
+        _cuda(f"w[{i}]", w, torch.uint8)
+    if in_f is None:
+        in_f = ws[0].shape[1] // 34 * 32
+    qs2, d2, m = _act(qs, d, in_f)
+    outs = [_out(None if ys is None else ys[i], m, w.shape[0], w.device) for i, w in enumerate(ws)]
+    VP = ctypes.c_void_p * count
+    rc = lib().memq_gemv_q8_0_group(count, VP(*[w.data_ptr() for w in ws]),
+                                    VP(*[y.data_ptr() for y in outs]),
+                                    (ctypes.c_int64 * count)(*[w.shape[0] for w in ws]),
+                                    _ptr(qs2), _ptr(d2), in_f, m, _stream(stream))
+    _check("memq_gemv_q8_0_group", rc)
+    return outs

@@ -16,6 +16,13 @@ extern "C" int memq_rmsnorm_q8_1_gemv_e4m3_blk128(const float *x, const float *w
                                          stream);
 }
 
+extern "C" int memq_gemv_e4m3_blk128_group(int count, const uint8_t *const *w,
+                                           const float *const *grid, float *const *y,
+                                           const int64_t *out_f, const int8_t *qs, const float *d,
+                                           int64_t in_f, int m, void *stream) {
+    return memq::group_entry<memq::kBlk>(count, w, grid, y, out_f, qs, d, in_f, m, stream);
+}
+
 // Internal: this translation unit's device fault word (not part of the public header).
 int memq_internal_fault_blk128(unsigned int *out, bool clear) {
     return memq::read_fault(out, clear) == cudaSuccess ? 0 : 1;

@@ -100,6 +100,9 @@ struct Geo {
     static constexpr int kWarpBlocks = kChunkBlocks / kWarps;  // E4M3: blocks per warp per stage
 };
 
+// Weight matrices one launch may cover (sharing the activation: gate / up, q / k / v).
+constexpr int kMaxGroup = 4;
+
 struct StreamArgs {
     const uint8_t *w;
     const float *aux;  // per-tensor scale (E4M3) or grid (block-128); unused for Q8_0
@@ -123,6 +126,14 @@ struct StreamArgs {
     uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_red, off_ring;
     int use_tma;  // 1: full tiles (and 8-row halves) come as one tensor copy each
     int ctas_per_sm;  // host: CTAs per SM the plan sized shared memory for
+    // The launch's matrices: matrix i owns CTAs [mat_cta[i], mat_cta[i+1]); each CTA takes w,
+    // aux, y and out_f above from its matrix.  A plain GEMV is a group of one.
+    int nmat;
+    int mat_cta[kMaxGroup + 1];
+    const uint8_t *mat_w[kMaxGroup];
+    const float *mat_aux[kMaxGroup];
+    float *mat_y[kMaxGroup];
+    int64_t mat_out_f[kMaxGroup];
 };
 
 // Tensor maps over the weight plane viewed as [out_f rows][row_bytes / 8] 64-bit elements, box
@@ -134,6 +145,10 @@ struct StreamArgs {
 struct TmaMaps {
     CUtensorMap tile;
     CUtensorMap oct;
+};
+
+struct TmaGroup {
+    TmaMaps m[kMaxGroup];
 };
 
 // Where the consumers read the activation from.
@@ -496,18 +511,30 @@ __device__ __forceinline__ bool thread_wait_bounded(uint64_t *bar, uint32_t pari
 
 template <int KIND, int M, int MODE, bool FUSE>
 __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
-    gemv_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMaps tm) {
+    gemv_stream_kernel(const __grid_constant__ StreamArgs args, const __grid_constant__ TmaGroup tg) {
     using G = Geo<KIND>;
     constexpr int TR = G::kTileRows;
     extern __shared__ __align__(128) uint8_t smem[];
     griddep_launch_dependents();
 
+    // This CTA's matrix, and its share of that matrix's rows.
+    int mi = 0;
+    while (mi + 1 < args.nmat && static_cast<int>(blockIdx.x) >= args.mat_cta[mi + 1]) ++mi;
+    StreamArgs a = args;
+    a.w = args.mat_w[mi];
+    a.aux = args.mat_aux[mi];
+    a.y = args.mat_y[mi];
+    a.out_f = args.mat_out_f[mi];
+    const TmaMaps &tm = tg.m[mi];
+    const int64_t cta = static_cast<int64_t>(blockIdx.x) - args.mat_cta[mi];
+    const int64_t ncta = args.mat_cta[mi + 1] - args.mat_cta[mi];
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = a.stages;
 
-    const int64_t R0 = static_cast<int64_t>(blockIdx.x) * a.out_f / gridDim.x;
-    const int64_t R1 = static_cast<int64_t>(blockIdx.x + 1) * a.out_f / gridDim.x;
+    const int64_t R0 = cta * a.out_f / ncta;
+    const int64_t R1 = (cta + 1) * a.out_f / ncta;
     const int ntiles = static_cast<int>((R1 - R0 + TR - 1) / TR);
     const int nch = (a.nb + G::kChunkBlocks - 1) / G::kChunkBlocks;
     const int items = ntiles * nch;
@@ -908,9 +935,19 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes);
     if (e != cudaSuccess) return e;
     per_sm = std::max(per_sm, 1);
-    // One wave of CTAs, never more CTAs than output rows.
-    int64_t grid = static_cast<int64_t>(info.sms) * std::min({per_sm, G::kCtasPerLaunch, a.ctas_per_sm});
-    grid = std::min<int64_t>(grid, a.out_f);
+    // One wave of CTAs, split over the launch's matrices in proportion to their rows (rounded
+    // up, so no matrix gets more rows per CTA than the plan assumed), never more CTAs than rows.
+    const int64_t total = static_cast<int64_t>(info.sms) * std::min({per_sm, G::kCtasPerLaunch, a.ctas_per_sm});
+    int64_t rows_all = 0;
+    for (int i = 0; i < a.nmat; ++i) rows_all += a.mat_out_f[i];
+    int64_t grid = 0;
+    for (int i = 0; i < a.nmat; ++i) {
+        int64_t n = (total * a.mat_out_f[i] + rows_all - 1) / rows_all;
+        n = std::max<int64_t>(1, std::min<int64_t>(n, a.mat_out_f[i]));
+        a.mat_cta[i] = static_cast<int>(grid);
+        grid += n;
+    }
+    a.mat_cta[a.nmat] = static_cast<int>(grid);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
@@ -921,9 +958,17 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    TmaMaps tm = {};
-    make_maps<KIND>(a, tm);
-    return cudaLaunchKernelEx(&cfg, kern, a, tm);
+    TmaGroup tg = {};
+    int tma_ok = 1;
+    for (int i = 0; i < a.nmat; ++i) {
+        StreamArgs ai = a;
+        ai.w = a.mat_w[i];
+        ai.out_f = a.mat_out_f[i];
+        make_maps<KIND>(ai, tg.m[i]);
+        tma_ok &= ai.use_tma;
+    }
+    a.use_tma = tma_ok;
+    return cudaLaunchKernelEx(&cfg, kern, a, tg);
 }
 
 template <int KIND, int MODE, bool FUSE>
@@ -1057,6 +1102,11 @@ StreamArgs base_args(const uint8_t *w, const float *aux, const int8_t *qs, const
     a.in_f = static_cast<int>(in_f);
     a.nb = static_cast<int>(in_f / 32);
     a.gcols = static_cast<int>((in_f + 127) / 128);
+    a.nmat = 1;
+    a.mat_w[0] = w;
+    a.mat_aux[0] = aux;
+    a.mat_y[0] = y;
+    a.mat_out_f[0] = out_f;
     return a;
 }
 
@@ -1089,6 +1139,59 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
             w, aux, qs, d, y, out_f, static_cast<int>(in_f), m);
         e = cudaGetLastError();
     }
+    return e == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+}
+
+// A group of GEMVs sharing one activation (qs, d, in_f, m) in one launch: the matrices' rows
+// are split over the CTAs in proportion, each CTA streams one matrix, and every CTA stages the
+// same activation.  Taken when every matrix is on the fast path; otherwise one GEMV per matrix.
+template <int KIND>
+int group_entry(int count, const uint8_t *const *w, const float *const *aux, float *const *y,
+                const int64_t *out_f, const int8_t *qs, const float *d, int64_t in_f, int m,
+                void *stream) {
+    if (count < 1 || count > kMaxGroup) return MEMQ_ERR_SHAPE;
+    if (!w || !y || !out_f || (!is_q80(KIND) && !aux)) return MEMQ_ERR_NULL;
+    int64_t rows_all = 0;
+    bool fast = true;
+    for (int i = 0; i < count; ++i) {
+        const int rc = check_gemv_args<KIND>(w[i], is_q80(KIND) ? nullptr : aux[i], qs, d, y[i],
+                                             out_f[i], in_f, m);
+        if (rc > 0) return rc;
+        if (rc == MEMQ_OK) return MEMQ_ERR_SHAPE;  // an empty matrix in a group
+        rows_all += out_f[i];
+        fast = fast && fast_path_ok<KIND>(w[i], qs, in_f);
+    }
+    if (!fast) {
+        for (int i = 0; i < count; ++i) {
+            const int rc = gemv_entry<KIND>(w[i], is_q80(KIND) ? nullptr : aux[i], qs, d, y[i],
+                                            out_f[i], in_f, m, stream);
+            if (rc != MEMQ_OK) return rc;
+        }
+        return MEMQ_OK;
+    }
+    int dev = 0;
+    DeviceInfo info;
+    if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
+    StreamArgs a = base_args<KIND>(w[0], is_q80(KIND) ? nullptr : aux[0], qs, d, y[0], out_f[0], in_f);
+    a.nmat = count;
+    for (int i = 0; i < count; ++i) {
+        a.mat_w[i] = w[i];
+        a.mat_aux[i] = is_q80(KIND) ? nullptr : aux[i];
+        a.mat_y[i] = y[i];
+        a.mat_out_f[i] = out_f[i];
+    }
+    uint32_t smem = 0;
+    int mode = kActGlobal;
+    if (!plan_stream<KIND>(rows_all, in_f, m, false, info, a, smem, mode)) {
+        for (int i = 0; i < count; ++i) {
+            const int rc = gemv_entry<KIND>(w[i], is_q80(KIND) ? nullptr : aux[i], qs, d, y[i],
+                                            out_f[i], in_f, m, stream);
+            if (rc != MEMQ_OK) return rc;
+        }
+        return MEMQ_OK;
+    }
+    const cudaError_t e = launch_planned<KIND, false>(m, mode, a, smem, dev, info,
+                                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
 }
 

@@ -23,6 +23,22 @@ extern "C" int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, floa
                                          stream);
 }
 
+extern "C" int memq_gemv_q8_0_group(int count, const void *const *w, float *const *y,
+                                    const int64_t *out_f, const int8_t *qs, const float *d,
+                                    int64_t in_f, int m, void *stream) {
+    if (count < 1 || count > memq::kMaxGroup) return MEMQ_ERR_SHAPE;
+    if (!w || !out_f) return MEMQ_ERR_NULL;
+    const uint8_t *w8[memq::kMaxGroup];
+    int64_t rows = 0;
+    for (int i = 0; i < count; ++i) {
+        w8[i] = static_cast<const uint8_t *>(w[i]);
+        rows += out_f[i];
+    }
+    if (memq::q80_on_tensor_cores(rows, in_f, m))
+        return memq::group_entry<memq::kQ80T>(count, w8, nullptr, y, out_f, qs, d, in_f, m, stream);
+    return memq::group_entry<memq::kQ80>(count, w8, nullptr, y, out_f, qs, d, in_f, m, stream);
+}
+
 // Internal: this translation unit's device fault word (not part of the public header).
 int memq_internal_fault_q8_0(unsigned int *out, bool clear) {
     return memq::read_fault(out, clear) == cudaSuccess ? 0 : 1;

@@ -36,7 +36,8 @@ def test_header_declares_the_boundary():
     for required in ("memq_rmsnorm_q8_1", "memq_gemv_e4m3", "memq_gemv_e4m3_blk128",
                      "memq_gemv_q8_0", "memq_rmsnorm_q8_1_gemv_e4m3",
                      "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
-                     "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
+                     "memq_gemv_e4m3_group", "memq_gemv_e4m3_blk128_group",
+                     "memq_gemv_q8_0_group", "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
                      "memq_repack_e4m3_blk128_q8_0",
                      "memq_status_string", "memq_device_fault", "memq_version"):
         assert required in names
@@ -78,6 +79,15 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.memq_rmsnorm_q8_1_gemv_e4m3_blk128(fake, fake, -1.0, fake, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_SHAPE
     assert lib.memq_rmsnorm_q8_1_gemv_q8_0(fake, fake, 1e-6, fake, fake, fake, None, fake, 4, 65536, 1, None) == m.Status.ERR_SHAPE
     assert lib.memq_rmsnorm_q8_1_gemv_q8_0(P(0x1004), fake, 1e-6, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_ALIGN
+    # grouped GEMVs: the count and the host arrays are checked first
+    VP2 = ctypes.c_void_p * 2
+    I2 = ctypes.c_int64 * 2
+    ws, ys = VP2(0x1000, 0x1000), VP2(0x1000, 0x1000)
+    assert lib.memq_gemv_e4m3_group(0, ws, ws, ys, I2(4, 4), fake, fake, 64, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_gemv_e4m3_blk128_group(5, ws, ws, ys, I2(4, 4), fake, fake, 64, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_gemv_q8_0_group(2, None, ys, I2(4, 4), fake, fake, 256, 1, None) == m.Status.ERR_NULL
+    assert lib.memq_gemv_e4m3_group(2, ws, ws, ys, I2(4, 0), fake, fake, 64, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_gemv_e4m3_group(2, ws, ws, ys, I2(4, 4), fake, fake, 64, 9, None) == m.Status.ERR_M_RANGE
     # silu(gate) * up -> q8_1 producer
     assert lib.memq_silu_mul_q8_1(fake, fake, None, fake, fake, 48, 1, None) == m.Status.ERR_SHAPE
     assert lib.memq_silu_mul_q8_1(None, fake, None, fake, fake, 64, 1, None) == m.Status.ERR_NULL
