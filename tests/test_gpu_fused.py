@@ -67,9 +67,12 @@ def run_case(memq, oracle, kind, out_f, in_f, m, seed, rows=None, page=True):
 
 
 @pytest.mark.parametrize("kind", KINDS)
+# in_f / 32 divisible by 8 runs the clustered prologue (8 CTAs share the RMSNorm -> q8_1);
+# 96 and 1056 (3 and 33 blocks) take the per-CTA prologue.
 @pytest.mark.parametrize("out_f,in_f,m", [(4096, 4096, 1), (1024, 4096, 1), (37, 256, 1),
                                           (257, 1024 + 256, 3), (777, 5120, 8), (5120, 5120, 2),
-                                          (300, 17408, 1)])
+                                          (300, 17408, 1), (3, 512, 2), (129, 96, 1),
+                                          (500, 1024 + 32, 4)])
 def test_fused_parity(memq, oracle, kind, out_f, in_f, m):
     rows = sample_rows(out_f, 128, seed=out_f + m) if out_f > 1024 else None
     run_case(memq, oracle, kind, out_f, in_f, m, seed=out_f + in_f + m, rows=rows)
