@@ -102,6 +102,9 @@ struct Geo {
 
 // Weight matrices one launch may cover (sharing the activation: gate / up, q / k / v).
 constexpr int kMaxGroup = 4;
+// Block-128: the per-CTA d * grid table is used up to this many activation rows (measured: it
+// saves the consumers a multiply per scale at m <= 2; at m = 8 its size costs ring stages).
+constexpr int kDgMaxM = 2;
 
 struct StreamArgs {
     const uint8_t *w;
@@ -124,6 +127,9 @@ struct StreamArgs {
     float *z_out;
     // Shared-memory layout (bytes); barriers at 0.
     uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_red, off_ring;
+    // Block-128 with a staged activation: the per-(grid row, token, block) scale
+    // d[token][block] * grid[row][block / 4], formed once per CTA (0 = not used).
+    uint32_t off_dg;
     int use_tma;  // 1: full tiles (and 8-row halves) come as one tensor copy each
     int ctas_per_sm;  // host: CTAs per SM the plan sized shared memory for
     // The launch's matrices: matrix i owns CTAs [mat_cta[i], mat_cta[i+1]); each CTA takes w,
@@ -189,14 +195,18 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
     const uint4 *bfrag = reinterpret_cast<const uint4 *>(sm + a.off_bfrag);
     const int8_t *s_qs = reinterpret_cast<const int8_t *>(sm + a.off_qs);
     const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
-    const float *grow0 = nullptr, *grow8 = nullptr;
+    const float *grow0 = nullptr, *grow8 = nullptr, *dg0 = nullptr, *dg8 = nullptr;
     if (KIND == kBlk) {
-        // Grid rows of this thread's two tile rows, from the CTA's staged grid rows.
+        // Grid rows of this thread's two tile rows, from the CTA's staged grid rows (or their
+        // d * grid tables).
         const int64_t r0 = row0 + g > row_last ? row_last : row0 + g;
         const int64_t r8 = row0 + g + 8 > row_last ? row_last : row0 + g + 8;
         const float *s_grid = reinterpret_cast<const float *>(sm + a.off_grid);
         grow0 = s_grid + ((r0 >> 7) - grow_base) * a.gcols;
         grow8 = s_grid + ((r8 >> 7) - grow_base) * a.gcols;
+        const float *s_dg = reinterpret_cast<const float *>(sm + a.off_dg);
+        dg0 = s_dg + ((r0 >> 7) - grow_base) * M * a.nb;
+        dg8 = s_dg + ((r8 >> 7) - grow_base) * M * a.nb;
     }
 #pragma unroll
     for (int b = 0; b < G::kWarpBlocks; ++b) {
@@ -219,22 +229,35 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
                     s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
                 }
             }
-            float k0 = 0.f, k1 = 0.f;
-            if (MODE == kActGlobal) {
-                if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
-                if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
+            float k0 = 0.f, k1 = 0.f, k2 = 0.f, k3 = 0.f;
+            if (KIND == kBlk && MODE != kActGlobal && M <= kDgMaxM) {
+                // the CTA's d * grid table: one load per scale, no multiply
+                if (2 * t < M) {
+                    k0 = dg0[(2 * t) * a.nb + kb];
+                    k2 = dg8[(2 * t) * a.nb + kb];
+                }
+                if (2 * t + 1 < M) {
+                    k1 = dg0[(2 * t + 1) * a.nb + kb];
+                    k3 = dg8[(2 * t + 1) * a.nb + kb];
+                }
             } else {
-                if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
-                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
-            }
-            float k2 = k0, k3 = k1;
-            if (KIND == kBlk) {
-                const float gg = grow0[kb >> 2];
-                const float gg8 = grow8[kb >> 2];
-                k0 *= gg;
-                k1 *= gg;
-                k2 *= gg8;
-                k3 *= gg8;
+                if (MODE == kActGlobal) {
+                    if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
+                    if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
+                } else {
+                    if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
+                    if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
+                }
+                k2 = k0;
+                k3 = k1;
+                if (KIND == kBlk) {
+                    const float gg = grow0[kb >> 2];
+                    const float gg8 = grow8[kb >> 2];
+                    k0 *= gg;
+                    k1 *= gg;
+                    k2 *= gg8;
+                    k3 *= gg8;
+                }
             }
             const uint8_t *pa = stage + g * G::kSlot + 32 * b + 8 * t;
             const uint2 wa = lds64(pa);
@@ -667,6 +690,23 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
             bfrag[i] = v;
         }
     }
+    if (KIND == kBlk && MODE != kActGlobal && M <= kDgMaxM) {
+        // d * grid for every (grid row of this CTA, token, block): the same f32 products the
+        // consumers would otherwise form per block.  (s_d and the grid rows are complete:
+        // written by this thread's own copies / waits or before the barrier below.)
+        named_barrier_consumers();
+        const float *s_d = reinterpret_cast<const float *>(smem + a.off_d);
+        const float *s_grid = reinterpret_cast<const float *>(smem + a.off_grid);
+        float *s_dg = reinterpret_cast<float *>(smem + a.off_dg);
+        const int nrows = static_cast<int>(((R1 - 1) >> 7) - grow_base + 1);
+        const int per_row = M * a.nb;
+        for (int i = threadIdx.x; i < nrows * per_row; i += kConsumerThreads) {
+            const int gr = i / per_row;
+            const int rem = i - gr * per_row;
+            const int kb = rem % a.nb;
+            s_dg[i] = __fmul_rn(s_d[rem], s_grid[gr * a.gcols + (kb >> 2)]);
+        }
+    }
     named_barrier_consumers();
 
     int c_stage = 0;
@@ -931,6 +971,7 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     a.off_d += bars;
     a.off_red += bars;
     a.off_ring += bars;
+    if (a.off_dg) a.off_dg += bars;
     smem_bytes = fixed + bars + static_cast<uint32_t>(S * G::kStage);
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes);
     if (e != cudaSuccess) return e;
@@ -1021,6 +1062,8 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * 64), 128);
     const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
     const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
+    // block-128 with a staged activation: the CTA's d * grid table
+    const uint32_t dgb = (KIND == kBlk && m <= kDgMaxM) ? align_up(static_cast<uint32_t>(grid_rows * m * nb * 4), 128) : 0u;
     const uint32_t red = fuse ? align_up((kWarps + 1) * 8, 128) : 0u;
     const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
     const uint32_t base = part + gridb + red + ring_min;
@@ -1036,9 +1079,9 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     for (int k = k_rows; k >= 1; --k) {
         // Shared memory one CTA may use and still leave room for k CTAs per SM.
         const uint32_t budget = std::min(optin, static_cast<uint32_t>(info.smem_sm / k - 1024));
-        if (G::kMma && base + qsb + db + frag <= budget) {
+        if (G::kMma && base + qsb + db + dgb + frag <= budget) {
             mode = kActFrag;
-        } else if (base + qsb + db <= budget) {
+        } else if (base + qsb + db + dgb <= budget) {
             mode = kActSmem;
         } else {
             continue;
@@ -1058,6 +1101,11 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     if (mode != kActGlobal) off += qsb;
     a.off_d = off;
     if (mode != kActGlobal) off += db;
+    a.off_dg = 0;
+    if (KIND == kBlk && mode != kActGlobal && m <= kDgMaxM) {
+        a.off_dg = off;
+        off += align_up(static_cast<uint32_t>(grid_rows * m * nb * 4), 128);
+    }
     a.off_red = off;
     off += red;  // cross-warp scratch of the fused prologue
     a.off_ring = off;
