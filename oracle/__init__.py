@@ -71,6 +71,10 @@ def _load():
                                                          P, I64, P, P]
             lib.memq_oracle_gemv_q8_0.argtypes = [P, P, P, I64, I64, ctypes.c_int, P, I64,
                                                   P, P]
+            lib.memq_oracle_mla_head_gemv.argtypes = [P, P, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_int, P, P]
+            lib.memq_oracle_mla_attn_gathered.argtypes = [P, P, P, P] + [ctypes.c_int] * 5 + [
+                ctypes.c_float, P, P, P]
             lib.memq_oracle_silu_mul.argtypes = [P, P, I64, P]
             lib.memq_oracle_f16_bits.argtypes = [ctypes.c_double]
             lib.memq_oracle_f16_bits.restype = ctypes.c_uint16
@@ -79,7 +83,8 @@ def _load():
                          "memq_oracle_rmsnorm", "memq_oracle_quantize_q8_1",
                          "memq_oracle_gemv_e4m3", "memq_oracle_gemv_e4m3_blk128",
                          "memq_oracle_gemv_q8_0", "memq_oracle_silu_mul",
-                         "memq_oracle_repack_q8_0"):
+                         "memq_oracle_repack_q8_0", "memq_oracle_mla_head_gemv",
+                         "memq_oracle_mla_attn_gathered"):
                 getattr(lib, name).restype = None
             _lib = lib
     return _lib
@@ -253,3 +258,50 @@ def repack_q8_0(w: np.ndarray, aux: np.ndarray, grid: bool):
     _load().memq_oracle_repack_q8_0(_ptr(w), _ptr(aux), int(grid), out_f, in_f, _ptr(out),
                                     _ptr(d))
     return out, d
+
+
+# ------------------------------------------------------------------------------------------
+# t <= 8 MLA decode attention (mla_decode_arm_gate.rs)
+# ------------------------------------------------------------------------------------------
+
+def mla_head_gemv(x: np.ndarray, w: np.ndarray):
+    """out[t,h,i] = sum_k x[t,h,k] * w[h,i,k]; x f32 [t,nh,cols], w f32 [nh,rows,cols].
+
+    Returns (out f64 [t,nh,rows], sabs f64 [t,nh,rows] = sum |terms|)."""
+    x = _c(x, np.float32)
+    w = _c(w, np.float32)
+    t, nh, cols = x.shape
+    assert w.shape[0] == nh and w.shape[2] == cols
+    rows = w.shape[1]
+    out = np.empty((t, nh, rows), np.float64)
+    sabs = np.empty((t, nh, rows), np.float64)
+    _load().memq_oracle_mla_head_gemv(_ptr(x), _ptr(w), t, nh, rows, cols, _ptr(out), _ptr(sabs))
+    return out, sabs
+
+
+def mla_absorb_q(q_nope, wk_b):
+    """absorb_q: q_nope [t,nh,d_nope], wk_b [nh,kv_rank,d_nope] -> [t,nh,kv_rank]."""
+    return mla_head_gemv(q_nope, wk_b)
+
+
+def mla_decompress_v(o_lat, wv_b):
+    """decompress_v: o_lat [t,nh,kv_rank], wv_b [nh,d_v,kv_rank] -> [t,nh,d_v]."""
+    return mla_head_gemv(o_lat, wv_b)
+
+
+def mla_attn_gathered(q_lat, q_pe, cache, idx, scale: float, d_rope: int = 0, scores=False):
+    """q_lat [t,nh,kv_rank], q_pe [t,nh,d_rope], cache [kv, kv_rank+d_rope], idx int32
+    [t,n_slots] -> (out f64 [t,nh,kv_rank], cabs f64 = max_j |c_j[r]|[, scores f64])."""
+    q_lat = _c(q_lat, np.float32)
+    t, nh, kv_rank = q_lat.shape
+    q_pe = _c(q_pe if q_pe is not None and q_pe.size else np.zeros((t, nh, max(d_rope, 1)), np.float32), np.float32)
+    cache = _c(cache, np.float32)
+    idx = _c(idx, np.int32)
+    n_slots = idx.shape[1]
+    out = np.empty((t, nh, kv_rank), np.float64)
+    cabs = np.empty((t, nh, kv_rank), np.float64)
+    sc = np.empty((t, nh, n_slots), np.float64) if scores else None
+    _load().memq_oracle_mla_attn_gathered(_ptr(q_lat), _ptr(q_pe), _ptr(cache), _ptr(idx), nh,
+                                          kv_rank, d_rope, t, n_slots, ctypes.c_float(scale),
+                                          _ptr(out), _ptr(cabs), None if sc is None else _ptr(sc))
+    return (out, cabs, sc) if scores else (out, cabs)

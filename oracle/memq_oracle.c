@@ -35,6 +35,10 @@
  *                        the repacked slab against the GEMV of the E4M3 source within the
  *                        quantization bound
  *
+ *   memq_oracle_mla_*    library einsum / softmax of the same operands, one-hot and constant
+ *                        inputs (attention over identical rows returns the row; a one-slot
+ *                        gather returns that slot), softmax shift invariance
+ *
  * Also from the pages (SURVEY's "next" rows): q8_fuse_gate.rs, `main` -- the silu(gate)*up ->
  * q8_1 activation producer named for the 1536-wide expert site; gemv_e4m3_bench.rs, module doc
  * "QUESTION" -- the ship path that dequantizes FP8 weights to a Q8_0 slab at load ("ARM B'").
@@ -42,6 +46,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 /* ---------------------------------------------------------------------------------------------
  * Format decoders.
@@ -333,4 +338,87 @@ void memq_oracle_repack_q8_0(const uint8_t *w, const float *aux, int grid, int64
             }
         }
     }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * t <= 8 MLA decode attention (mla_decode_arm_gate.rs: the three kernels `absorb_q`,
+ * `decompress_v` and `attn_gathered`, geometry nh = 64 heads, kv_rank = 512, d_nope = d_v = 256,
+ * d_rope = 0, a top-k gather of n_slots rows from a cache of kv rows).  The pages give shapes and
+ * call sequences only; the readings:
+ *   absorb_q      out[t][h][r] = sum_d q_nope[t][h][d] * wk_b[h][r][d]       (wk_b [nh][kv_rank][d_nope])
+ *   decompress_v  out[t][h][v] = sum_r o_lat[t][h][r] * wv_b[h][v][r]        (wv_b [nh][d_v][kv_rank])
+ *   attn_gathered per (t, h), over the gathered rows c_j = cache[idx[t][j]] (kv_rank + d_rope
+ *                 floats): s_j = scale * (q_lat[t][h] . c_j[0:kv_rank] + q_pe[t][h] . c_j[kv_rank:]),
+ *                 p = softmax(s), out[t][h][r] = sum_j p_j * c_j[r]          (out [t][nh][kv_rank])
+ * Each also returns sabs, the sum of |terms| of every output (the scale of its rounding error).
+ * ------------------------------------------------------------------------------------------- */
+
+/* The per-head product shared by absorb_q and decompress_v: out[t][h][i] = sum_k x[t][h][k] *
+ * w[h][i][k], x [t][nh][cols], w [nh][rows][cols], out / sabs [t][nh][rows]. */
+void memq_oracle_mla_head_gemv(const float *x, const float *w, int t, int nh, int rows, int cols,
+                               double *out, double *sabs)
+{
+    for (int tt = 0; tt < t; ++tt)
+        for (int h = 0; h < nh; ++h)
+            for (int i = 0; i < rows; ++i) {
+                double acc = 0.0, s = 0.0;
+                const float *xr = x + ((int64_t)tt * nh + h) * cols;
+                const float *wr = w + ((int64_t)h * rows + i) * cols;
+                for (int k = 0; k < cols; ++k) {
+                    double p = (double)xr[k] * (double)wr[k];
+                    acc += p;
+                    s += fabs(p);
+                }
+                out[((int64_t)tt * nh + h) * rows + i] = acc;
+                sabs[((int64_t)tt * nh + h) * rows + i] = s;
+            }
+}
+
+/* out, cabs: [t][nh][kv_rank]; cabs[t][h][r] = max_j |c_j[r]| (the scale of the output's
+ * error).  scores (may be NULL): [t][nh][n_slots], the s_j. */
+void memq_oracle_mla_attn_gathered(const float *q_lat, const float *q_pe, const float *cache,
+                                   const int32_t *idx, int nh, int kv_rank, int d_rope, int t,
+                                   int n_slots, float scale, double *out, double *cabs,
+                                   double *scores)
+{
+    const int row = kv_rank + d_rope;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n_slots);
+    for (int tt = 0; tt < t; ++tt)
+        for (int h = 0; h < nh; ++h) {
+            const float *q = q_lat + ((int64_t)tt * nh + h) * kv_rank;
+            const float *qp = q_pe + ((int64_t)tt * nh + h) * d_rope;
+            double m = -INFINITY;
+            for (int j = 0; j < n_slots; ++j) {
+                const float *c = cache + (int64_t)idx[(int64_t)tt * n_slots + j] * row;
+                double dot = 0.0;
+                for (int r = 0; r < kv_rank; ++r)
+                    dot += (double)q[r] * (double)c[r];
+                for (int r = 0; r < d_rope; ++r)
+                    dot += (double)qp[r] * (double)c[kv_rank + r];
+                s[j] = (double)scale * dot;
+                if (scores)
+                    scores[((int64_t)tt * nh + h) * n_slots + j] = s[j];
+                if (s[j] > m)
+                    m = s[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < n_slots; ++j)
+                l += exp(s[j] - m);
+            double *o = out + ((int64_t)tt * nh + h) * kv_rank;
+            double *ca = cabs + ((int64_t)tt * nh + h) * kv_rank;
+            for (int r = 0; r < kv_rank; ++r) {
+                o[r] = 0.0;
+                ca[r] = 0.0;
+            }
+            for (int j = 0; j < n_slots; ++j) {
+                const float *c = cache + (int64_t)idx[(int64_t)tt * n_slots + j] * row;
+                double pj = exp(s[j] - m) / l;
+                for (int r = 0; r < kv_rank; ++r) {
+                    o[r] += pj * (double)c[r];
+                    if (fabs((double)c[r]) > ca[r])
+                        ca[r] = fabs((double)c[r]);
+                }
+            }
+        }
+    free(s);
 }

@@ -14,6 +14,11 @@ Generators taken from the memra-engine 0.125.0 source pages, kept bit-exact:
 * ``lcg_blk_grid`` -- gemv_e4m3_bench.rs, ``synth_blk_grid`` (2^(-6 + (s>>20) % 5)).
 * ``lcg_q8_0`` -- gemv_e4m3_bench.rs, ``synth_q8_0`` (fixed f16 scale 0x1400, qs = s>>24).
 
+* ``mla_randf`` / ``mla_randidx`` -- mla_decode_arm_gate.rs, ``randf`` / ``randidx`` (64-bit LCG with
+  Knuth's MMIX constants from ``seed | 1``; ``randf`` maps ``(s >> 33) as u32 as f32`` by dividing by
+  ``u32::MAX as f32 / 2`` and subtracting 1 in f32 -- (s >> 33) has 31 bits, so the values lie in
+  [-1, 0); ``randidx`` is ``(s >> 33) % max``).
+
 For sizes where a sequential generator is too slow in Python, and for the distributions the
 workload descriptions give without naming a generator, a counter-based SplitMix64
 (Steele, Lea & Flood, "Fast splittable pseudorandom number generators", OOPSLA 2014; the
@@ -175,3 +180,48 @@ def activation_rows(ncols: int, rows: int, page_streams: bool = True, seed_x: in
         x = uniform_pm4(seed_x ^ ncols, rows * ncols).reshape(rows, ncols)
         w = uniform_pm4(seed_w ^ ncols, ncols)
     return x, w
+
+
+# ------------------------------------------------------------------------------------------
+# mla_decode_arm_gate.rs generators (64-bit LCG, MMIX constants), bit-exact, vectorised by
+# jump-ahead like _lcg_states.
+# ------------------------------------------------------------------------------------------
+_MMIX_A = 6364136223846793005
+_MMIX_C = 1442695040888963407
+
+
+def _mmix_states(seed: int, n: int) -> np.ndarray:
+    """States s_1..s_n of s <- s*A + C (mod 2^64) from s_0 = seed | 1."""
+    blk = min(n, 1 << 14)
+    first = np.empty(blk, np.uint64)
+    s = (seed | 1) & MASK64
+    for k in range(blk):
+        s = (s * _MMIX_A + _MMIX_C) & MASK64
+        first[k] = s
+    if blk == n:
+        return first
+    A, C = 1, 0
+    for _ in range(blk):
+        A, C = (A * _MMIX_A) & MASK64, (C * _MMIX_A + _MMIX_C) & MASK64
+    out = np.empty(n, np.uint64)
+    cur = first
+    pos = 0
+    with np.errstate(over="ignore"):
+        while pos < n:
+            take = min(blk, n - pos)
+            out[pos:pos + take] = cur[:take]
+            pos += take
+            cur = cur * np.uint64(A) + np.uint64(C)
+    return out
+
+
+def mla_randf(n: int, seed: int) -> np.ndarray:
+    """mla_decode_arm_gate.rs ``randf(n, seed)``: f32 in [-1, 0)."""
+    hi = (_mmix_states(seed, n) >> np.uint64(33)).astype(np.uint32)
+    return hi.astype(np.float32) / np.float32(np.float32(4294967295.0) / np.float32(2.0)) - np.float32(1.0)
+
+
+def mla_randidx(n: int, seed: int, max_excl: int) -> np.ndarray:
+    """mla_decode_arm_gate.rs ``randidx(n, seed, max_excl)``: int32 in [0, max_excl)."""
+    hi = (_mmix_states(seed, n) >> np.uint64(33)).astype(np.uint32)
+    return (hi % np.uint32(max_excl)).astype(np.int32)

@@ -51,10 +51,16 @@ MUTATIONS = {
                              "(float)memq_oracle_e4m3(w[r * in_f + i]);"),
     "repack_f16_byte_order": ("blk[0] = (uint8_t)(h & 0xFF);\n            blk[1] = (uint8_t)(h >> 8);",
                               "blk[1] = (uint8_t)(h & 0xFF);\n            blk[0] = (uint8_t)(h >> 8);"),
+    "mla_gemv_transposed": ("const float *wr = w + ((int64_t)h * rows + i) * cols;\n                for (int k = 0; k < cols; ++k) {\n                    double p = (double)xr[k] * (double)wr[k];",
+                            "const float *wr = w + ((int64_t)h * rows) * cols;\n                for (int k = 0; k < cols; ++k) {\n                    double p = (double)xr[k] * (double)wr[(int64_t)k * rows % (rows * cols) + i % cols];"),
+    "mla_softmax_no_shift": ("l += exp(s[j] - m);", "l += exp(s[j]);"),
+    "mla_scale_dropped": ("s[j] = (double)scale * dot;", "s[j] = dot;"),
+    "mla_gather_index": ("const float *c = cache + (int64_t)idx[(int64_t)tt * n_slots + j] * row;\n                double dot",
+                         "const float *c = cache + (int64_t)idx[j] * row;\n                double dot"),
 }
 
 PIN_TESTS = ["tests/test_oracle_decode.py", "tests/test_oracle_producer.py",
-             "tests/test_oracle_gemv.py", "tests/test_oracle_next.py"]
+             "tests/test_oracle_gemv.py", "tests/test_oracle_next.py", "tests/test_oracle_mla.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
