@@ -50,6 +50,8 @@ WORKLOADS = {
 }
 DEFAULT_WORKLOAD = "q8_0_4096x4096_m1"
 L2_BYTES = 129 * 2 ** 20
+# f32 FMA peak of the CUDA cores: 152 SMs x 128 FMA / clock x 2 FLOP x 2.07 GHz (maximum clock)
+F32_FMA_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 2)
 
 
 def parse_workload(name: str):
@@ -466,6 +468,8 @@ def run_ours(args, world, rank, local):
         return run_other(args, world, rank, local, dev)
     if args.workload == "c3":
         return run_c3(args, world, rank, local, dev)
+    if args.workload.startswith("mla_"):
+        return run_mla(args, world, rank, local, dev)
     kind, out_f, in_f, m, copies = parse_workload(args.workload)
     fused = args.step == "fused"
     wl = DecodeStep(kind, out_f, in_f, m, copies, dev, fused=fused)
@@ -662,6 +666,102 @@ def run_c3(args, world, rank, local, dev, out_f=17408, in_f=5120, rounds=15):
             "byte_ratio": round(arms["q8_0"].gemv_bytes / arms["e4m3"].gemv_bytes, 4),
             "peak": {"hbm_gbs": peak, "source": peak_kind},
             "gpu_launches": rounds * sum(n.values()), "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+class MlaStep:
+    """One MLA decode attention kernel at the geometry of mla_decode_arm_gate.rs: 64 heads,
+    kv_rank 512, d_nope = d_v = 256, d_rope 0, 2048 gathered slots from a pool of kv rows."""
+
+    def __init__(self, kernel, t, kv, device, split=0):
+        import torch
+        import quantized_decode_memq_gb300 as memq
+        from quantized_decode_memq_gb300 import synth
+        self.memq, self.kernel, self.t, self.split = memq, kernel, t, split
+        nh, kvr = synth.MLA_NH, synth.MLA_KV_RANK
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        if kernel == "attn":
+            q_lat, _, cache, idx = synth.mla_attn_inputs(t, kv)
+            self.args = (dev(q_lat), None, dev(cache), dev(idx), synth.MLA_SCALE)
+            n_slots = idx.shape[1]
+            self.out = torch.empty((t, nh, kvr), dtype=torch.float32, device=device)
+            # gathered rows once per query row, the queries, the indices, the output
+            self.step_bytes = t * n_slots * kvr * 4 + q_lat.nbytes + idx.nbytes + self.out.numel() * 4
+            self.flops = t * nh * n_slots * (2 * kvr + 2 * kvr)
+        else:
+            x, w = (synth.mla_absorb_inputs(t) if kernel == "absorb"
+                    else synth.mla_decompress_inputs(t))
+            self.args = (dev(x), dev(w))
+            self.out = torch.empty((t, nh, w.shape[1]), dtype=torch.float32, device=device)
+            self.step_bytes = w.nbytes + x.nbytes + self.out.numel() * 4
+            self.flops = 2 * t * w.size
+        self.scrub = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=device)
+        self.launches_per_step = 1
+
+    def step(self, i):
+        fn = {"attn": self.memq.memq_mla_attn_gathered, "absorb": self.memq.memq_mla_absorb_q,
+              "decompress": self.memq.memq_mla_decompress_v}[self.kernel]
+        fn(*self.args, out=self.out, split=self.split)
+
+
+def run_mla(args, world, rank, local, dev):
+    """mla_<absorb|decompress>_t<t> and mla_attn_t<t>_kv<kv>: each timed launch follows a 256 MB
+    L2 scrub (outside the events), as the page times its kernels from the cold L2 that the
+    expert stream between two MLA layers leaves."""
+    import torch
+    from quantized_decode_memq_gb300 import build
+    build.build()
+    parts = args.workload.split("_")
+    kernel, t = parts[1], int(parts[2][1:])
+    kv = int(parts[3][2:]) if kernel == "attn" else 0
+    wl = MlaStep(kernel, t, kv, dev, split=args.split)
+    stream = torch.cuda.Stream(device=dev)
+    K, W = min(args.steps, 400), min(args.warmup, 50)  # one scrub + one launch per sample
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            wl.scrub.zero_()
+            wl.step(i)
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            wl.scrub.zero_()
+            evs[i][0].record(stream)
+            wl.step(i)
+            evs[i][1].record(stream)
+    stream.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    per = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    t_launch, _ = aggregate(float(np.mean(per)), 1.0)
+    if kernel == "attn":
+        achieved = wl.flops / t_launch / 1e12
+        peak = F32_FMA_TFLOPS
+        roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": "derived: 152 SMs x 128 f32 FMA/clk x 2 FLOP x 2.07 GHz"}
+    else:
+        peak, peak_kind = measured_peak_hbm()
+        achieved = wl.step_bytes / t_launch / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind}
+    desc = {"absorb": f"mla_absorb_q t={t}: 64 heads x (512 x 256) f32 weights",
+            "decompress": f"mla_decompress_v t={t}: 64 heads x (256 x 512) f32 weights",
+            "attn": f"mla_attn_gathered t={t}: 64 heads, kv_rank 512, 2048 slots from {kv} rows"}
+    line = {"metric": "MLA decode kernel time per launch (L2 scrubbed before each)",
+            "value": round(t_launch * 1e6, 3), "unit": "us", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": t_launch * 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": desc[kernel], "split": args.split or "auto",
+                       "step_bytes": wl.step_bytes, "flops": wl.flops,
+                       "timing": "one launch per sample after a 256 MB scrub, CUDA events",
+                       "min_us": round(min(per) * 1e6, 3)},
+            "roofline": roof, "gpu_launches": K, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -926,7 +1026,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    help="one of %s, or <e4m3|blk128|q8_0>_<out_f>x<in_f>_m<m>" % sorted(WORKLOADS))
+                    help="one of %s, or <e4m3|blk128|q8_0>_<out_f>x<in_f>_m<m>, c3, "
+                         "producer_<ncols>x<rows>, silu_<ncols>x<rows>, "
+                         "repack_<e4m3|blk128>_<out_f>x<in_f>, stack<layers>, "
+                         "mla_<absorb|decompress>_t<t>, mla_attn_t<t>_kv<kv>" % sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -936,6 +1039,8 @@ def main(argv=None):
                     help="decode step as one fused launch or as producer + GEMV launches; "
                          "for the stack, 'group' runs the GEMVs that share an activation as one "
                          "grouped launch")
+    ap.add_argument("--split", type=int, default=0,
+                    help="MLA workloads: the kernels' split (0 = the library's choice)")
     ap.add_argument("--ncu-launches", type=int, default=0,
                     help="profiling entry: run one producer and N GEMV launches, no timing")
     args = ap.parse_args(argv)

@@ -145,7 +145,6 @@ int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps, cons
                                 int8_t *qs, float *d, float *z, float *y, int64_t out_f,
                                 int64_t in_f, int m, void *stream);
 
-/* Human-readable name of a memq_status value (static storage; never NULL). */
 /*
  * memq_gemv_*_group -- up to 4 GEMVs of the same container that share one activation (qs, d,
  * in_f, m), e.g. the gate and up projections, or q and k/v, in ONE launch: the matrices' rows
@@ -205,6 +204,45 @@ int memq_repack_e4m3_q8_0(const uint8_t *w, const float *w_scale, void *out, int
 int memq_repack_e4m3_blk128_q8_0(const uint8_t *w, const float *grid, void *out, int64_t out_f,
                                  int64_t in_f, void *stream);
 
+/*
+ * The t <= 8 MLA decode attention kernels of mla_decode_arm_gate.rs (module doc and `main`: 64
+ * heads, kv_rank 512, d_nope = d_v = 256, d_rope 0, a top-k gather of 2048 rows from a pool of
+ * cached latent rows, t_q in {1, 2, 4, 8}).  All f32, row-major, with t in [1, 8] query rows
+ * (MEMQ_ERR_M_RANGE otherwise).  `split` is launch geometry only (0 = the library's choice):
+ * for absorb_q / decompress_v, s >= 1 CTAs share the rows of one head; for attn_gathered,
+ * s in {1, 2, 4, 8} puts 8 / s heads in each CTA.  For every split the outputs are
+ * bit-identical (each output element is produced by the same floating-point operations in the
+ * same order), which is the "split twin" property the page gates on.
+ *
+ * memq_mla_absorb_q:     out[t][h][r] = sum_{d < d_nope} q_nope[t][h][d] * wk_b[h][r][d]
+ *   q_nope device [t][nh][d_nope], 16-byte aligned;  wk_b device [nh][kv_rank][d_nope],
+ *   16-byte aligned;  out device [t][nh][kv_rank], 4-byte aligned.
+ * memq_mla_decompress_v: out[t][h][v] = sum_{r < kv_rank} o_lat[t][h][r] * wv_b[h][v][r]
+ *   o_lat device [t][nh][kv_rank], 16-byte aligned;  wv_b device [nh][d_v][kv_rank], 16-byte
+ *   aligned;  out device [t][nh][d_v], 4-byte aligned.
+ * The reduced dimension (d_nope, resp. kv_rank) must be 128, 256, 512 or 1024; the other >= 1;
+ * 1 <= nh <= 65536.
+ *
+ * memq_mla_attn_gathered: for each query row t and head h, over the gathered slots j < n_slots
+ * with c_j = cache[idx[t][j]] (kv_rank latent floats, then d_rope rope floats):
+ *     s_j = scale * (q_lat[t][h] . c_j[:kv_rank] + q_pe[t][h] . c_j[kv_rank:])
+ *     out[t][h][:] = sum_j softmax(s)_j * c_j[:kv_rank]
+ *   q_lat device [t][nh][kv_rank];  q_pe device [t][nh][d_rope] (may be NULL when d_rope == 0)
+ *   cache device [pool][kv_rank + d_rope], 16-byte aligned;  idx device int32 [t][n_slots],
+ *   each in [0, pool) (not checked: an index outside the pool is outside the contract)
+ *   out device [t][nh][kv_rank];  q_lat, q_pe, idx, out 4-byte aligned
+ *   kv_rank in {128, 256, 512, 1024};  0 <= d_rope <= 128;  n_slots >= 1;  scale finite.
+ * Errors: MEMQ_ERR_SHAPE, MEMQ_ERR_NULL, MEMQ_ERR_ALIGN, MEMQ_ERR_M_RANGE, MEMQ_ERR_LAUNCH.
+ */
+int memq_mla_absorb_q(const float *q_nope, const float *wk_b, float *out, int t, int nh,
+                      int d_nope, int kv_rank, int split, void *stream);
+int memq_mla_decompress_v(const float *o_lat, const float *wv_b, float *out, int t, int nh,
+                          int d_v, int kv_rank, int split, void *stream);
+int memq_mla_attn_gathered(const float *q_lat, const float *q_pe, const float *cache,
+                           const int32_t *idx, float *out, int nh, int kv_rank, int d_rope, int t,
+                           int n_slots, float scale, int split, void *stream);
+
+/* Human-readable name of a memq_status value (static storage; never NULL). */
 const char *memq_status_string(int status);
 
 /*

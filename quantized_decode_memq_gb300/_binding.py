@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
             L.memq_silu_mul_q8_1.argtypes = [P, P, P, P, P, I64, I64, P]
             L.memq_repack_e4m3_q8_0.argtypes = [P, P, P, I64, I64, P]
             L.memq_repack_e4m3_blk128_q8_0.argtypes = [P, P, P, I64, I64, P]
+            L.memq_mla_absorb_q.argtypes = [P, P, P, I32, I32, I32, I32, I32, P]
+            L.memq_mla_decompress_v.argtypes = [P, P, P, I32, I32, I32, I32, I32, P]
+            L.memq_mla_attn_gathered.argtypes = [P, P, P, P, P, I32, I32, I32, I32, I32,
+                                                 ctypes.c_float, I32, P]
             L.memq_device_fault.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             L.memq_status_string.argtypes = [I32]
             L.memq_status_string.restype = ctypes.c_char_p
@@ -401,3 +405,68 @@ def _group_q8(ws, qs, d, in_f, ys, stream):
                                     _ptr(qs2), _ptr(d2), in_f, m, _stream(stream))
     _check("memq_gemv_q8_0_group", rc)
     return outs
+
+
+def _head_gemv(fn: str, x, w, out, split, stream):
+    _cuda("x", x, torch.float32)
+    _cuda("w", w, torch.float32)
+    if x.dim() != 3 or w.dim() != 3:
+        raise ValueError(f"{fn}: x must be [t, nh, k] and w [nh, n, k]")
+    t, nh, k = x.shape
+    n = w.shape[1]
+    if tuple(w.shape) != (nh, n, k):
+        raise ValueError(f"{fn}: w has shape {tuple(w.shape)}, expected ({nh}, n, {k})")
+    if out is None:
+        out = torch.empty((t, nh, n), dtype=torch.float32, device=x.device)
+    _cuda("out", out, torch.float32, (t, nh, n))
+    # absorb_q takes (d_nope, kv_rank) = (k, n); decompress_v takes (d_v, kv_rank) = (n, k)
+    dims = (k, n) if fn == "memq_mla_absorb_q" else (n, k)
+    rc = getattr(lib(), fn)(_ptr(x), _ptr(w), _ptr(out), t, nh, *dims, split, _stream(stream))
+    _check(fn, rc)
+    return out
+
+
+def memq_mla_absorb_q(q_nope: torch.Tensor, wk_b: torch.Tensor, *, out=None, split: int = 0,
+                      stream=None):
+    """out[t, h, r] = sum_d q_nope[t, h, d] * wk_b[h, r, d].  q_nope f32 [t, nh, d_nope],
+    wk_b f32 [nh, kv_rank, d_nope] -> f32 [t, nh, kv_rank]."""
+    return _head_gemv("memq_mla_absorb_q", q_nope, wk_b, out, split, stream)
+
+
+def memq_mla_decompress_v(o_lat: torch.Tensor, wv_b: torch.Tensor, *, out=None, split: int = 0,
+                          stream=None):
+    """out[t, h, v] = sum_r o_lat[t, h, r] * wv_b[h, v, r].  o_lat f32 [t, nh, kv_rank],
+    wv_b f32 [nh, d_v, kv_rank] -> f32 [t, nh, d_v]."""
+    return _head_gemv("memq_mla_decompress_v", o_lat, wv_b, out, split, stream)
+
+
+def memq_mla_attn_gathered(q_lat: torch.Tensor, q_pe, cache: torch.Tensor, idx: torch.Tensor,
+                           scale: float, *, out=None, split: int = 0, stream=None):
+    """Softmax attention of each (t, h) query over its gathered cache rows.
+
+    q_lat f32 [t, nh, kv_rank]; q_pe f32 [t, nh, d_rope] or None (d_rope 0);
+    cache f32 [pool, kv_rank + d_rope]; idx int32 [t, n_slots] -> f32 [t, nh, kv_rank]."""
+    _cuda("q_lat", q_lat, torch.float32)
+    if q_lat.dim() != 3:
+        raise ValueError("memq_mla_attn_gathered: q_lat must be [t, nh, kv_rank]")
+    t, nh, kv_rank = q_lat.shape
+    _cuda("cache", cache, torch.float32)
+    if cache.dim() != 2:
+        raise ValueError("memq_mla_attn_gathered: cache must be [pool, kv_rank + d_rope]")
+    d_rope = cache.shape[1] - kv_rank
+    if q_pe is not None:
+        _cuda("q_pe", q_pe, torch.float32, (t, nh, d_rope))
+    elif d_rope != 0:
+        raise ValueError("memq_mla_attn_gathered: q_pe is required when d_rope > 0")
+    _cuda("idx", idx, torch.int32)
+    if idx.dim() != 2 or idx.shape[0] != t:
+        raise ValueError(f"memq_mla_attn_gathered: idx must be [{t}, n_slots]")
+    n_slots = idx.shape[1]
+    if out is None:
+        out = torch.empty((t, nh, kv_rank), dtype=torch.float32, device=q_lat.device)
+    _cuda("out", out, torch.float32, (t, nh, kv_rank))
+    rc = lib().memq_mla_attn_gathered(_ptr(q_lat), _ptr(q_pe), _ptr(cache), _ptr(idx), _ptr(out),
+                                      nh, kv_rank, d_rope, t, n_slots, float(scale), split,
+                                      _stream(stream))
+    _check("memq_mla_attn_gathered", rc)
+    return out

@@ -225,3 +225,42 @@ def mla_randidx(n: int, seed: int, max_excl: int) -> np.ndarray:
     """mla_decode_arm_gate.rs ``randidx(n, seed, max_excl)``: int32 in [0, max_excl)."""
     hi = (_mmix_states(seed, n) >> np.uint64(33)).astype(np.uint32)
     return (hi % np.uint32(max_excl)).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------------------------
+# MLA decode attention inputs, as mla_decode_arm_gate.rs (`main`) draws them: every array from
+# randf with the page's per-array seed xor'd with t (and with the pool depth kv for the cache
+# and the gather indices); n_slots = min(2048, kv).
+# ---------------------------------------------------------------------------------------------
+MLA_NH, MLA_KV_RANK, MLA_D_NOPE, MLA_D_V, MLA_N_SLOTS = 64, 512, 256, 256, 2048
+MLA_SCALE = float(np.float32(1.0) / np.float32(23.323808))
+
+
+def mla_absorb_inputs(t: int, nh: int = MLA_NH, kv_rank: int = MLA_KV_RANK,
+                      d_nope: int = MLA_D_NOPE):
+    """(q_nope f32 [t, nh, d_nope], wk_b f32 [nh, kv_rank, d_nope])."""
+    q = mla_randf(t * nh * d_nope, 0xB2000001 ^ t).reshape(t, nh, d_nope)
+    w = mla_randf(nh * kv_rank * d_nope, 0xB2000002 ^ t).reshape(nh, kv_rank, d_nope)
+    return q, w
+
+
+def mla_decompress_inputs(t: int, nh: int = MLA_NH, kv_rank: int = MLA_KV_RANK,
+                          d_v: int = MLA_D_V):
+    """(o_lat f32 [t, nh, kv_rank], wv_b f32 [nh, d_v, kv_rank])."""
+    o = mla_randf(t * nh * kv_rank, 0xB2000003 ^ t).reshape(t, nh, kv_rank)
+    w = mla_randf(nh * d_v * kv_rank, 0xB2000004 ^ t).reshape(nh, d_v, kv_rank)
+    return o, w
+
+
+def mla_attn_inputs(t: int, kv: int, nh: int = MLA_NH, kv_rank: int = MLA_KV_RANK,
+                    d_rope: int = 0, n_slots: int | None = None):
+    """(q_lat [t, nh, kv_rank], q_pe [t, nh, d_rope] or None, cache [kv, kv_rank + d_rope],
+    idx int32 [t, n_slots]); n_slots defaults to min(2048, kv)."""
+    if n_slots is None:
+        n_slots = min(MLA_N_SLOTS, kv)
+    q_lat = mla_randf(t * nh * kv_rank, 0xB2000005 ^ t).reshape(t, nh, kv_rank)
+    q_pe = (mla_randf(t * nh * d_rope, 0xB2000006 ^ t).reshape(t, nh, d_rope)
+            if d_rope else None)
+    cache = mla_randf(kv * (kv_rank + d_rope), 0xB2000007 ^ kv).reshape(kv, kv_rank + d_rope)
+    idx = mla_randidx(t * n_slots, 0xB2000008 ^ t ^ kv, kv).reshape(t, n_slots)
+    return q_lat, q_pe, cache, idx

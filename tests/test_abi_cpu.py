@@ -38,7 +38,8 @@ def test_header_declares_the_boundary():
                      "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
                      "memq_gemv_e4m3_group", "memq_gemv_e4m3_blk128_group",
                      "memq_gemv_q8_0_group", "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
-                     "memq_repack_e4m3_blk128_q8_0",
+                     "memq_repack_e4m3_blk128_q8_0", "memq_mla_absorb_q",
+                     "memq_mla_decompress_v", "memq_mla_attn_gathered",
                      "memq_status_string", "memq_device_fault", "memq_version"):
         assert required in names
 
@@ -98,6 +99,29 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.memq_repack_e4m3_blk128_q8_0(fake, None, fake, 4, 64, None) == m.Status.ERR_NULL
     assert lib.memq_repack_e4m3_q8_0(fake, fake, P(0x1002), 4, 64, None) == m.Status.ERR_ALIGN
     assert lib.memq_repack_e4m3_q8_0(None, None, None, 0, 64, None) == m.Status.OK
+    # MLA decode attention kernels: (.., t, nh, d_nope | d_v, kv_rank, split, stream)
+    assert lib.memq_mla_absorb_q(fake, fake, fake, 0, 64, 256, 512, 0, None) == m.Status.ERR_M_RANGE
+    assert lib.memq_mla_absorb_q(fake, fake, fake, 9, 64, 256, 512, 0, None) == m.Status.ERR_M_RANGE
+    assert lib.memq_mla_absorb_q(fake, fake, fake, 1, 64, 200, 512, 0, None) == m.Status.ERR_SHAPE
+    assert lib.memq_mla_absorb_q(fake, fake, fake, 1, 64, 2048, 512, 0, None) == m.Status.ERR_SHAPE
+    assert lib.memq_mla_absorb_q(fake, fake, fake, 1, 64, 256, 512, -1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_mla_absorb_q(fake, None, fake, 1, 64, 256, 512, 0, None) == m.Status.ERR_NULL
+    assert lib.memq_mla_absorb_q(P(0x1004), fake, fake, 1, 64, 256, 512, 0, None) == m.Status.ERR_ALIGN
+    assert lib.memq_mla_decompress_v(fake, fake, fake, 1, 64, 256, 500, 0, None) == m.Status.ERR_SHAPE
+    assert lib.memq_mla_decompress_v(fake, fake, fake, 1, 0, 256, 512, 0, None) == m.Status.ERR_SHAPE
+    assert lib.memq_mla_decompress_v(fake, fake, P(0x1002), 1, 64, 256, 512, 0, None) == m.Status.ERR_ALIGN
+    #   (q_lat, q_pe, cache, idx, out, nh, kv_rank, d_rope, t, n_slots, scale, split, stream)
+    attn = lib.memq_mla_attn_gathered
+    assert attn(fake, None, fake, fake, fake, 64, 512, 0, 9, 2048, 0.04, 0, None) == m.Status.ERR_M_RANGE
+    assert attn(fake, None, fake, fake, fake, 64, 512, 0, 1, 0, 0.04, 0, None) == m.Status.ERR_SHAPE
+    assert attn(fake, None, fake, fake, fake, 64, 384 + 1, 0, 1, 16, 0.04, 0, None) == m.Status.ERR_SHAPE
+    assert attn(fake, fake, fake, fake, fake, 64, 512, 129, 1, 16, 0.04, 0, None) == m.Status.ERR_SHAPE
+    assert attn(fake, None, fake, fake, fake, 64, 512, 0, 1, 16, 0.04, 3, None) == m.Status.ERR_SHAPE
+    assert attn(fake, None, fake, fake, fake, 64, 512, 0, 1, 16, float("inf"), 0, None) == m.Status.ERR_SHAPE
+    assert attn(fake, None, fake, fake, fake, 64, 512, 64, 1, 16, 0.04, 0, None) == m.Status.ERR_NULL
+    assert attn(fake, None, fake, None, fake, 64, 512, 0, 1, 16, 0.04, 0, None) == m.Status.ERR_NULL
+    assert attn(fake, None, P(0x1004), fake, fake, 64, 512, 0, 1, 16, 0.04, 0, None) == m.Status.ERR_ALIGN
+    assert attn(fake, None, fake, P(0x1002), fake, 64, 512, 0, 1, 16, 0.04, 0, None) == m.Status.ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
