@@ -696,8 +696,15 @@ class MlaStep:
             self.out = torch.empty((t, nh, w.shape[1]), dtype=torch.float32, device=device)
             self.step_bytes = w.nbytes + x.nbytes + self.out.numel() * 4
             self.flops = 2 * t * w.size
-        self.scrub = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=device)
+        # L2 scrub: 256 MB READ through the SMs (a written scrub would leave L2 full of dirty
+        # lines whose write-back the timed kernel would pay for)
+        self.scrub = torch.ones(256 * 2 ** 20 // 4, dtype=torch.float32, device=device)
+        self.scrub_out = torch.empty((), dtype=torch.float32, device=device)
         self.launches_per_step = 1
+
+    def flush(self):
+        import torch
+        torch.sum(self.scrub, dim=0, out=self.scrub_out)
 
     def step(self, i):
         fn = {"attn": self.memq.memq_mla_attn_gathered, "absorb": self.memq.memq_mla_absorb_q,
@@ -707,7 +714,7 @@ class MlaStep:
 
 def run_mla(args, world, rank, local, dev):
     """mla_<absorb|decompress>_t<t> and mla_attn_t<t>_kv<kv>: each timed launch follows a 256 MB
-    L2 scrub (outside the events), as the page times its kernels from the cold L2 that the
+    L2 scrub read (outside the events), as the page times its kernels from the cold L2 that the
     expert stream between two MLA layers leaves."""
     import torch
     from quantized_decode_memq_gb300 import build
@@ -722,7 +729,7 @@ def run_mla(args, world, rank, local, dev):
            for _ in range(K)]
     with torch.cuda.stream(stream):
         for i in range(W):
-            wl.scrub.zero_()
+            wl.flush()
             wl.step(i)
     stream.synchronize()
     sampler = ClockSampler(local)
@@ -730,7 +737,7 @@ def run_mla(args, world, rank, local, dev):
     barrier()
     with torch.cuda.stream(stream):
         for i in range(K):
-            wl.scrub.zero_()
+            wl.flush()
             evs[i][0].record(stream)
             wl.step(i)
             evs[i][1].record(stream)
@@ -759,7 +766,7 @@ def run_mla(args, world, rank, local, dev):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": desc[kernel], "split": args.split or "auto",
                        "step_bytes": wl.step_bytes, "flops": wl.flops,
-                       "timing": "one launch per sample after a 256 MB scrub, CUDA events",
+                       "timing": "one launch per sample after a 256 MB scrub read, CUDA events",
                        "min_us": round(min(per) * 1e6, 3)},
             "roofline": roof, "gpu_launches": K, "clocks": clocks}
     if rank == 0:

@@ -249,7 +249,10 @@ const char *memq_status_string(int status);
  * memq_device_fault -- read and clear the current device's fault word.
  * Synchronizes `stream`, then stores the word in *fault_out (0 = no fault) and resets it.
  * Bit 0: a GEMV consumer's bounded wait on a shared-memory barrier expired; bit 1: the GEMV
- * producer's.  The kernel that gave up wrote nothing more and returned.
+ * producer's.  The kernel that gave up wrote nothing more and returned.  Bit 2: an
+ * memq_mla_attn_gathered CTA's bounded wait for its gathered rows expired; bit 3: the same in
+ * memq_mla_absorb_q / memq_mla_decompress_v.  That CTA stopped streaming, waited (bounded) for
+ * its copies in flight and returned; the call's outputs are invalid.
  * Returns MEMQ_ERR_NULL for a NULL fault_out, MEMQ_ERR_DEVICE if the copy fails.
  */
 int memq_device_fault(void *stream, uint32_t *fault_out);

@@ -7,15 +7,16 @@
 int memq_internal_fault_e4m3(unsigned int *out, bool clear);
 int memq_internal_fault_blk128(unsigned int *out, bool clear);
 int memq_internal_fault_q8_0(unsigned int *out, bool clear);
+int memq_internal_fault_mla(unsigned int *out, bool clear);
 
 extern "C" int memq_device_fault(void *stream, uint32_t *fault_out) {
     if (!fault_out) return MEMQ_ERR_NULL;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MEMQ_ERR_DEVICE;
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, e = 0;
     if (memq_internal_fault_e4m3(&a, true) || memq_internal_fault_blk128(&b, true) ||
-        memq_internal_fault_q8_0(&c, true))
+        memq_internal_fault_q8_0(&c, true) || memq_internal_fault_mla(&e, true))
         return MEMQ_ERR_DEVICE;
-    *fault_out = a | b | c;
+    *fault_out = a | b | c | e;
     return MEMQ_OK;
 }
 

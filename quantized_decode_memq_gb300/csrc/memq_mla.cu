@@ -10,23 +10,32 @@
 //   attn_gathered out[t][h][:] = softmax_j(scale * (q_lat[t][h] . c_j + q_pe[t][h] . c_j,rope)) . c_j
 //                 over the gathered rows c_j = cache[idx[t][j]]
 //
+// Every dot product here has the same shape: lane l of a warp sums, in order, the products of
+// its float4s (float4 index l + 32 c, c ascending; components x, y, z, w), then the 32 lane
+// partials are added along the xor tree of offsets 16, 8, 4, 2, 1.  xor_reduce_scatter() runs
+// that tree for many dots at once with fewer shuffles and the same bits, so how dots are
+// batched (which the split and the head grouping change) never changes a result.
+//
 // head_gemv_kernel (absorb_q, decompress_v): a per-head batched GEMV over f32 weights (33.5 MB
 // at the page geometry, read once: HBM-bound).  CTA (h, part) takes rows [part*rows/split,
-// (part+1)*rows/split) of head h; a warp streams whole weight rows as float4s (two rows at a
-// time), the t activation rows of head h sit in shared memory.  A row's sum is the lane's
-// float4s in increasing order, then a fixed xor-shuffle tree: the same operations for every
-// split, so the split twins are bit-identical by construction.
+// (part+1)*rows/split) of head h, contiguous in memory; a producer warp streams them into a
+// shared-memory ring by bulk copies while 8 consumer warps take 2 rows of each stage against
+// the t activation rows of head h (in shared memory).  The default split fills one wave of
+// resident CTAs.
 //
 // attn_gathered_kernel: every head of query row t gathers the same n_slots rows, so a CTA
 // serves a group of H heads from one staged copy of them, and a cluster of 8 CTAs splits the
-// slots into 8 fixed ranges.  Each CTA runs an online softmax over its range (running max m,
-// sum l, outputs rescaled by exp(m_old - m_new) per staged chunk of 16 rows); the 8 partials
-// are merged through distributed shared memory in part order.  The slot ranges, chunks and
-// merge order do not depend on H, which is the entry point's `split` (H = 8 / split), so the
-// split twins are bit-identical.  No global scratch: the partials live in shared memory.
+// slots into 8 fixed ranges.  The gathered rows stream into a ring of shared-memory stages by
+// bulk copies (one per row, completing on an mbarrier per stage), issued S - 1 chunks ahead of
+// the compute.  Each CTA runs an online softmax over its range (running max m, sum l, outputs
+// rescaled by exp(m_old - m_new) per chunk of 16 rows); the 8 partials are merged through
+// distributed shared memory in part order.  The slot ranges, chunks and merge order do not
+// depend on H, which is the entry point's `split` (H = 8 / split), so the split twins are
+// bit-identical.  No global scratch: the partials live in shared memory.
 //
 // Plain stream-ordered launches (no programmatic dependent launch): every input is complete
 // when a kernel starts.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -36,66 +45,171 @@
 namespace memq {
 namespace {
 
+// Device fault word of this translation unit: bit 2 = an attention kernel's bounded wait for
+// its gathered rows expired (the kernel then stops streaming, finishes its barriers and
+// returns); bit 3 = the same in absorb_q / decompress_v.
+__device__ unsigned int g_mla_fault = 0;
+constexpr unsigned int kFaultAttnWait = 4u;
+
 constexpr int kMlaThreads = 256;
 constexpr int kMlaWarps = kMlaThreads / 32;
 constexpr int kMaxT = 8;
 constexpr int kMaxHeads = 1 << 16;
 constexpr int64_t kMaxGrid = (int64_t{1} << 31) - 1;
-constexpr int kMaxRope = 128;  // with kv_rank <= 1024: at most 152 KB of shared memory
+constexpr int kMaxRope = 128;  // with kv_rank <= 1024 the attention kernel fits shared memory
+
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+
+// Sums v[e] over the 32 lanes for every e < NV (a power of two <= 32) along the xor tree of
+// offsets 16, 8, 4, 2, 1, each step adding the partner's partial to one's own -- the tree of
+// warp_sum, so each sum is bit-identical to warp_sum of that element.  At the step of offset o a
+// lane sends the half of its remaining elements that its partner keeps (lanes with bit o set
+// keep the upper half), so NV sums take NV - 1 + 5 - log2(NV) shuffles instead of 5 NV.
+// On return lane l holds, in v[0], the sum of element l >> (5 - log2 NV).
+template <int NV>
+__device__ __forceinline__ float xor_reduce_scatter(float (&v)[NV], int lane) {
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const int off = 16 >> s;
+        const int n = NV >> s;  // elements this lane still holds
+        if (n > 1) {
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < n / 2; ++i) {
+                const float send = upper ? v[i] : v[i + n / 2];
+                const float keep = upper ? v[i + n / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(kFullMask, send, off);
+            }
+        } else {
+            v[0] += __shfl_xor_sync(kFullMask, v[0], off);
+        }
+    }
+    return v[0];
+}
 
 // ------------------------------------------------------------------------------------------
-// Per-head batched GEMV.  CV = cols / 128 float4s per lane per row (2 or 4 at the page
-// geometry; any cols that is a multiple of 128 up to 1024).
+// Per-head batched GEMV.  CTA (h, part) owns rows [r0, r1) of head h, which are contiguous in
+// memory: a producer warp streams them into a ring of S stages of kHeadRows rows with one bulk
+// copy per stage (full barrier: transaction bytes; empty barrier: one arrival per consumer
+// warp), while the 8 consumer warps take kHeadRB rows of each stage.  CV = cols / 128 float4s
+// per lane per row; T = t rounded up to a power of two (rows of x beyond t are zero in shared
+// memory and their sums are not stored).
 // ------------------------------------------------------------------------------------------
-template <int CV>
-__global__ void __launch_bounds__(kMlaThreads)
-    head_gemv_kernel(const float *__restrict__ x, const float *__restrict__ w,
-                     float *__restrict__ out, int t, int nh, int rows, int split) {
-    extern __shared__ __align__(16) float sx[];  // [t][cols]
+constexpr int kHeadRB = 2;                     // rows per consumer warp per stage
+constexpr int kHeadRows = kMlaWarps * kHeadRB;  // rows per stage
+constexpr int kHeadThreads = kMlaThreads + 32;  // + the producer warp
+constexpr int kHeadMaxStages = 4;
+constexpr unsigned int kFaultHeadWait = 8u;
+
+struct HeadArgs {
+    const float *x, *w;
+    float *out;
+    int t, nh, rows, split, stages;
+};
+
+template <int CV, int T>
+__global__ void __launch_bounds__(kHeadThreads)
+    head_gemv_kernel(const __grid_constant__ HeadArgs a) {
     constexpr int cols = CV * 128;
+    constexpr int NV = kHeadRB * T;
+    constexpr int kLaneShift = 5 - ilog2(NV);  // lane l holds element l >> kLaneShift
+    constexpr uint32_t row_bytes = cols * 4u;
+    extern __shared__ __align__(128) float hsm[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(hsm);  // [kHeadMaxStages]
+    uint64_t *empty = full + kHeadMaxStages;             // [kHeadMaxStages]
+    float *sx = hsm + 4 * kHeadMaxStages + 16;           // [T][cols] (128-byte aligned)
+    float *ring = sx + T * cols;                         // [S][kHeadRows][cols]
+    const int S = a.stages, split = a.split, rows = a.rows, nh = a.nh, t = a.t;
     const int h = blockIdx.x / split;
     const int part = blockIdx.x - h * split;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < t * cols / 4; i += kMlaThreads) {
-        const int tt = i / (cols / 4), k = i - tt * (cols / 4);
-        reinterpret_cast<float4 *>(sx)[i] =
-            __ldg(reinterpret_cast<const float4 *>(x + (static_cast<int64_t>(tt) * nh + h) * cols) + k);
-    }
-    __syncthreads();
     const int r0 = static_cast<int>(static_cast<int64_t>(part) * rows / split);
     const int r1 = static_cast<int>(static_cast<int64_t>(part + 1) * rows / split);
-    const float4 *wh = reinterpret_cast<const float4 *>(w + static_cast<int64_t>(h) * rows * cols);
-    const float4 *sx4 = reinterpret_cast<const float4 *>(sx);
-    for (int i = r0 + 2 * warp; i < r1; i += 2 * kMlaWarps) {
-        const bool two = i + 1 < r1;
-        float4 wa[CV], wb[CV];
-#pragma unroll
-        for (int c = 0; c < CV; ++c) {
-            wa[c] = __ldcs(wh + static_cast<int64_t>(i) * (cols / 4) + lane + 32 * c);
-            wb[c] = two ? __ldcs(wh + static_cast<int64_t>(i + 1) * (cols / 4) + lane + 32 * c)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nst = (r1 - r0 + kHeadRows - 1) / kHeadRows;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kHeadMaxStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kMlaWarps);
         }
-        for (int tt = 0; tt < t; ++tt) {
-            float pa = 0.f, pb = 0.f;
-#pragma unroll
-            for (int c = 0; c < CV; ++c) {
-                const float4 xv = sx4[tt * (cols / 4) + lane + 32 * c];
-                pa = fmaf(xv.x, wa[c].x, pa);
-                pa = fmaf(xv.y, wa[c].y, pa);
-                pa = fmaf(xv.z, wa[c].z, pa);
-                pa = fmaf(xv.w, wa[c].w, pa);
-                pb = fmaf(xv.x, wb[c].x, pb);
-                pb = fmaf(xv.y, wb[c].y, pb);
-                pb = fmaf(xv.z, wb[c].z, pb);
-                pb = fmaf(xv.w, wb[c].w, pb);
-            }
-            pa = warp_sum(pa);
-            pb = warp_sum(pb);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (warp == kMlaWarps) {
+        // Producer: stage st holds rows r0 + st * kHeadRows ...; slot st % S is reused once the
+        // consumers released stage st - S.
+        const uint64_t pol = l2_evict_first_policy();
+        const float *src = a.w + (static_cast<int64_t>(h) * rows + r0) * cols;
+        bool ok = true;
+        int st = 0;
+        for (; st < nst && ok; ++st) {
+            const int slot = st % S;
+            if (st >= S) ok = warp_wait_bounded(&empty[slot], static_cast<uint32_t>((st / S - 1) & 1));
+            if (!ok) break;
+            const int nrs = min(kHeadRows, r1 - r0 - st * kHeadRows);
             if (lane == 0) {
-                out[(static_cast<int64_t>(tt) * nh + h) * rows + i] = pa;
-                if (two) out[(static_cast<int64_t>(tt) * nh + h) * rows + i + 1] = pb;
+                mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nrs) * row_bytes);
+                bulk_g2s(ring + static_cast<int64_t>(slot) * kHeadRows * cols,
+                         src + static_cast<int64_t>(st) * kHeadRows * cols,
+                         static_cast<uint32_t>(nrs) * row_bytes, &full[slot], pol);
+            }
+            __syncwarp();
+        }
+        if (!ok && lane == 0) atomicOr(&g_mla_fault, kFaultHeadWait);
+        // Every copy issued must land before the CTA's shared memory goes away.
+        for (int q = max(0, st - S); q < st; ++q)
+            (void)warp_wait_bounded(&full[q % S], static_cast<uint32_t>((q / S) & 1));
+        return;
+    }
+    // Consumers: x rows of head h into shared memory (overlapping the first weight copies).
+    for (int i = threadIdx.x; i < T * cols / 4; i += kMlaThreads) {
+        const int tt = i / (cols / 4), k = i - tt * (cols / 4);
+        reinterpret_cast<float4 *>(sx)[i] =
+            tt < t ? __ldg(reinterpret_cast<const float4 *>(a.x + (static_cast<int64_t>(tt) * nh + h) * cols) + k)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kMlaThreads) : "memory");
+    const float4 *sx4 = reinterpret_cast<const float4 *>(sx);
+    const int my_e = lane >> kLaneShift;
+    const int my_b = my_e / T, my_t = my_e - my_b * T;
+    const bool writer = (lane & ((1 << kLaneShift) - 1)) == 0;
+    for (int st = 0; st < nst; ++st) {
+        const int slot = st % S;
+        if (!warp_wait_bounded(&full[slot], static_cast<uint32_t>((st / S) & 1))) {
+            if (lane == 0) atomicOr(&g_mla_fault, kFaultHeadWait);
+            break;
+        }
+        const int i = r0 + st * kHeadRows + warp * kHeadRB;  // this warp's first row
+        const float4 *wr = reinterpret_cast<const float4 *>(ring + static_cast<int64_t>(slot) * kHeadRows * cols) +
+                           warp * kHeadRB * (cols / 4);
+        float4 wv[kHeadRB][CV];
+#pragma unroll
+        for (int b = 0; b < kHeadRB; ++b)
+#pragma unroll
+            for (int c = 0; c < CV; ++c) wv[b][c] = wr[b * (cols / 4) + lane + 32 * c];
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[slot])) : "memory");
+        float p[NV];
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) {
+            float4 xv[CV];
+#pragma unroll
+            for (int c = 0; c < CV; ++c) xv[c] = sx4[tt * (cols / 4) + lane + 32 * c];
+#pragma unroll
+            for (int b = 0; b < kHeadRB; ++b) {
+                float s = 0.f;
+#pragma unroll
+                for (int c = 0; c < CV; ++c) {
+                    s = fmaf(xv[c].x, wv[b][c].x, s);
+                    s = fmaf(xv[c].y, wv[b][c].y, s);
+                    s = fmaf(xv[c].z, wv[b][c].z, s);
+                    s = fmaf(xv[c].w, wv[b][c].w, s);
+                }
+                p[b * T + tt] = s;
             }
         }
+        const float sum = xor_reduce_scatter<NV>(p, lane);
+        if (writer && my_t < t && i + my_b < r1)
+            a.out[(static_cast<int64_t>(my_t) * nh + h) * rows + i + my_b] = sum;
     }
 }
 
@@ -103,14 +217,12 @@ __global__ void __launch_bounds__(kMlaThreads)
 // Gathered attention.  One cluster of kParts CTAs per (t, group of H heads); CTA `part` of the
 // cluster takes the fixed slot range [part * per, (part + 1) * per) and keeps, per head, the
 // running max m, sum l and unnormalised output acc[kv_rank] of an online softmax over that
-// range, kRowsC staged rows at a time.  The partials are then combined through distributed
-// shared memory, part 0 first.  Nothing in a (t, h, r) output's arithmetic depends on H, so
-// every head grouping (the `split` of the entry point) gives the same bits.
+// range, kRowsC gathered rows at a time.  KV = kv_rank / 128.
 // ------------------------------------------------------------------------------------------
 constexpr int kParts = 8;   // slot parts per (t, head group) = CTAs per cluster
-constexpr int kRowsC = 16;  // gathered rows staged per step (>= 8 so the rows buffer can hold
-                            // the H x kv_rank partial outputs for the combine)
-
+constexpr int kRowsC = 16;  // gathered rows per chunk (>= 8 so one stage can hold the H x
+                            // kv_rank partial outputs for the merge)
+constexpr int kMaxStages = 4;
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -131,24 +243,37 @@ __device__ __forceinline__ float ld_dsmem(const float *p, uint32_t rank) {
     return v;
 }
 
+struct AttnArgs {
+    const float *q_lat, *q_pe, *cache;
+    const int32_t *idx;
+    float *out;
+    int nh, d_rope, n_slots, stages;
+    float scale;
+};
+
 template <int KV, int H>
-__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads)
-    attn_gathered_kernel(const float *__restrict__ q_lat, const float *__restrict__ q_pe,
-                         const float *__restrict__ cache, const int32_t *__restrict__ idx,
-                         float *__restrict__ out, int nh, int d_rope, int n_slots, float scale) {
+__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
+    attn_gathered_kernel(const __grid_constant__ AttnArgs a) {
     constexpr int kv_rank = KV * 128;
     constexpr int KD = (kv_rank + kMlaThreads - 1) / kMlaThreads;  // output dims per thread
+    constexpr int NV = 2 * H;                                     // dots per warp per chunk
+    constexpr int kLaneShift = 5 - ilog2(NV);
     extern __shared__ __align__(16) float sm[];
+    const int d_rope = a.d_rope, n_slots = a.n_slots, S = a.stages, nh = a.nh;
     const int row_len = kv_rank + d_rope;
     const int row_pad = (row_len + 3) & ~3;  // float4-aligned rows in shared memory
-    float *sq = sm;                           // [H][row_pad]   the group's queries
-    float *rows = sq + H * row_pad;           // [kRowsC][row_pad], then [H][kv_rank] partials
-    float *ss = rows + kRowsC * row_pad;      // [kRowsC][H]    scaled scores of the chunk
-    float *pw = ss + kRowsC * H;              // [kRowsC][H]    softmax weights of the chunk
-    float *smm = pw + kRowsC * H;             // [H] running max
-    float *smn = smm + H;                     // [H] the chunk's new max
-    float *sal = smn + H;                     // [H] rescale factor exp(m_old - m_new)
-    float *sl = sal + H;                      // [H] running sum
+    const int stage_f = kRowsC * row_pad;
+    // Bulk copies need 16-byte aligned rows in global memory: row_len % 4 == 0.  Otherwise the
+    // rows are staged with plain loads into one stage, synchronously.
+    const bool bulk = (row_len & 3) == 0;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm);  // [kMaxStages] rows landed
+    float *sq = sm + 2 * kMaxStages;                     // [H][row_pad]   the group's queries
+    float *ring = sq + H * row_pad;                      // [S][kRowsC][row_pad]
+    float *ss = ring + S * stage_f;                      // [kRowsC][H] scaled scores
+    float *pw = ss + kRowsC * H;                         // [kRowsC][H] softmax weights
+    float *smm = pw + kRowsC * H;                        // [H] running max
+    float *sal = smm + H;                                // [H] rescale factor exp(m_old - m_new)
+    float *sl = sal + H;                                 // [H] running sum
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int part = static_cast<int>(cluster_ctarank());
@@ -156,19 +281,59 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads)
     const int grp = blockIdx.x / kParts;
     const int tt = grp / ngrp, h0 = (grp - tt * ngrp) * H;
 
+    const int per = ((n_slots + kParts - 1) / kParts + kRowsC - 1) / kRowsC * kRowsC;
+    const int j_begin = min(part * per, n_slots), j_end = min(j_begin + per, n_slots);
+    const int nchunks = (j_end - j_begin + kRowsC - 1) / kRowsC;
+    const int32_t *ix = a.idx + static_cast<int64_t>(tt) * n_slots;
+    const uint32_t row_bytes = static_cast<uint32_t>(row_len) * 4u;
+
+    if (tid == 0) {
+        for (int s = 0; s < kMaxStages; ++s) mbar_init(&bars[s], 1);
+        mbar_init_fence();
+    }
     for (int i = tid; i < H * row_len; i += kMlaThreads) {
         const int hh = i / row_len, k = i - hh * row_len;
         const int64_t th = static_cast<int64_t>(tt) * nh + min(h0 + hh, nh - 1);
-        sq[hh * row_pad + k] = k < kv_rank ? __ldg(q_lat + th * kv_rank + k)
-                                           : __ldg(q_pe + th * d_rope + (k - kv_rank));
+        sq[hh * row_pad + k] = k < kv_rank ? __ldg(a.q_lat + th * kv_rank + k)
+                                           : __ldg(a.q_pe + th * d_rope + (k - kv_rank));
     }
     if (tid < H) {
         smm[tid] = -INFINITY;
         sl[tid] = 0.f;
     }
-    const int per = ((n_slots + kParts - 1) / kParts + kRowsC - 1) / kRowsC * kRowsC;
-    const int j_begin = min(part * per, n_slots), j_end = min(j_begin + per, n_slots);
-    const int32_t *ix = idx + static_cast<int64_t>(tt) * n_slots;
+    __syncthreads();
+    // The lane's latent query slices of all H heads in registers when they take <= 64 of them.
+    constexpr bool kQReg = H * KV <= 16;
+    float4 qreg[kQReg ? H : 1][kQReg ? KV : 1];
+    if constexpr (kQReg) {
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh)
+#pragma unroll
+            for (int k = 0; k < KV; ++k)
+                qreg[hh][k] = reinterpret_cast<const float4 *>(sq + hh * row_pad)[lane + 32 * k];
+    }
+
+    // Warp 0 issues the bulk copies, S - 1 chunks ahead: lane j < 16 copies row j of a chunk.
+    // `nidx` holds the gather index of the lane's row in the next chunk to issue.
+    int issued = 0;
+    int nidx = 0;
+    if (bulk && warp == 0 && lane < kRowsC && j_begin + lane < j_end) nidx = __ldg(ix + j_begin + lane);
+    auto issue_next = [&]() {  // warp 0 only; chunk `issued` into stage issued % S
+        if (issued >= nchunks) return;
+        const int j0 = j_begin + issued * kRowsC;
+        const int nj = min(kRowsC, j_end - j0);
+        uint64_t *bar = &bars[issued % S];
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nj) * row_bytes);
+        __syncwarp();
+        if (lane < nj)
+            bulk_g2s_plain(ring + (issued % S) * stage_f + lane * row_pad,
+                           a.cache + static_cast<int64_t>(nidx) * row_len, row_bytes, bar);
+        ++issued;
+        const int jn = j0 + kRowsC + lane;
+        if (lane < kRowsC && issued < nchunks && jn < j_end) nidx = __ldg(ix + jn);
+    };
+    if (bulk && warp == 0)
+        for (int c = 0; c < S - 1; ++c) issue_next();
 
     float acc[KD][H];
 #pragma unroll
@@ -176,62 +341,91 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads)
 #pragma unroll
         for (int hh = 0; hh < H; ++hh) acc[k][hh] = 0.f;
 
-    for (int j0 = j_begin; j0 < j_end; j0 += kRowsC) {
+    bool failed = false;  // this thread's wait for a stage gave up
+    for (int c = 0; c < nchunks; ++c) {
+        const int j0 = j_begin + c * kRowsC;
         const int nj = min(kRowsC, j_end - j0);
-        __syncthreads();  // the previous chunk's rows and weights are no longer read
-        for (int i = tid; i < nj * (kv_rank / 4); i += kMlaThreads) {
-            const int j = i / (kv_rank / 4), k = i - j * (kv_rank / 4);
-            const float *src = cache + static_cast<int64_t>(__ldg(ix + j0 + j)) * row_len + 4 * k;
-            float4 v;
-            if (row_len % 4 == 0) {
-                v = __ldg(reinterpret_cast<const float4 *>(src));
-            } else {
-                v = make_float4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
+        const float *rows = ring + (bulk ? (c % S) * stage_f : 0);
+        if (bulk) {
+            // stage (c - 1) % S was released by the barrier that ended chunk c - 1
+            if (warp == 0) issue_next();
+            if (!warp_wait_bounded(&bars[c % S], static_cast<uint32_t>((c / S) & 1))) {
+                failed = true;
+                if (lane == 0) atomicOr(&g_mla_fault, kFaultAttnWait);
             }
-            reinterpret_cast<float4 *>(rows + j * row_pad)[k] = v;
+        } else {
+            float *dst = ring;
+            for (int i = tid; i < nj * row_len; i += kMlaThreads) {
+                const int j = i / row_len, k = i - j * row_len;
+                dst[j * row_pad + k] = __ldg(a.cache + static_cast<int64_t>(__ldg(ix + j0 + j)) * row_len + k);
+            }
+            __syncthreads();
         }
-        for (int i = tid; i < nj * d_rope; i += kMlaThreads) {
-            const int j = i / d_rope, k = i - j * d_rope;
-            rows[j * row_pad + kv_rank + k] =
-                __ldg(cache + static_cast<int64_t>(__ldg(ix + j0 + j)) * row_len + kv_rank + k);
-        }
-        __syncthreads();
-        // Scores: warp w takes rows w, w + 8; a lane's partial covers its float4s of the latent
-        // part in order, then its rope floats; a fixed xor tree sums the lanes.
-        for (int j = warp; j < nj; j += kMlaWarps) {
-            const float4 *r4 = reinterpret_cast<const float4 *>(rows + j * row_pad);
-            float4 rv[KV];
+        // Scores: warp w takes rows w and w + 8 for all H heads (2H dots, one reduce-scatter);
+        // both rows stay in registers while the heads' queries stream past them.
+        {
+            float p[NV];
+            const int ja = warp < nj ? warp : 0;  // rows past the chunk end: computed, not stored
+            const int jb = warp + kMlaWarps < nj ? warp + kMlaWarps : 0;
+            const float4 *ra = reinterpret_cast<const float4 *>(rows + ja * row_pad);
+            const float4 *rb = reinterpret_cast<const float4 *>(rows + jb * row_pad);
+            float4 rva[KV], rvb[KV];
 #pragma unroll
-            for (int c = 0; c < KV; ++c) rv[c] = r4[lane + 32 * c];
+            for (int k = 0; k < KV; ++k) {
+                rva[k] = ra[lane + 32 * k];
+                rvb[k] = rb[lane + 32 * k];
+            }
 #pragma unroll
             for (int hh = 0; hh < H; ++hh) {
                 const float4 *q4 = reinterpret_cast<const float4 *>(sq + hh * row_pad);
-                float s = 0.f;
+                float sa = 0.f, sb = 0.f;
 #pragma unroll
-                for (int c = 0; c < KV; ++c) {
-                    const float4 a = q4[lane + 32 * c];
-                    s = fmaf(a.x, rv[c].x, s);
-                    s = fmaf(a.y, rv[c].y, s);
-                    s = fmaf(a.z, rv[c].z, s);
-                    s = fmaf(a.w, rv[c].w, s);
+                for (int k = 0; k < KV; ++k) {
+                    const float4 qv = kQReg ? qreg[kQReg ? hh : 0][kQReg ? k : 0] : q4[lane + 32 * k];
+                    sa = fmaf(qv.x, rva[k].x, sa);
+                    sa = fmaf(qv.y, rva[k].y, sa);
+                    sa = fmaf(qv.z, rva[k].z, sa);
+                    sa = fmaf(qv.w, rva[k].w, sa);
+                    sb = fmaf(qv.x, rvb[k].x, sb);
+                    sb = fmaf(qv.y, rvb[k].y, sb);
+                    sb = fmaf(qv.z, rvb[k].z, sb);
+                    sb = fmaf(qv.w, rvb[k].w, sb);
                 }
-                for (int k = lane; k < d_rope; k += 32)
-                    s = fmaf(sq[hh * row_pad + kv_rank + k], rows[j * row_pad + kv_rank + k], s);
-                s = warp_sum(s);
-                if (lane == 0) ss[j * H + hh] = __fmul_rn(scale, s);
+                for (int k = lane; k < d_rope; k += 32) {
+                    const float qk = sq[hh * row_pad + kv_rank + k];
+                    sa = fmaf(qk, rows[ja * row_pad + kv_rank + k], sa);
+                    sb = fmaf(qk, rows[jb * row_pad + kv_rank + k], sb);
+                }
+                p[hh] = sa;
+                p[H + hh] = sb;
             }
+            const float sum = xor_reduce_scatter<NV>(p, lane);
+            const int e = lane >> kLaneShift;
+            const int j = warp + (e / H) * kMlaWarps, hh = e % H;
+            if ((lane & ((1 << kLaneShift) - 1)) == 0 && j < nj) ss[j * H + hh] = __fmul_rn(a.scale, sum);
         }
-        __syncthreads();
-        // Online softmax step, per head: new max over the chunk, weights, rescale factor.
-        if (tid < nj * H) {
-            const int hh = tid % H, j = tid / H;
+        // The chunk's scores are complete; a wait that gave up anywhere stops every warp here,
+        // together (the barrier's OR is the same in every thread).
+        if (__syncthreads_or(failed)) break;
+        // Online softmax step: warp hh < H updates head hh, lane j < nj holding score j.  The
+        // chunk's max is a shuffle max (exact), its weight sum a fixed xor tree over lanes 0-15.
+        if (warp < H) {
+            const int hh = warp;
             const float mo = smm[hh];
-            float mc = mo;
-            for (int q = 0; q < nj; ++q) mc = fmaxf(mc, ss[q * H + hh]);
-            pw[tid] = expf(ss[tid] - mc);
-            if (j == 0) {
-                sal[hh] = mo == -INFINITY ? 0.f : expf(mo - mc);
-                smn[hh] = mc;
+            const float s = lane < nj ? ss[lane * H + hh] : -INFINITY;
+            float mc = fmaxf(mo, s);
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFullMask, mc, off));
+            const float pj = lane < nj ? expf(s - mc) : 0.f;
+            if (lane < nj) pw[lane * H + hh] = pj;
+            float lc = pj;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) lc += __shfl_xor_sync(kFullMask, lc, off);
+            if (lane == 0) {
+                const float al = mo == -INFINITY ? 0.f : expf(mo - mc);
+                sal[hh] = al;
+                sl[hh] = fmaf(sl[hh], al, lc);
+                smm[hh] = mc;
             }
         }
         __syncthreads();
@@ -239,24 +433,42 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads)
         for (int k = 0; k < KD; ++k) {
             const int d = tid + k * kMlaThreads;
             if (d < kv_rank) {
+                float al[H];
 #pragma unroll
-                for (int hh = 0; hh < H; ++hh) acc[k][hh] *= sal[hh];
+                for (int hh = 0; hh < H; ++hh) al[hh] = sal[hh];
+#pragma unroll
+                for (int hh = 0; hh < H; ++hh) acc[k][hh] *= al[hh];
                 for (int j = 0; j < nj; ++j) {
                     const float rv = rows[j * row_pad + d];
+                    float pj[H];
+                    if constexpr (H % 4 == 0) {
 #pragma unroll
-                    for (int hh = 0; hh < H; ++hh) acc[k][hh] = fmaf(pw[j * H + hh], rv, acc[k][hh]);
+                        for (int q = 0; q < H / 4; ++q) {
+                            const float4 v4 = reinterpret_cast<const float4 *>(pw + j * H)[q];
+                            pj[4 * q] = v4.x;
+                            pj[4 * q + 1] = v4.y;
+                            pj[4 * q + 2] = v4.z;
+                            pj[4 * q + 3] = v4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int hh = 0; hh < H; ++hh) pj[hh] = pw[j * H + hh];
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < H; ++hh) acc[k][hh] = fmaf(pj[hh], rv, acc[k][hh]);
                 }
             }
         }
-        if (tid < H) {
-            float lc = 0.f;
-            for (int j = 0; j < nj; ++j) lc += pw[j * H + tid];
-            sl[tid] = fmaf(sl[tid], sal[tid], lc);
-            smm[tid] = smn[tid];
-        }
+        __syncthreads();  // the stage and the chunk's weights are free again
     }
-    __syncthreads();  // the rows buffer is free: it takes this part's partial outputs
-    float *sacc = rows;
+    if (bulk && warp == 0) {
+        // Every copy issued must land before the stages take the partials or the CTA exits (all
+        // of them already have unless a wait gave up).
+        for (int c = max(0, issued - S); c < issued; ++c)
+            (void)warp_wait_bounded(&bars[c % S], static_cast<uint32_t>((c / S) & 1));
+    }
+    __syncthreads();
+    float *sacc = ring;  // this part's partial outputs [H][kv_rank] (fits one stage)
 #pragma unroll
     for (int k = 0; k < KD; ++k) {
         const int d = tid + k * kMlaThreads;
@@ -266,23 +478,26 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads)
         }
     }
     cluster_sync_all();
-    // Combine: this CTA finalises outputs [c0, c1) of the group's H x kv_rank, parts in order.
+    // Merge: this CTA finalises outputs [c0, c1) of the group's H x kv_rank, parts in order.
     const int c0 = part * (H * kv_rank) / kParts, c1 = (part + 1) * (H * kv_rank) / kParts;
     for (int i = c0 + tid; i < c1; i += kMlaThreads) {
         const int hh = i / kv_rank, d = i - hh * kv_rank;
+        float mq[kParts];
         float mx = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kParts; ++q) mx = fmaxf(mx, ld_dsmem(smm + hh, q));
+        for (int q = 0; q < kParts; ++q) {
+            mq[q] = ld_dsmem(smm + hh, q);
+            mx = fmaxf(mx, mq[q]);
+        }
         float lsum = 0.f, o = 0.f;
 #pragma unroll
         for (int q = 0; q < kParts; ++q) {
-            const float mq = ld_dsmem(smm + hh, q);
-            const float wq = mq == -INFINITY ? 0.f : expf(mq - mx);
+            const float wq = mq[q] == -INFINITY ? 0.f : expf(mq[q] - mx);
             lsum = fmaf(ld_dsmem(sl + hh, q), wq, lsum);
             o = fmaf(ld_dsmem(sacc + i, q), wq, o);
         }
         if (h0 + hh < nh)
-            out[(static_cast<int64_t>(tt) * nh + h0 + hh) * kv_rank + d] = __fdiv_rn(o, lsum);
+            a.out[(static_cast<int64_t>(tt) * nh + h0 + hh) * kv_rank + d] = __fdiv_rn(o, lsum);
     }
     cluster_sync_all();  // no CTA leaves while another still reads its shared memory
 }
@@ -296,6 +511,45 @@ int sm_count() {
     return sms;
 }
 
+template <int CV, int T>
+int launch_head(const float *x, const float *w, float *out, int t, int nh, int rows, int split,
+                cudaStream_t st) {
+    const auto kern = head_gemv_kernel<CV, T>;
+    const size_t fixed = sizeof(float) * (4 * kHeadMaxStages + 16 + static_cast<size_t>(T) * CV * 128);
+    const size_t stage = sizeof(float) * static_cast<size_t>(kHeadRows) * CV * 128;
+    // As many stages as fit in about half an SM's shared memory (two CTAs per SM), 2 to 4.
+    const int stages = std::max(2, std::min(kHeadMaxStages,
+                                            static_cast<int>((100 * 1024 - static_cast<int64_t>(fixed)) /
+                                                             static_cast<int64_t>(stage))));
+    const size_t smem = fixed + stages * stage;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return MEMQ_ERR_LAUNCH;
+    if (split == 0) {
+        // one wave of resident CTAs over all heads
+        const int sms = sm_count();
+        int occ = 0;
+        if (sms <= 0 || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kHeadThreads, smem) !=
+                            cudaSuccess)
+            return MEMQ_ERR_LAUNCH;
+        split = static_cast<int>(std::max<int64_t>(1, static_cast<int64_t>(std::max(occ, 1)) * sms / nh));
+    }
+    if (split > rows) split = rows;
+    if (static_cast<int64_t>(nh) * split > kMaxGrid) split = static_cast<int>(kMaxGrid / nh);
+    const HeadArgs args{x, w, out, t, nh, rows, split, stages};
+    kern<<<static_cast<unsigned>(nh * split), kHeadThreads, smem, st>>>(args);
+    return cudaGetLastError() == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+}
+
+template <int CV>
+int launch_head_t(const float *x, const float *w, float *out, int t, int nh, int rows, int split,
+                  cudaStream_t st) {
+    if (t <= 1) return launch_head<CV, 1>(x, w, out, t, nh, rows, split, st);
+    if (t <= 2) return launch_head<CV, 2>(x, w, out, t, nh, rows, split, st);
+    if (t <= 4) return launch_head<CV, 4>(x, w, out, t, nh, rows, split, st);
+    return launch_head<CV, 8>(x, w, out, t, nh, rows, split, st);
+}
+
 int head_gemv_entry(const float *x, const float *w, float *out, int t, int nh, int rows, int cols,
                     int split, void *stream) {
     if (t < 1 || t > kMaxT) return MEMQ_ERR_M_RANGE;
@@ -304,26 +558,58 @@ int head_gemv_entry(const float *x, const float *w, float *out, int t, int nh, i
         return MEMQ_ERR_SHAPE;
     if (!x || !w || !out) return MEMQ_ERR_NULL;
     if (!aligned16(x) || !aligned16(w) || (reinterpret_cast<uintptr_t>(out) & 3u)) return MEMQ_ERR_ALIGN;
-    const int sms = sm_count();
-    if (sms <= 0) return MEMQ_ERR_LAUNCH;
-    if (split == 0) split = (4 * sms + nh - 1) / nh;
-    if (split > rows) split = rows;
-    if (static_cast<int64_t>(nh) * split > kMaxGrid) split = static_cast<int>(kMaxGrid / nh);
-    const size_t smem = static_cast<size_t>(t) * cols * sizeof(float);
-    const dim3 grid(static_cast<unsigned>(nh * split));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (cols / 128) {
-        case 1: head_gemv_kernel<1><<<grid, kMlaThreads, smem, st>>>(x, w, out, t, nh, rows, split); break;
-        case 2: head_gemv_kernel<2><<<grid, kMlaThreads, smem, st>>>(x, w, out, t, nh, rows, split); break;
-        case 4: head_gemv_kernel<4><<<grid, kMlaThreads, smem, st>>>(x, w, out, t, nh, rows, split); break;
-        case 8: head_gemv_kernel<8><<<grid, kMlaThreads, smem, st>>>(x, w, out, t, nh, rows, split); break;
+        case 1: return launch_head_t<1>(x, w, out, t, nh, rows, split, st);
+        case 2: return launch_head_t<2>(x, w, out, t, nh, rows, split, st);
+        case 4: return launch_head_t<4>(x, w, out, t, nh, rows, split, st);
+        case 8: return launch_head_t<8>(x, w, out, t, nh, rows, split, st);
         default: return MEMQ_ERR_SHAPE;
     }
+}
+
+template <int KV, int H>
+int launch_attn(const AttnArgs &args0, int t, cudaStream_t st) {
+    AttnArgs args = args0;
+    const int row_len = KV * 128 + args.d_rope;
+    const int row_pad = (row_len + 3) & ~3;
+    const size_t fixed = sizeof(uint64_t) * kMaxStages +
+                         sizeof(float) * (static_cast<size_t>(H) * row_pad + 2 * kRowsC * H + 3 * H + 4);
+    const size_t stage = sizeof(float) * static_cast<size_t>(kRowsC) * row_pad;
+    // As many stages as fit in about half an SM's shared memory (two CTAs per SM), 2 to 4.
+    int stages = static_cast<int>((112 * 1024 - static_cast<int64_t>(fixed)) / static_cast<int64_t>(stage));
+    stages = std::max(2, std::min(kMaxStages, stages));
+    if ((row_len & 3) != 0) stages = 1;  // plain loads: one stage
+    args.stages = stages;
+    const size_t smem = fixed + stages * stage;
+    if (cudaFuncSetAttribute(attn_gathered_kernel<KV, H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return MEMQ_ERR_LAUNCH;
+    const unsigned groups = static_cast<unsigned>(t) * static_cast<unsigned>((args.nh + H - 1) / H);
+    attn_gathered_kernel<KV, H><<<groups * kParts, kMlaThreads, smem, st>>>(args);
     return cudaGetLastError() == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+}
+
+template <int KV>
+int launch_attn_h(int H, const AttnArgs &args, int t, cudaStream_t st) {
+    switch (H) {
+        case 8: return launch_attn<KV, 8>(args, t, st);
+        case 4: return launch_attn<KV, 4>(args, t, st);
+        case 2: return launch_attn<KV, 2>(args, t, st);
+        default: return launch_attn<KV, 1>(args, t, st);
+    }
 }
 
 }  // namespace
 }  // namespace memq
+
+// Internal: this translation unit's device fault word (not part of the public header).
+int memq_internal_fault_mla(unsigned int *out, bool clear) {
+    if (cudaMemcpyFromSymbol(out, memq::g_mla_fault, sizeof(unsigned int)) != cudaSuccess) return 1;
+    if (!clear) return 0;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(memq::g_mla_fault, &zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
 
 extern "C" int memq_mla_absorb_q(const float *q_nope, const float *wk_b, float *out, int t,
                                  int nh, int d_nope, int kv_rank, int split, void *stream) {
@@ -335,50 +621,15 @@ extern "C" int memq_mla_decompress_v(const float *o_lat, const float *wv_b, floa
     return memq::head_gemv_entry(o_lat, wv_b, out, t, nh, d_v, kv_rank, split, stream);
 }
 
-namespace memq {
-namespace {
-
-template <int KV, int H>
-int launch_attn(const float *q_lat, const float *q_pe, const float *cache, const int32_t *idx,
-                float *out, int nh, int d_rope, int t, int n_slots, float scale, cudaStream_t st) {
-    const int row_pad = (KV * 128 + d_rope + 3) & ~3;
-    const size_t smem = sizeof(float) * (static_cast<size_t>(row_pad) * (H + kRowsC) +
-                                         2 * kRowsC * H + 4 * H);
-    if (cudaFuncSetAttribute(attn_gathered_kernel<KV, H>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return MEMQ_ERR_LAUNCH;
-    const unsigned groups = static_cast<unsigned>(t) * static_cast<unsigned>((nh + H - 1) / H);
-    attn_gathered_kernel<KV, H><<<groups * kParts, kMlaThreads, smem, st>>>(
-        q_lat, q_pe, cache, idx, out, nh, d_rope, n_slots, scale);
-    return cudaGetLastError() == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
-}
-
-template <int KV>
-int launch_attn_h(int H, const float *q_lat, const float *q_pe, const float *cache,
-                  const int32_t *idx, float *out, int nh, int d_rope, int t, int n_slots,
-                  float scale, cudaStream_t st) {
-    switch (H) {
-        case 8: return launch_attn<KV, 8>(q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
-        case 4: return launch_attn<KV, 4>(q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
-        case 2: return launch_attn<KV, 2>(q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
-        default: return launch_attn<KV, 1>(q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
-    }
-}
-
-}  // namespace
-}  // namespace memq
-
 extern "C" int memq_mla_attn_gathered(const float *q_lat, const float *q_pe, const float *cache,
                                       const int32_t *idx, float *out, int nh, int kv_rank,
                                       int d_rope, int t, int n_slots, float scale, int split,
                                       void *stream) {
     using namespace memq;
     if (t < 1 || t > kMaxT) return MEMQ_ERR_M_RANGE;
-    if (nh < 1 || nh > kMaxHeads || kv_rank < 128 || kv_rank % 128 != 0 || kv_rank > 1024 || d_rope < 0 ||
-        d_rope > kMaxRope || n_slots < 1 || !(split == 0 || split == 1 || split == 2 ||
-                                               split == 4 || split == 8) ||
-        !std::isfinite(scale))
+    if (nh < 1 || nh > kMaxHeads || kv_rank < 128 || kv_rank % 128 != 0 || kv_rank > 1024 ||
+        d_rope < 0 || d_rope > kMaxRope || n_slots < 1 ||
+        !(split == 0 || split == 1 || split == 2 || split == 4 || split == 8) || !std::isfinite(scale))
         return MEMQ_ERR_SHAPE;
     if (!q_lat || !cache || !idx || !out || (d_rope > 0 && !q_pe)) return MEMQ_ERR_NULL;
     if (!aligned16(cache) || (reinterpret_cast<uintptr_t>(q_lat) & 3u) ||
@@ -399,12 +650,13 @@ extern "C" int memq_mla_attn_gathered(const float *q_lat, const float *q_pe, con
         }
     }
     const int H = 8 / split;
+    const AttnArgs args{q_lat, q_pe, cache, idx, out, nh, d_rope, n_slots, 0, scale};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (kv_rank / 128) {
-        case 1: return launch_attn_h<1>(H, q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
-        case 2: return launch_attn_h<2>(H, q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
-        case 4: return launch_attn_h<4>(H, q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
-        case 8: return launch_attn_h<8>(H, q_lat, q_pe, cache, idx, out, nh, d_rope, t, n_slots, scale, st);
+        case 1: return launch_attn_h<1>(H, args, t, st);
+        case 2: return launch_attn_h<2>(H, args, t, st);
+        case 4: return launch_attn_h<4>(H, args, t, st);
+        case 8: return launch_attn_h<8>(H, args, t, st);
         default: return MEMQ_ERR_SHAPE;
     }
 }
