@@ -176,21 +176,32 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per GEMV launch from the committed ncu capture of this workload, or None when
-    there is none or the kernel sources changed since it was taken."""
-    import glob
+# Source files each committed traffic record depends on (the kernel and its building blocks).
+TRAFFIC_SOURCES = {
+    "gemv_traffic.json": ("memq_dev.cuh", "memq_gemv_kernels.cuh", "memq_gemv_e4m3.cu",
+                          "memq_gemv_blk128.cu", "memq_gemv_q8_0.cu"),
+    "mla_traffic.json": ("memq_dev.cuh", "memq_mla.cu"),
+}
+
+
+def sources_sha256(record: str) -> str:
     import hashlib
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES[record]:
+        with open(os.path.join(ROOT, "quantized_decode_memq_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str, record: str = "gemv_traffic.json"):
+    """DRAM bytes per launch from the committed ncu capture of this workload, or None when there
+    is none or the kernel's sources changed since it was taken."""
     try:
-        with open(os.path.join(ROOT, "profiles", "gemv_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", record)) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(ROOT, "quantized_decode_memq_gb300", "csrc", "*.cu*"))):
-        with open(path, "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != rec.get("kernel_sources_sha256"):
+    if sources_sha256(record) != rec.get("kernel_sources_sha256"):
         return None
     return rec.get("dram_bytes_per_launch", {}).get(workload)
 
@@ -750,13 +761,15 @@ def run_mla(args, world, rank, local, dev):
         achieved = wl.flops / t_launch / 1e12
         peak = F32_FMA_TFLOPS
         roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic(args.workload, "mla_traffic.json"),
                 "peak_kind": "derived: 152 SMs x 128 f32 FMA/clk x 2 FLOP x 2.07 GHz"}
     else:
         peak, peak_kind = measured_peak_hbm()
         achieved = wl.step_bytes / t_launch / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind}
+                "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic(args.workload, "mla_traffic.json"), "peak_kind": peak_kind}
     desc = {"absorb": f"mla_absorb_q t={t}: 64 heads x (512 x 256) f32 weights",
             "decompress": f"mla_decompress_v t={t}: 64 heads x (256 x 512) f32 weights",
             "attn": f"mla_attn_gathered t={t}: 64 heads, kv_rank 512, 2048 slots from {kv} rows"}
