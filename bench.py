@@ -14,7 +14,8 @@ Printed (rank 0, one JSON line):
               duration in a decode loop (graph of back-to-back launches over the rotated
               copies, DRAM-cold), against the measured HBM copy bandwidth; the one-launch-at-a-
               time figure is reported beside it.
-  e2e         the same metric through the public API with host buffers: per step the
+  e2e         the same metric through the public API with host buffers, per step one replay of
+              a CUDA graph holding those calls (the eager Python loop is reported beside it): the
               activation row is copied host->device from pinned memory, the chain runs, the
               result y is copied device->host and the host waits for it.
   cpu_baseline  the f64 oracle on the host cores on a bounded sample of the same workload.
@@ -550,8 +551,10 @@ def run_ours(args, world, rank, local):
     gemv_s = time_gemv_launches(wl, stream, n=max(64, 4 * copies), fn=launch_fn)
     peak, peak_kind = measured_peak_hbm()
 
-    e2e = time_e2e(wl, stream, steps=min(K, args.e2e_steps))
+    e2e = time_e2e(wl, stream, steps=min(K, args.e2e_steps), graphs=True)
     e2e_t, e2e_units = aggregate(e2e["elapsed"], float(e2e["steps"] * wl.step_bytes))
+    eager = time_e2e(wl, stream, steps=min(K, args.e2e_steps))
+    eager_t, eager_units = aggregate(eager["elapsed"], float(eager["steps"] * wl.step_bytes))
 
     line = {
         "metric": METRIC,
@@ -603,6 +606,11 @@ def run_ours(args, world, rank, local):
             "d2h_bytes_per_step": e2e["d2h"],
             "steps": e2e["steps"],
             "us_per_step": round(e2e_t / e2e["steps"] * 1e6, 2),
+            "mode": "per step: one replay of a CUDA graph holding the public-API calls "
+                    "(H2D of x from pinned memory, producer, GEMV, D2H of y), then a host wait",
+            "eager": {"value": round(eager_units / eager_t / 1e9, 3),
+                      "us_per_step": round(eager_t / eager["steps"] * 1e6, 2),
+                      "mode": "the same calls issued from Python every step"},
         },
         "gpu_launches": (1 if fused else 2) * K,
         "clocks": clocks,
@@ -703,7 +711,11 @@ class MlaStep:
         else:
             x, w = (synth.mla_absorb_inputs(t) if kernel == "absorb"
                     else synth.mla_decompress_inputs(t))
-            self.args = (dev(x), dev(w))
+            # rotated weight copies (past twice the L2) for the back-to-back loop timing
+            self.copies = max(2, -(-2 * L2_BYTES // w.nbytes))
+            w0 = dev(w)
+            self.w = [w0] + [w0.clone() for _ in range(self.copies - 1)]
+            self.args = (dev(x), w0)
             self.out = torch.empty((t, nh, w.shape[1]), dtype=torch.float32, device=device)
             self.step_bytes = w.nbytes + x.nbytes + self.out.numel() * 4
             self.flops = 2 * t * w.size
@@ -720,7 +732,8 @@ class MlaStep:
     def step(self, i):
         fn = {"attn": self.memq.memq_mla_attn_gathered, "absorb": self.memq.memq_mla_absorb_q,
               "decompress": self.memq.memq_mla_decompress_v}[self.kernel]
-        fn(*self.args, out=self.out, split=self.split)
+        args = self.args if self.kernel == "attn" else (self.args[0], self.w[i % self.copies])
+        fn(*args, out=self.out, split=self.split)
 
 
 def run_mla(args, world, rank, local, dev):
@@ -770,6 +783,11 @@ def run_mla(args, world, rank, local, dev):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": profiled_traffic(args.workload, "mla_traffic.json"), "peak_kind": peak_kind}
+        # decode-loop view: back-to-back launches over the rotated weight copies (DRAM-cold)
+        loop_s = time_gemv_back_to_back(wl, stream, wl.copies, fn=wl.step)
+        roof["loop_period_us"] = round(loop_s * 1e6, 3)
+        roof["loop_gbs"] = round(wl.step_bytes / loop_s / 1e9, 1)
+        roof["loop_frac"] = round(wl.step_bytes / loop_s / 1e9 / peak, 4)
     desc = {"absorb": f"mla_absorb_q t={t}: 64 heads x (512 x 256) f32 weights",
             "decompress": f"mla_decompress_v t={t}: 64 heads x (256 x 512) f32 weights",
             "attn": f"mla_attn_gathered t={t}: 64 heads, kv_rank 512, 2048 slots from {kv} rows"}
@@ -913,27 +931,42 @@ def time_gemv_back_to_back(wl, stream, n, fn=None):
     return a.elapsed_time(b) / 1e3 / (4 * n)
 
 
-def time_e2e(wl, stream, steps):
-    """Public API with host buffers: H2D of the activation row, the chain, D2H of y, wait."""
+def time_e2e(wl, stream, steps, graphs=False):
+    """Public API with host buffers: per step the H2D copy of the activation row (pinned), the
+    chain, the D2H copy of y and a host wait for it.  With graphs=True each step is one replay of
+    a CUDA graph that captured exactly those public-API calls (one graph per rotated weight
+    copy), the way a caller removes the per-call launch overhead of a decode loop."""
     import torch
     x_pin = torch.from_numpy(wl.x_host.copy()).pin_memory()
     y_pin = torch.empty(wl.y.shape, dtype=torch.float32).pin_memory()
     h2d = x_pin.numel() * 4
     d2h = y_pin.numel() * 4
+
+    def one(i):
+        wl.x.copy_(x_pin, non_blocking=True)
+        wl.step(i)
+        y_pin.copy_(wl.y, non_blocking=True)
+
+    run = one
+    if graphs:
+        gs = []
+        with torch.cuda.stream(stream):
+            for c in range(wl.copies):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                    one(c)
+                gs.append(g)
+        run = lambda i: gs[i % len(gs)].replay()  # noqa: E731
     with torch.cuda.stream(stream):
         for i in range(8):
-            wl.x.copy_(x_pin, non_blocking=True)
-            wl.step(i)
-            y_pin.copy_(wl.y, non_blocking=True)
+            run(i)
             stream.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         a.record(stream)
         for i in range(steps):
-            wl.x.copy_(x_pin, non_blocking=True)
-            wl.step(i)
-            y_pin.copy_(wl.y, non_blocking=True)
+            run(i)
             stream.synchronize()
         b.record(stream)
         stream.synchronize()
