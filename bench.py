@@ -800,6 +800,8 @@ def run_mla(args, world, rank, local, dev):
                        "timing": "one launch per sample after a 256 MB scrub read, CUDA events",
                        "min_us": round(min(per) * 1e6, 3)},
             "roofline": roof, "gpu_launches": K, "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_mla(kernel, t, kv, min(args.cpu_seconds, 10.0))
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -876,6 +878,8 @@ def run_other(args, world, rank, local, dev):
                        "timing": "steps replayed from a CUDA graph, CUDA events"},
             "pct_of_peak": round(100.0 * value / peak, 2),
             "gpu_launches": wl.launches_per_step * steps, "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("stack"):
+        line["cpu_baseline"] = cpu_baseline_other(args.workload, min(args.cpu_seconds, 10.0))
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -1019,6 +1023,77 @@ def cpu_baseline(wl, seconds):
             "kind": "oracle",
             "sample": f"{n} full decode steps (f64 C oracle: producer + {kind} GEMV "
                       f"{out_f}x{in_f} m={m}), {el:.1f} s wall, single thread",
+            "host_cpus": os.cpu_count()}
+
+
+def _time_oracle(fn, seconds):
+    """Calls fn until `seconds` of wall time have passed (at least twice); seconds per call."""
+    fn()  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and n >= 2) or n >= 100000:
+            return el / n, n, el
+
+
+def cpu_baseline_other(workload, seconds):
+    """The oracle on a bounded sample of a producer / silu / repack workload, scaled to the whole
+    workload's bytes (GB/s, single thread)."""
+    import oracle
+    from quantized_decode_memq_gb300 import synth
+    oracle.build()
+    head, shape = workload.split("_", 1)
+    if head == "repack":
+        kind, dims = shape.split("_")
+        out_f, in_f = (int(v) for v in dims.split("x"))
+        rows = min(out_f, 256)
+        w = synth.e4m3_bytes(0x7600, rows, in_f)
+        grid = kind == "blk128"
+        aux = (synth.grid_log2_uniform(0x7601, rows, in_f) if grid
+               else np.array([2.0 ** -4], np.float32))
+        per, n, el = _time_oracle(lambda: oracle.repack_q8_0(w, aux, grid), seconds)
+        total = per * out_f / rows
+        nbytes = out_f * in_f + out_f * in_f // 32 * 34
+        sample = f"{n} x {rows} rows of {out_f} ({el:.1f} s)"
+    else:
+        ncols, rows_all = (int(v) for v in shape.split("x"))
+        rows = min(rows_all, 64)
+        g = synth.uniform_pm4(0x7500, rows * ncols).reshape(rows, ncols)
+        if head == "silu":
+            u = synth.uniform_pm4(0x7501, rows * ncols).reshape(rows, ncols)
+            per, n, el = _time_oracle(lambda: oracle.silu_mul_q8_1(g, u), seconds)
+            nbytes = rows_all * ncols * (4 + 4 + 4 + 1) + rows_all * ncols // 32 * 4
+        else:
+            wn = synth.uniform_pm4(0x7502, ncols)
+            per, n, el = _time_oracle(lambda: oracle.rmsnorm_q8_1(g, wn), seconds)
+            nbytes = producer_bytes(rows_all, ncols) + rows_all * ncols * 4
+        total = per * rows_all / rows
+        sample = f"{n} x {rows} rows of {rows_all} ({el:.1f} s)"
+    return {"value": round(nbytes / total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"f64 C oracle, {sample}, scaled to the whole workload", "host_cpus": os.cpu_count()}
+
+
+def cpu_baseline_mla(kernel, t, kv, seconds):
+    """The oracle on a bounded sample (a few heads) of an MLA launch, scaled to all 64 heads: us
+    per launch, single thread."""
+    import oracle
+    from quantized_decode_memq_gb300 import synth
+    oracle.build()
+    nh_s = 2
+    if kernel == "attn":
+        q_lat, _, cache, idx = synth.mla_attn_inputs(t, kv)
+        q = np.ascontiguousarray(q_lat[:, :nh_s])
+        fn = lambda: oracle.mla_attn_gathered(q, None, cache, idx, synth.MLA_SCALE)  # noqa: E731
+    else:
+        x, w = synth.mla_absorb_inputs(t) if kernel == "absorb" else synth.mla_decompress_inputs(t)
+        xs, ws = np.ascontiguousarray(x[:, :nh_s]), np.ascontiguousarray(w[:nh_s])
+        fn = lambda: oracle.mla_head_gemv(xs, ws)  # noqa: E731
+    per, n, el = _time_oracle(fn, seconds)
+    return {"value": round(per * synth.MLA_NH / nh_s * 1e6, 1), "unit": "us", "cores": 1,
+            "kind": "oracle", "sample": f"f64 C oracle, {n} calls on {nh_s} of {synth.MLA_NH} heads "
+                                        f"({el:.1f} s), scaled to all heads",
             "host_cpus": os.cpu_count()}
 
 
