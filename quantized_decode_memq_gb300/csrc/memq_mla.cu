@@ -33,9 +33,11 @@
 // depend on H, which is the entry point's `split` (H = 8 / split), so the split twins are
 // bit-identical.  No global scratch: the partials live in shared memory.
 //
-// Plain stream-ordered launches (no programmatic dependent launch): every input is complete
-// when a kernel starts.
+// absorb_q / decompress_v use programmatic dependent launch (the constant weights stream while
+// the preceding grid finishes; x is read after griddepcontrol.wait, through L2).  attn_gathered
+// is a plain stream-ordered launch: every one of its inputs may come from the preceding grid.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(kHeadThreads)
     uint64_t *empty = full + kHeadMaxStages;             // [kHeadMaxStages]
     float *sx = hsm + 4 * kHeadMaxStages + 16;           // [T][cols] (128-byte aligned)
     float *ring = sx + T * cols;                         // [S][kHeadRows][cols]
+    griddep_launch_dependents();
     const int S = a.stages, split = a.split, rows = a.rows, nh = a.nh, t = a.t;
     const int h = blockIdx.x / split;
     const int part = blockIdx.x - h * split;
@@ -160,11 +163,13 @@ __global__ void __launch_bounds__(kHeadThreads)
             (void)warp_wait_bounded(&full[q % S], static_cast<uint32_t>((q / S) & 1));
         return;
     }
-    // Consumers: x rows of head h into shared memory (overlapping the first weight copies).
+    // Consumers: x rows of head h into shared memory (overlapping the first weight copies).  x
+    // may be the preceding launch's output: wait for that grid, then read through L2.
+    griddep_wait();
     for (int i = threadIdx.x; i < T * cols / 4; i += kMlaThreads) {
         const int tt = i / (cols / 4), k = i - tt * (cols / 4);
         reinterpret_cast<float4 *>(sx)[i] =
-            tt < t ? __ldg(reinterpret_cast<const float4 *>(a.x + (static_cast<int64_t>(tt) * nh + h) * cols) + k)
+            tt < t ? __ldcg(reinterpret_cast<const float4 *>(a.x + (static_cast<int64_t>(tt) * nh + h) * cols) + k)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kMlaThreads) : "memory");
@@ -504,11 +509,31 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kMaxDevices = 64;
+
+// SM count of the current device (queried once per device).
 int sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev < kMaxDevices && (sms = cache[dev].load(std::memory_order_relaxed)) > 0) return sms;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
     return sms;
+}
+
+// Lets `kern` use the device's whole opt-in shared memory, once per (kernel, device); `done`
+// is the caller's per-kernel record (one bit per device).
+bool allow_max_smem(const void *kern, std::atomic<uint64_t> &done) {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const uint64_t bit = dev < kMaxDevices ? (uint64_t{1} << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+        return false;
+    if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return true;
 }
 
 template <int CV, int T>
@@ -522,9 +547,8 @@ int launch_head(const float *x, const float *w, float *out, int t, int nh, int r
                                             static_cast<int>((100 * 1024 - static_cast<int64_t>(fixed)) /
                                                              static_cast<int64_t>(stage))));
     const size_t smem = fixed + stages * stage;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
-        return MEMQ_ERR_LAUNCH;
+    static std::atomic<uint64_t> attr_done{0};
+    if (!allow_max_smem(reinterpret_cast<const void *>(kern), attr_done)) return MEMQ_ERR_LAUNCH;
     if (split == 0) {
         // one wave of resident CTAs over all heads
         const int sms = sm_count();
@@ -537,8 +561,19 @@ int launch_head(const float *x, const float *w, float *out, int t, int nh, int r
     if (split > rows) split = rows;
     if (static_cast<int64_t>(nh) * split > kMaxGrid) split = static_cast<int>(kMaxGrid / nh);
     const HeadArgs args{x, w, out, t, nh, rows, split, stages};
-    kern<<<static_cast<unsigned>(nh * split), kHeadThreads, smem, st>>>(args);
-    return cudaGetLastError() == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+    // Programmatic dependent launch: the weight stream may start while the preceding grid
+    // finishes; the consumers wait for it before reading x.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nh * split));
+    cfg.blockDim = dim3(kHeadThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args) == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
 }
 
 template <int CV>
@@ -582,8 +617,8 @@ int launch_attn(const AttnArgs &args0, int t, cudaStream_t st) {
     if ((row_len & 3) != 0) stages = 1;  // plain loads: one stage
     args.stages = stages;
     const size_t smem = fixed + stages * stage;
-    if (cudaFuncSetAttribute(attn_gathered_kernel<KV, H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    static std::atomic<uint64_t> attr_done{0};
+    if (!allow_max_smem(reinterpret_cast<const void *>(attn_gathered_kernel<KV, H>), attr_done))
         return MEMQ_ERR_LAUNCH;
     const unsigned groups = static_cast<unsigned>(t) * static_cast<unsigned>((args.nh + H - 1) / H);
     attn_gathered_kernel<KV, H><<<groups * kParts, kMlaThreads, smem, st>>>(args);

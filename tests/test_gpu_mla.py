@@ -177,3 +177,62 @@ def test_attn_gathered_sharp_softmax(memq, oracle):
     slots and the running max changes between chunks."""
     q_lat, _, cache, idx = synth.mla_attn_inputs(1, 2048, nh=8)
     run_attn(memq, oracle, q_lat, None, cache, idx, 4.0)
+
+
+def test_head_gemv_hand_off_between_overlapping_launches(memq):
+    """decompress_v's output [t, 64, 256] is absorb_q's input: launched back to back, absorb_q's
+    weight stream overlaps the end of decompress_v (programmatic dependent launch) and its
+    consumers must still read the finished x.  20 chains on fresh inputs, each bit-identical to
+    the same two calls separated by a device synchronize."""
+    t = 4
+    _, wk = synth.mla_absorb_inputs(t)
+    _, wv = synth.mla_decompress_inputs(t)
+    dwk, dwv = to_dev(wk), to_dev(wv)
+    o_all = [to_dev(synth.mla_randf(t * 64 * 512, 0x8200 + i).reshape(t, 64, 512)) for i in range(20)]
+    mid = torch.empty((t, 64, 256), dtype=torch.float32, device="cuda")
+    outs = []
+    for o in o_all:  # back to back on one stream, one shared intermediate buffer
+        memq.memq_mla_decompress_v(o, dwv, out=mid)
+        outs.append(memq.memq_mla_absorb_q(mid, dwk))
+    torch.cuda.synchronize()
+    for o, got in zip(o_all, outs):
+        m2 = memq.memq_mla_decompress_v(o, dwv)
+        torch.cuda.synchronize()
+        ref = memq.memq_mla_absorb_q(m2, dwk)
+        torch.cuda.synchronize()
+        assert_bits_equal(got, ref, "chained absorb_q")
+    assert memq.memq_device_fault() == 0
+
+
+def test_mla_kernels_in_a_cuda_graph(memq):
+    """The three kernels captured in one CUDA graph and replayed give the eager outputs."""
+    t = 2
+    q, wk = synth.mla_absorb_inputs(t)
+    o, wv = synth.mla_decompress_inputs(t)
+    q_lat, _, cache, idx = synth.mla_attn_inputs(t, 4096)
+    dq, dwk, do, dwv = to_dev(q), to_dev(wk), to_dev(o), to_dev(wv)
+    dql, dc, di = to_dev(q_lat), to_dev(cache), to_dev(idx)
+    outs = [torch.empty((t, 64, 512), dtype=torch.float32, device="cuda"),
+            torch.empty((t, 64, 256), dtype=torch.float32, device="cuda"),
+            torch.empty((t, 64, 512), dtype=torch.float32, device="cuda")]
+
+    def run():
+        memq.memq_mla_absorb_q(dq, dwk, out=outs[0])
+        memq.memq_mla_decompress_v(do, dwv, out=outs[1])
+        memq.memq_mla_attn_gathered(dql, None, dc, di, synth.MLA_SCALE, out=outs[2])
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run()
+        s.synchronize()
+        eager = [x.clone() for x in outs]
+        for x in outs:
+            x.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            run()
+        g.replay()
+        g.replay()
+    s.synchronize()
+    for a, b in zip(outs, eager):
+        assert_bits_equal(a, b, "graph replay")
