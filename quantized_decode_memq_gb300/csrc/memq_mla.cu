@@ -26,8 +26,8 @@
 // attn_gathered_kernel: every head of query row t gathers the same n_slots rows, so a CTA
 // serves a group of H heads from one staged copy of them, and a cluster of 8 CTAs splits the
 // slots into 8 fixed ranges.  The gathered rows stream into a ring of shared-memory stages by
-// bulk copies (one per row, completing on an mbarrier per stage), issued S - 1 chunks ahead of
-// the compute.  Each CTA runs an online softmax over its range (running max m, sum l, outputs
+// bulk copies (one per row, completing on an mbarrier per stage; each warp issues 2 rows of a
+// chunk), issued S - 1 chunks ahead of the compute.  Each CTA runs an online softmax over its range (running max m, sum l, outputs
 // rescaled by exp(m_old - m_new) per chunk of 16 rows); the 8 partials are merged through
 // distributed shared memory in part order.  The slot ranges, chunks and merge order do not
 // depend on H, which is the entry point's `split` (H = 8 / split), so the split twins are
@@ -318,26 +318,31 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
                 qreg[hh][k] = reinterpret_cast<const float4 *>(sq + hh * row_pad)[lane + 32 * k];
     }
 
-    // Warp 0 issues the bulk copies, S - 1 chunks ahead: lane j < 16 copies row j of a chunk.
-    // `nidx` holds the gather index of the lane's row in the next chunk to issue.
+    // Every warp issues the bulk copies of 2 rows of each chunk, S - 1 chunks ahead (lane r < 2
+    // copies row 2 * warp + r), so no warp carries all 16 copy issues; warp 0 lane 0 announces
+    // the chunk's bytes with the stage barrier's single arrival (the phase cannot complete
+    // before that arrival, whatever order the copies land in).  `nidx` holds the gather index of
+    // the lane's row in the next chunk to issue, loaded one chunk ahead.
+    constexpr int kRowsPerWarp = kRowsC / kMlaWarps;
+    static_assert(kRowsPerWarp * kMlaWarps == kRowsC && kRowsPerWarp <= 32, "rows of a chunk per warp");
+    const int my_row = warp * kRowsPerWarp + lane;  // meaningful for lane < kRowsPerWarp
     int issued = 0;
     int nidx = 0;
-    if (bulk && warp == 0 && lane < kRowsC && j_begin + lane < j_end) nidx = __ldg(ix + j_begin + lane);
-    auto issue_next = [&]() {  // warp 0 only; chunk `issued` into stage issued % S
+    if (bulk && lane < kRowsPerWarp && j_begin + my_row < j_end) nidx = __ldg(ix + j_begin + my_row);
+    auto issue_next = [&]() {  // every warp, in step; chunk `issued` into stage issued % S
         if (issued >= nchunks) return;
         const int j0 = j_begin + issued * kRowsC;
         const int nj = min(kRowsC, j_end - j0);
         uint64_t *bar = &bars[issued % S];
-        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nj) * row_bytes);
-        __syncwarp();
-        if (lane < nj)
-            bulk_g2s_plain(ring + (issued % S) * stage_f + lane * row_pad,
+        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nj) * row_bytes);
+        if (lane < kRowsPerWarp && my_row < nj)
+            bulk_g2s_plain(ring + (issued % S) * stage_f + my_row * row_pad,
                            a.cache + static_cast<int64_t>(nidx) * row_len, row_bytes, bar);
         ++issued;
-        const int jn = j0 + kRowsC + lane;
-        if (lane < kRowsC && issued < nchunks && jn < j_end) nidx = __ldg(ix + jn);
+        const int jn = j0 + kRowsC + my_row;
+        if (lane < kRowsPerWarp && issued < nchunks && jn < j_end) nidx = __ldg(ix + jn);
     };
-    if (bulk && warp == 0)
+    if (bulk)
         for (int c = 0; c < S - 1; ++c) issue_next();
 
     float acc[KD][H];
@@ -353,7 +358,7 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
         const float *rows = ring + (bulk ? (c % S) * stage_f : 0);
         if (bulk) {
             // stage (c - 1) % S was released by the barrier that ended chunk c - 1
-            if (warp == 0) issue_next();
+            issue_next();
             if (!warp_wait_bounded(&bars[c % S], static_cast<uint32_t>((c / S) & 1))) {
                 failed = true;
                 if (lane == 0) atomicOr(&g_mla_fault, kFaultAttnWait);
@@ -467,8 +472,8 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
         __syncthreads();  // the stage and the chunk's weights are free again
     }
     if (bulk && warp == 0) {
-        // Every copy issued must land before the stages take the partials or the CTA exits (all
-        // of them already have unless a wait gave up).
+        // Every copy issued (by any warp: all issue in step) must land before the stages take
+        // the partials or the CTA exits (all of them already have unless a wait gave up).
         for (int c = max(0, issued - S); c < issued; ++c)
             (void)warp_wait_bounded(&bars[c % S], static_cast<uint32_t>((c / S) & 1));
     }
