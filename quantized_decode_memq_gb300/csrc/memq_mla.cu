@@ -257,10 +257,10 @@ struct AttnArgs {
 };
 
 template <int KV, int H>
-__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
+__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H <= 2 ? 3 : 2)
     attn_gathered_kernel(const __grid_constant__ AttnArgs a) {
     constexpr int kv_rank = KV * 128;
-    constexpr int KD = (kv_rank + kMlaThreads - 1) / kMlaThreads;  // output dims per thread
+    constexpr int KP = (kv_rank / 2 + kMlaThreads - 1) / kMlaThreads;  // output dim pairs per thread
     constexpr int NV = 2 * H;                                     // dots per warp per chunk
     constexpr int kLaneShift = 5 - ilog2(NV);
     extern __shared__ __align__(16) float sm[];
@@ -345,11 +345,11 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
     if (bulk)
         for (int c = 0; c < S - 1; ++c) issue_next();
 
-    float acc[KD][H];
+    float2 acc[KP][H];
 #pragma unroll
-    for (int k = 0; k < KD; ++k)
+    for (int k = 0; k < KP; ++k)
 #pragma unroll
-        for (int hh = 0; hh < H; ++hh) acc[k][hh] = 0.f;
+        for (int hh = 0; hh < H; ++hh) acc[k][hh] = make_float2(0.f, 0.f);
 
     bool failed = false;  // this thread's wait for a stage gave up
     for (int c = 0; c < nchunks; ++c) {
@@ -439,17 +439,22 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
             }
         }
         __syncthreads();
+        // Accumulate: thread tid owns the dim pairs (2p, 2p + 1), p = tid + 256 k; one 8-byte
+        // load per row serves both dims.
 #pragma unroll
-        for (int k = 0; k < KD; ++k) {
-            const int d = tid + k * kMlaThreads;
+        for (int k = 0; k < KP; ++k) {
+            const int d = 2 * (tid + k * kMlaThreads);
             if (d < kv_rank) {
                 float al[H];
 #pragma unroll
                 for (int hh = 0; hh < H; ++hh) al[hh] = sal[hh];
 #pragma unroll
-                for (int hh = 0; hh < H; ++hh) acc[k][hh] *= al[hh];
+                for (int hh = 0; hh < H; ++hh) {
+                    acc[k][hh].x *= al[hh];
+                    acc[k][hh].y *= al[hh];
+                }
                 for (int j = 0; j < nj; ++j) {
-                    const float rv = rows[j * row_pad + d];
+                    const float2 rv = *reinterpret_cast<const float2 *>(rows + j * row_pad + d);
                     float pj[H];
                     if constexpr (H % 4 == 0) {
 #pragma unroll
@@ -460,12 +465,19 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
                             pj[4 * q + 2] = v4.z;
                             pj[4 * q + 3] = v4.w;
                         }
+                    } else if constexpr (H == 2) {
+                        const float2 v2 = *reinterpret_cast<const float2 *>(pw + j * 2);
+                        pj[0] = v2.x;
+                        pj[1] = v2.y;
                     } else {
 #pragma unroll
                         for (int hh = 0; hh < H; ++hh) pj[hh] = pw[j * H + hh];
                     }
 #pragma unroll
-                    for (int hh = 0; hh < H; ++hh) acc[k][hh] = fmaf(pj[hh], rv, acc[k][hh]);
+                    for (int hh = 0; hh < H; ++hh) {
+                        acc[k][hh].x = fmaf(pj[hh], rv.x, acc[k][hh].x);
+                        acc[k][hh].y = fmaf(pj[hh], rv.y, acc[k][hh].y);
+                    }
                 }
             }
         }
@@ -480,11 +492,11 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
     __syncthreads();
     float *sacc = ring;  // this part's partial outputs [H][kv_rank] (fits one stage)
 #pragma unroll
-    for (int k = 0; k < KD; ++k) {
-        const int d = tid + k * kMlaThreads;
+    for (int k = 0; k < KP; ++k) {
+        const int d = 2 * (tid + k * kMlaThreads);
         if (d < kv_rank) {
 #pragma unroll
-            for (int hh = 0; hh < H; ++hh) sacc[hh * kv_rank + d] = acc[k][hh];
+            for (int hh = 0; hh < H; ++hh) *reinterpret_cast<float2 *>(sacc + hh * kv_rank + d) = acc[k][hh];
         }
     }
     cluster_sync_all();
@@ -616,8 +628,10 @@ int launch_attn(const AttnArgs &args0, int t, cudaStream_t st) {
     const size_t fixed = sizeof(uint64_t) * kMaxStages +
                          sizeof(float) * (static_cast<size_t>(H) * row_pad + 2 * kRowsC * H + 3 * H + 4);
     const size_t stage = sizeof(float) * static_cast<size_t>(kRowsC) * row_pad;
-    // As many stages as fit in about half an SM's shared memory (two CTAs per SM), 2 to 4.
-    int stages = static_cast<int>((112 * 1024 - static_cast<int64_t>(fixed)) / static_cast<int64_t>(stage));
+    // As many stages as fit in the share of an SM's shared memory of one of the CTAs the
+    // register budget allows per SM (three for H <= 2, else two), 2 to 4.
+    const int64_t budget = H <= 2 ? 72 * 1024 : 112 * 1024;
+    int stages = static_cast<int>((budget - static_cast<int64_t>(fixed)) / static_cast<int64_t>(stage));
     stages = std::max(2, std::min(kMaxStages, stages));
     if ((row_len & 3) != 0) stages = 1;  // plain loads: one stage
     args.stages = stages;
