@@ -91,14 +91,15 @@ __device__ __forceinline__ float xor_reduce_scatter(float (&v)[NV], int lane) {
 
 // ------------------------------------------------------------------------------------------
 // Per-head batched GEMV.  CTA (h, part) owns rows [r0, r1) of head h, which are contiguous in
-// memory: a producer warp streams them into a ring of S stages of kHeadRows rows with one bulk
+// memory: a producer warp streams them into a ring of S stages of 8 * kHeadRB rows with one bulk
 // copy per stage (full barrier: transaction bytes; empty barrier: one arrival per consumer
 // warp), while the 8 consumer warps take kHeadRB rows of each stage.  CV = cols / 128 float4s
 // per lane per row; T = t rounded up to a power of two (rows of x beyond t are zero in shared
 // memory and their sums are not stored).
 // ------------------------------------------------------------------------------------------
-constexpr int kHeadRB = 2;                     // rows per consumer warp per stage
-constexpr int kHeadRows = kMlaWarps * kHeadRB;  // rows per stage
+// Rows per consumer warp per stage: 4 for several tokens on rows of <= 256 floats (the x rows
+// read from shared memory then serve 4 weight rows), else 2.
+__host__ __device__ constexpr int head_rb(int CV, int T) { return T >= 4 && CV <= 2 ? 4 : 2; }
 constexpr int kHeadThreads = kMlaThreads + 32;  // + the producer warp
 constexpr int kHeadMaxStages = 4;
 constexpr unsigned int kFaultHeadWait = 8u;
@@ -113,6 +114,8 @@ template <int CV, int T>
 __global__ void __launch_bounds__(kHeadThreads)
     head_gemv_kernel(const __grid_constant__ HeadArgs a) {
     constexpr int cols = CV * 128;
+    constexpr int kHeadRB = head_rb(CV, T);
+    constexpr int kHeadRows = kMlaWarps * kHeadRB;  // rows per stage
     constexpr int NV = kHeadRB * T;
     constexpr int kLaneShift = 5 - ilog2(NV);  // lane l holds element l >> kLaneShift
     constexpr uint32_t row_bytes = cols * 4u;
@@ -558,7 +561,7 @@ int launch_head(const float *x, const float *w, float *out, int t, int nh, int r
                 cudaStream_t st) {
     const auto kern = head_gemv_kernel<CV, T>;
     const size_t fixed = sizeof(float) * (4 * kHeadMaxStages + 16 + static_cast<size_t>(T) * CV * 128);
-    const size_t stage = sizeof(float) * static_cast<size_t>(kHeadRows) * CV * 128;
+    const size_t stage = sizeof(float) * static_cast<size_t>(kMlaWarps * head_rb(CV, T)) * CV * 128;
     // As many stages as fit in about half an SM's shared memory (two CTAs per SM), 2 to 4.
     const int stages = std::max(2, std::min(kHeadMaxStages,
                                             static_cast<int>((100 * 1024 - static_cast<int64_t>(fixed)) /
