@@ -35,13 +35,17 @@
  *                        the repacked slab against the GEMV of the E4M3 source within the
  *                        quantization bound
  *
- *   memq_oracle_mla_*    library einsum / softmax of the same operands, one-hot and constant
- *                        inputs (attention over identical rows returns the row; a one-slot
- *                        gather returns that slot), softmax shift invariance
+ *   memq_oracle_mla_*    library einsum / softmax of the same operands; closed forms
+ *                        (attention over identical rows returns the row, a one-slot gather
+ *                        returns that slot, scale 0 gives the mean of the rows); the rope term
+ *                        equals the same problem on concatenated queries and rows; a zeroed
+ *                        head's weights give that head a zero output
  *
- * Also from the pages (SURVEY's "next" rows): q8_fuse_gate.rs, `main` -- the silu(gate)*up ->
- * q8_1 activation producer named for the 1536-wide expert site; gemv_e4m3_bench.rs, module doc
- * "QUESTION" -- the ship path that dequantizes FP8 weights to a Q8_0 slab at load ("ARM B'").
+ * Also from the pages: q8_fuse_gate.rs, `main` -- the silu(gate)*up -> q8_1 activation producer
+ * named for the 1536-wide expert site; gemv_e4m3_bench.rs, module doc "QUESTION" -- the ship
+ * path that dequantizes FP8 weights to a Q8_0 slab at load ("ARM B'"); mla_decode_arm_gate.rs,
+ * module doc and `main` -- the t <= 8 MLA decode attention kernels absorb_q, decompress_v and
+ * attn_gathered.
  */
 #include <math.h>
 #include <stddef.h>
