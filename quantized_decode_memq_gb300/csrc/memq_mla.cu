@@ -194,8 +194,6 @@ __global__ void __launch_bounds__(kHeadThreads)
         for (int b = 0; b < kHeadRB; ++b)
 #pragma unroll
             for (int c = 0; c < CV; ++c) wv[b][c] = wr[b * (cols / 4) + lane + 32 * c];
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[slot])) : "memory");
         float p[NV];
 #pragma unroll
         for (int tt = 0; tt < T; ++tt) {
@@ -215,6 +213,11 @@ __global__ void __launch_bounds__(kHeadThreads)
                 p[b * T + tt] = s;
             }
         }
+        // Release the stage only now: every lane has used (so received) the weights it loaded
+        // from it.  An arrival right after issuing the loads would let the next bulk copy
+        // overwrite the stage while loads are still in flight.
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[slot])) : "memory");
         const float sum = xor_reduce_scatter<NV>(p, lane);
         if (writer && my_t < t && i + my_b < r1)
             a.out[(static_cast<int64_t>(my_t) * nh + h) * rows + i + my_b] = sum;

@@ -236,3 +236,19 @@ def test_mla_kernels_in_a_cuda_graph(memq):
     s.synchronize()
     for a, b in zip(outs, eager):
         assert_bits_equal(a, b, "graph replay")
+
+
+@pytest.mark.parametrize("which", ["absorb", "decompress"])
+def test_head_gemv_stage_reuse_repeatable(memq, which):
+    """A stage of the weight ring is released only after its weights have been used: released
+    earlier, the next bulk copy could overwrite loads still in flight and change a few outputs
+    from one launch to the next.  40 launches over several splits, each bit-identical to split 1."""
+    t = 8
+    x, w = synth.mla_absorb_inputs(t) if which == "absorb" else synth.mla_decompress_inputs(t)
+    fn = memq.memq_mla_absorb_q if which == "absorb" else memq.memq_mla_decompress_v
+    dx, dw = to_dev(x), to_dev(w)
+    base = fn(dx, dw, split=1)
+    outs = [fn(dx, dw, split=s) for s in (7, 3, 0, 5) * 10]
+    torch.cuda.synchronize()
+    for k, got in enumerate(outs):
+        assert_bits_equal(got, base, f"launch {k}")
