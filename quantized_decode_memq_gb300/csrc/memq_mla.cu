@@ -33,9 +33,10 @@
 // depend on H, which is the entry point's `split` (H = 8 / split), so the split twins are
 // bit-identical.  No global scratch: the partials live in shared memory.
 //
-// absorb_q / decompress_v use programmatic dependent launch (the constant weights stream while
-// the preceding grid finishes; x is read after griddepcontrol.wait, through L2).  attn_gathered
-// is a plain stream-ordered launch: every one of its inputs may come from the preceding grid.
+// All three use programmatic dependent launch.  absorb_q / decompress_v stream their constant
+// weights while the preceding grid finishes and read x after griddepcontrol.wait, through L2;
+// attn_gathered only sets up its barriers before the wait (every one of its inputs may come from
+// the preceding grid) and then reads through L2 and the async proxy.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -270,6 +271,7 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
     constexpr int NV = 2 * H;                                     // dots per warp per chunk
     constexpr int kLaneShift = 5 - ilog2(NV);
     extern __shared__ __align__(16) float sm[];
+    griddep_launch_dependents();
     const int d_rope = a.d_rope, n_slots = a.n_slots, S = a.stages, nh = a.nh;
     const int row_len = kv_rank + d_rope;
     const int row_pad = (row_len + 3) & ~3;  // float4-aligned rows in shared memory
@@ -302,11 +304,14 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
         for (int s = 0; s < kMaxStages; ++s) mbar_init(&bars[s], 1);
         mbar_init_fence();
     }
+    // Every input may be the preceding grid's output (the absorbed query, the top-k indices,
+    // the newest cache row): wait for it, then read through L2 (or the async proxy) only.
+    griddep_wait();
     for (int i = tid; i < H * row_len; i += kMlaThreads) {
         const int hh = i / row_len, k = i - hh * row_len;
         const int64_t th = static_cast<int64_t>(tt) * nh + min(h0 + hh, nh - 1);
-        sq[hh * row_pad + k] = k < kv_rank ? __ldg(a.q_lat + th * kv_rank + k)
-                                           : __ldg(a.q_pe + th * d_rope + (k - kv_rank));
+        sq[hh * row_pad + k] = k < kv_rank ? __ldcg(a.q_lat + th * kv_rank + k)
+                                           : __ldcg(a.q_pe + th * d_rope + (k - kv_rank));
     }
     if (tid < H) {
         smm[tid] = -INFINITY;
@@ -334,7 +339,7 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
     const int my_row = warp * kRowsPerWarp + lane;  // meaningful for lane < kRowsPerWarp
     int issued = 0;
     int nidx = 0;
-    if (bulk && lane < kRowsPerWarp && j_begin + my_row < j_end) nidx = __ldg(ix + j_begin + my_row);
+    if (bulk && lane < kRowsPerWarp && j_begin + my_row < j_end) nidx = __ldcg(ix + j_begin + my_row);
     auto issue_next = [&]() {  // every warp, in step; chunk `issued` into stage issued % S
         if (issued >= nchunks) return;
         const int j0 = j_begin + issued * kRowsC;
@@ -346,7 +351,7 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
                            a.cache + static_cast<int64_t>(nidx) * row_len, row_bytes, bar);
         ++issued;
         const int jn = j0 + kRowsC + my_row;
-        if (lane < kRowsPerWarp && issued < nchunks && jn < j_end) nidx = __ldg(ix + jn);
+        if (lane < kRowsPerWarp && issued < nchunks && jn < j_end) nidx = __ldcg(ix + jn);
     };
     if (bulk)
         for (int c = 0; c < S - 1; ++c) issue_next();
@@ -373,7 +378,7 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
             float *dst = ring;
             for (int i = tid; i < nj * row_len; i += kMlaThreads) {
                 const int j = i / row_len, k = i - j * row_len;
-                dst[j * row_pad + k] = __ldg(a.cache + static_cast<int64_t>(__ldg(ix + j0 + j)) * row_len + k);
+                dst[j * row_pad + k] = __ldcg(a.cache + static_cast<int64_t>(__ldcg(ix + j0 + j)) * row_len + k);
             }
             __syncthreads();
         }
@@ -646,8 +651,19 @@ int launch_attn(const AttnArgs &args0, int t, cudaStream_t st) {
     if (!allow_max_smem(reinterpret_cast<const void *>(attn_gathered_kernel<KV, H>), attr_done))
         return MEMQ_ERR_LAUNCH;
     const unsigned groups = static_cast<unsigned>(t) * static_cast<unsigned>((args.nh + H - 1) / H);
-    attn_gathered_kernel<KV, H><<<groups * kParts, kMlaThreads, smem, st>>>(args);
-    return cudaGetLastError() == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+    // Programmatic dependent launch (the cluster shape comes from the kernel's attribute).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(groups * kParts);
+    cfg.blockDim = dim3(kMlaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_gathered_kernel<KV, H>, args) == cudaSuccess ? MEMQ_OK
+                                                                                      : MEMQ_ERR_LAUNCH;
 }
 
 template <int KV>

@@ -252,3 +252,33 @@ def test_head_gemv_stage_reuse_repeatable(memq, which):
     torch.cuda.synchronize()
     for k, got in enumerate(outs):
         assert_bits_equal(got, base, f"launch {k}")
+
+
+def test_mla_chain_hand_offs(memq):
+    """absorb_q -> attn_gathered -> decompress_v back to back (each kernel's output is the next
+    one's input, every launch overlapping its predecessor's end through programmatic dependent
+    launch): 10 chains on fresh queries, each bit-identical to the same three calls separated by
+    device synchronizes."""
+    t = 2
+    _, wk = synth.mla_absorb_inputs(t)
+    _, wv = synth.mla_decompress_inputs(t)
+    _, _, cache, idx = synth.mla_attn_inputs(t, 32768)
+    dwk, dwv, dc, di = to_dev(wk), to_dev(wv), to_dev(cache), to_dev(idx)
+    qs = [to_dev(synth.mla_randf(t * 64 * 256, 0x8300 + i).reshape(t, 64, 256)) for i in range(10)]
+    q_lat = torch.empty((t, 64, 512), dtype=torch.float32, device="cuda")
+    o_lat = torch.empty((t, 64, 512), dtype=torch.float32, device="cuda")
+    outs = []
+    for q in qs:
+        memq.memq_mla_absorb_q(q, dwk, out=q_lat)
+        memq.memq_mla_attn_gathered(q_lat, None, dc, di, synth.MLA_SCALE, out=o_lat)
+        outs.append(memq.memq_mla_decompress_v(o_lat, dwv))
+    torch.cuda.synchronize()
+    for q, got in zip(qs, outs):
+        a = memq.memq_mla_absorb_q(q, dwk)
+        torch.cuda.synchronize()
+        b = memq.memq_mla_attn_gathered(a, None, dc, di, synth.MLA_SCALE)
+        torch.cuda.synchronize()
+        ref = memq.memq_mla_decompress_v(b, dwv)
+        torch.cuda.synchronize()
+        assert_bits_equal(got, ref, "chained MLA step")
+    assert memq.memq_device_fault() == 0
