@@ -700,7 +700,21 @@ class MlaStep:
         self.memq, self.kernel, self.t, self.split = memq, kernel, t, split
         nh, kvr = synth.MLA_NH, synth.MLA_KV_RANK
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
-        if kernel == "attn":
+        if kernel == "step":
+            # the whole attention step: absorb_q -> attn_gathered -> decompress_v, each kernel's
+            # output the next one's input
+            q_nope, wk = synth.mla_absorb_inputs(t)
+            _, wv = synth.mla_decompress_inputs(t)
+            _, _, cache, idx = synth.mla_attn_inputs(t, kv)
+            self.q_nope, self.wk, self.wv = dev(q_nope), dev(wk), dev(wv)
+            self.cache, self.idx = dev(cache), dev(idx)
+            self.q_lat = torch.empty((t, nh, kvr), dtype=torch.float32, device=device)
+            self.o_lat = torch.empty((t, nh, kvr), dtype=torch.float32, device=device)
+            self.out = torch.empty((t, nh, wv.shape[1]), dtype=torch.float32, device=device)
+            n_slots = idx.shape[1]
+            self.step_bytes = wk.nbytes + wv.nbytes + t * n_slots * kvr * 4
+            self.flops = 2 * t * (wk.size + wv.size) + t * nh * n_slots * (2 * kvr + 2 * kvr)
+        elif kernel == "attn":
             q_lat, _, cache, idx = synth.mla_attn_inputs(t, kv)
             self.args = (dev(q_lat), None, dev(cache), dev(idx), synth.MLA_SCALE)
             n_slots = idx.shape[1]
@@ -729,7 +743,23 @@ class MlaStep:
         import torch
         torch.sum(self.scrub, dim=0, out=self.scrub_out)
 
+    def chain_part(self, k):
+        """Kernel k of the whole step (0 absorb_q, 1 attn_gathered, 2 decompress_v)."""
+        m = self.memq
+        if k == 0:
+            m.memq_mla_absorb_q(self.q_nope, self.wk, out=self.q_lat, split=self.split)
+        elif k == 1:
+            from quantized_decode_memq_gb300 import synth
+            m.memq_mla_attn_gathered(self.q_lat, None, self.cache, self.idx, synth.MLA_SCALE,
+                                     out=self.o_lat, split=self.split)
+        else:
+            m.memq_mla_decompress_v(self.o_lat, self.wv, out=self.out, split=self.split)
+
     def step(self, i):
+        if self.kernel == "step":
+            for k in range(3):
+                self.chain_part(k)
+            return
         fn = {"attn": self.memq.memq_mla_attn_gathered, "absorb": self.memq.memq_mla_absorb_q,
               "decompress": self.memq.memq_mla_decompress_v}[self.kernel]
         args = self.args if self.kernel == "attn" else (self.args[0], self.w[i % self.copies])
@@ -745,7 +775,7 @@ def run_mla(args, world, rank, local, dev):
     build.build()
     parts = args.workload.split("_")
     kernel, t = parts[1], int(parts[2][1:])
-    kv = int(parts[3][2:]) if kernel == "attn" else 0
+    kv = int(parts[3][2:]) if kernel in ("attn", "step") else 0
     wl = MlaStep(kernel, t, kv, dev, split=args.split)
     stream = torch.cuda.Stream(device=dev)
     K, W = min(args.steps, 400), min(args.warmup, 50)  # one scrub + one launch per sample
@@ -770,13 +800,30 @@ def run_mla(args, world, rank, local, dev):
     clocks = sampler.stop()
     per = [a.elapsed_time(b) / 1e3 for a, b in evs]
     t_launch, _ = aggregate(float(np.mean(per)), 1.0)
-    if kernel == "attn":
+    if kernel in ("attn", "step"):
         achieved = wl.flops / t_launch / 1e12
         peak = F32_FMA_TFLOPS
         roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": profiled_traffic(args.workload, "mla_traffic.json"),
                 "peak_kind": "derived: 152 SMs x 128 f32 FMA/clk x 2 FLOP x 2.07 GHz"}
+        if kernel == "step":
+            # the same kernels one at a time (each after its own scrub), for the overlap gain
+            iso = []
+            for k in range(3):
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(20)]
+                with torch.cuda.stream(stream):
+                    for a_, b_ in ev:
+                        wl.flush()
+                        a_.record(stream)
+                        wl.chain_part(k)
+                        b_.record(stream)
+                stream.synchronize()
+                iso.append(float(np.mean([a_.elapsed_time(b_) for a_, b_ in ev])) * 1e3)
+            roof["isolated_us"] = {"absorb_q": round(iso[0], 2), "attn_gathered": round(iso[1], 2),
+                                   "decompress_v": round(iso[2], 2), "sum": round(sum(iso), 2)}
+            roof["traffic"] = None
     else:
         peak, peak_kind = measured_peak_hbm()
         achieved = wl.step_bytes / t_launch / 1e9
@@ -790,8 +837,11 @@ def run_mla(args, world, rank, local, dev):
         roof["loop_frac"] = round(wl.step_bytes / loop_s / 1e9 / peak, 4)
     desc = {"absorb": f"mla_absorb_q t={t}: 64 heads x (512 x 256) f32 weights",
             "decompress": f"mla_decompress_v t={t}: 64 heads x (256 x 512) f32 weights",
-            "attn": f"mla_attn_gathered t={t}: 64 heads, kv_rank 512, 2048 slots from {kv} rows"}
-    line = {"metric": "MLA decode kernel time per launch (L2 scrubbed before each)",
+            "attn": f"mla_attn_gathered t={t}: 64 heads, kv_rank 512, 2048 slots from {kv} rows",
+            "step": f"MLA attention step t={t}: absorb_q -> attn_gathered (2048 slots from {kv} "
+                    f"rows) -> decompress_v, back to back"}
+    line = {"metric": ("MLA attention step time (L2 scrubbed before each)" if kernel == "step" else
+                       "MLA decode kernel time per launch (L2 scrubbed before each)"),
             "value": round(t_launch * 1e6, 3), "unit": "us", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": t_launch * 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -799,9 +849,16 @@ def run_mla(args, world, rank, local, dev):
                        "step_bytes": wl.step_bytes, "flops": wl.flops,
                        "timing": "one launch per sample after a 256 MB scrub read, CUDA events",
                        "min_us": round(min(per) * 1e6, 3)},
-            "roofline": roof, "gpu_launches": K, "clocks": clocks}
+            "roofline": roof, "gpu_launches": K * (3 if kernel == "step" else 1), "clocks": clocks}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_mla(kernel, t, kv, min(args.cpu_seconds, 10.0))
+        if kernel == "step":
+            cb = [cpu_baseline_mla(k, t, kv, min(args.cpu_seconds, 10.0) / 3)
+                  for k in ("absorb", "attn", "decompress")]
+            line["cpu_baseline"] = dict(cb[1], value=round(sum(c["value"] for c in cb), 1),
+                                        sample="sum of the three kernels' oracle samples: " +
+                                               "; ".join(c["sample"] for c in cb))
+        else:
+            line["cpu_baseline"] = cpu_baseline_mla(kernel, t, kv, min(args.cpu_seconds, 10.0))
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -1157,7 +1214,8 @@ def main(argv=None):
                     help="one of %s, or <e4m3|blk128|q8_0>_<out_f>x<in_f>_m<m>, c3, "
                          "producer_<ncols>x<rows>, silu_<ncols>x<rows>, "
                          "repack_<e4m3|blk128>_<out_f>x<in_f>, stack<layers>, "
-                         "mla_<absorb|decompress>_t<t>, mla_attn_t<t>_kv<kv>" % sorted(WORKLOADS))
+                         "mla_<absorb|decompress>_t<t>, mla_attn_t<t>_kv<kv>, mla_step_t<t>_kv<kv>"
+                         % sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
