@@ -19,16 +19,19 @@
 // head_gemv_kernel (absorb_q, decompress_v): a per-head batched GEMV over f32 weights (33.5 MB
 // at the page geometry, read once: HBM-bound).  CTA (h, part) takes rows [part*rows/split,
 // (part+1)*rows/split) of head h, contiguous in memory; a producer warp streams them into a
-// shared-memory ring by bulk copies while 8 consumer warps take 2 rows of each stage against
-// the t activation rows of head h (in shared memory).  The default split fills one wave of
-// resident CTAs.
+// shared-memory ring by bulk copies while 8 consumer warps take 2 rows of each stage (4 for
+// t >= 4 on rows of <= 256 floats) against the t activation rows of head h (in shared memory);
+// a warp releases a stage only after using what it loaded from it.  The default split fills one
+// wave of resident CTAs.
 //
 // attn_gathered_kernel: every head of query row t gathers the same n_slots rows, so a CTA
 // serves a group of H heads from one staged copy of them, and a cluster of 8 CTAs splits the
 // slots into 8 fixed ranges.  The gathered rows stream into a ring of shared-memory stages by
 // bulk copies (one per row, completing on an mbarrier per stage; each warp issues 2 rows of a
-// chunk), issued S - 1 chunks ahead of the compute.  Each CTA runs an online softmax over its range (running max m, sum l, outputs
-// rescaled by exp(m_old - m_new) per chunk of 16 rows); the 8 partials are merged through
+// chunk), issued S - 1 chunks ahead of the compute.  Each CTA runs an online softmax over its
+// range (running max m, sum l, outputs rescaled by exp(m_old - m_new) per chunk of 16 rows);
+// one warp per head runs the softmax step, every thread accumulates two output dims of every
+// head of the group.  The 8 partials are merged through
 // distributed shared memory in part order.  The slot ranges, chunks and merge order do not
 // depend on H, which is the entry point's `split` (H = 8 / split), so the split twins are
 // bit-identical.  No global scratch: the partials live in shared memory.
@@ -578,13 +581,19 @@ int launch_head(const float *x, const float *w, float *out, int t, int nh, int r
     static std::atomic<uint64_t> attr_done{0};
     if (!allow_max_smem(reinterpret_cast<const void *>(kern), attr_done)) return MEMQ_ERR_LAUNCH;
     if (split == 0) {
-        // one wave of resident CTAs over all heads
+        // one wave of resident CTAs over all heads (CTAs per SM queried once per device)
+        static std::atomic<int> occ_cache[kMaxDevices];
         const int sms = sm_count();
-        int occ = 0;
-        if (sms <= 0 || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kHeadThreads, smem) !=
-                            cudaSuccess)
-            return MEMQ_ERR_LAUNCH;
-        split = static_cast<int>(std::max<int64_t>(1, static_cast<int64_t>(std::max(occ, 1)) * sms / nh));
+        int dev = 0, occ = 0;
+        if (sms <= 0 || cudaGetDevice(&dev) != cudaSuccess) return MEMQ_ERR_LAUNCH;
+        if (dev < kMaxDevices) occ = occ_cache[dev].load(std::memory_order_relaxed);
+        if (occ <= 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kHeadThreads, smem) != cudaSuccess)
+                return MEMQ_ERR_LAUNCH;
+            occ = std::max(occ, 1);
+            if (dev < kMaxDevices) occ_cache[dev].store(occ, std::memory_order_relaxed);
+        }
+        split = static_cast<int>(std::max<int64_t>(1, static_cast<int64_t>(occ) * sms / nh));
     }
     if (split > rows) split = rows;
     if (static_cast<int64_t>(nh) * split > kMaxGrid) split = static_cast<int>(kMaxGrid / nh);
