@@ -9,20 +9,26 @@
  *      memq_gemv_q8_0         ggml block_q8_0 weights (f16 scale + 32 int8)     (1.0625 B/weight)
  *
  * Around them: the fused decode steps memq_rmsnorm_q8_1_gemv_* (stage 1 inside the GEMV
- * launch), the silu(gate) * up -> q8_1 producer memq_silu_mul_q8_1, and the load-time repack of
- * E4M3 weights into a Q8_0 slab, memq_repack_e4m3[_blk128]_q8_0.
+ * launch), the grouped GEMVs memq_gemv_*_group, the silu(gate) * up -> q8_1 producer
+ * memq_silu_mul_q8_1, the load-time repack of E4M3 weights into a Q8_0 slab,
+ * memq_repack_e4m3[_blk128]_q8_0, and the t <= 8 MLA decode attention kernels memq_mla_absorb_q,
+ * memq_mla_attn_gathered and memq_mla_decompress_v.
  *
  * The operations are the ones defined on the memra-engine 0.125.0 source pages:
  * q8_fuse_gate.rs (module doc: the `rms_norm` -> `quantize_q8_1` chain and the fused
- * `rms_norm_zq8_f32` producer) and gemv_e4m3_bench.rs (module doc, "THE COMPARISON" and "THE
- * BLOCK-128 ARM", and the container generators `synth_e4m3`, `synth_blk_grid`, `synth_q8_0`).
+ * `rms_norm_zq8_f32` producer), gemv_e4m3_bench.rs (module doc, "THE COMPARISON" and "THE
+ * BLOCK-128 ARM", and the container generators `synth_e4m3`, `synth_blk_grid`, `synth_q8_0`)
+ * and mla_decode_arm_gate.rs (module doc and `main`: the MLA kernels and their split twins).
  *
  * Conventions for every entry point:
  *   - Pointers named "device" must be device-accessible memory of the current CUDA device
  *     (cudaMalloc / torch CUDA tensors).  The caller owns every buffer; the library never
  *     allocates, frees or keeps a pointer after the call returns.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue work;
- *     they never synchronize.  Results are ready when the stream reaches the launch.
+ *     they never synchronize.  Results are ready when the stream reaches the launch.  Launches
+ *     may begin before the preceding work on the stream has finished (programmatic dependent
+ *     launch), but read nothing the stream wrote before that work is complete; callers see
+ *     plain stream order.
  *   - Arguments are validated on the host before anything is launched; on any error the call
  *     returns a nonzero memq_status and writes nothing.  A launch failure returns
  *     MEMQ_ERR_LAUNCH.  Device-side waits are bounded: if one ever expires, the kernel records
