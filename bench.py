@@ -49,7 +49,7 @@ WORKLOADS = {
     "e4m3_17408x5120_m1": ("e4m3", 17408, 5120, 1, 4),
     "q8_0_17408x5120_m1": ("q8_0", 17408, 5120, 1, 4),
 }
-DEFAULT_WORKLOAD = "q8_0_4096x4096_m1"
+DEFAULT_WORKLOAD = "c3"
 L2_BYTES = 129 * 2 ** 20
 # f32 FMA peak of the CUDA cores: 152 SMs x 128 FMA / clock x 2 FLOP x 2.07 GHz (maximum clock)
 F32_FMA_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 2)
@@ -621,72 +621,414 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_c3(args, world, rank, local, dev, out_f=17408, in_f=5120, rounds=15):
-    """The three containers on the same 17408 x 5120 shape at m = 1, interleaved: per arm a CUDA
-    graph of back-to-back GEMV launches over its own rotated weight copies; the graphs are
-    replayed in turn (E4M3, block-128, Q8_0) for `rounds` rounds, each replay timed with CUDA
-    events; per arm the median launch period.  Reports the Q8_0 : E4M3 time ratio next to the
-    1.0625 byte ratio."""
+C3_OUT_F, C3_IN_F = 17408, 5120
+ARMS = ("e4m3", "blk", "q8_0")
+ARM_NAMES = {"e4m3": "E4M3 (per-tensor scale)", "blk": "E4M3 block-128", "q8_0": "Q8_0"}
+NOMINAL_HBM_GBS = 8000.0
+
+
+def _median_event_us(pairs, div=1):
+    return float(np.median([a.elapsed_time(b) * 1e3 / div for a, b in pairs]))
+
+
+def time_isolated(fn, n, stream):
+    """Median device time of n individually event-bracketed launches of fn(i) (rotated copies),
+    each queued behind a GPU-side sleep so that no host latency lands between its events."""
     import torch
-    from quantized_decode_memq_gb300 import build
-    build.build()
+    res = []
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(200000)
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+            stream.synchronize()
+            res.append(a.elapsed_time(b) * 1e3)
+    return float(np.median(res[2:] if len(res) > 6 else res))
+
+
+class L2Scrub:
+    """Evicts L2 with this library's own RMSNorm -> q8_1 kernel over a 256 MB activation: it reads
+    256 MB and writes 256 MB of z plus 64 MB of q8_1 codes, more than twice the 129 MB L2 each
+    way (as mla_decode_arm_gate.rs scrubs with an rms_norm pass before every timed launch)."""
+
+    ROWS, NCOLS = 8192, 8192
+
+    def __init__(self, device):
+        import torch
+        import quantized_decode_memq_gb300 as memq
+        self.memq = memq
+        self.x = torch.ones((self.ROWS, self.NCOLS), dtype=torch.float32, device=device)
+        self.w = torch.ones(self.NCOLS, dtype=torch.float32, device=device)
+        self.z = torch.empty_like(self.x)
+        self.qs = torch.empty((self.ROWS, self.NCOLS), dtype=torch.int8, device=device)
+        self.d = torch.empty((self.ROWS, self.NCOLS // 32), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.memq.memq_rmsnorm_q8_1(self.x, self.w, 1e-6, qs=self.qs, d=self.d, z=self.z)
+
+
+def time_isolated_scrubbed(fn, scrub, n, stream):
+    """Median device time of n event-bracketed launches of fn(0) -- always the same weights --
+    each right after an L2 scrub: the cross-check that the rotated copies leave every launch as
+    cold as a scrubbed one."""
+    import torch
+    res = []
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            scrub()
+            torch.cuda._sleep(200000)
+            a.record(stream)
+            fn(0)
+            b.record(stream)
+            stream.synchronize()
+            res.append(a.elapsed_time(b) * 1e3)
+    return float(np.median(res[2:] if len(res) > 6 else res))
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def affinity_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_arms(arms, seconds):
+    """The f64 oracle (producer + each arm's GEMV on a bounded row sample of the same shape) on
+    the host cores: single-threaded, and with the rows split over every core of the process's
+    affinity mask (one thread per core calling the unchanged oracle on its row range; the
+    oracle's C loops run without the interpreter lock).  GB/s of the whole three-arm step,
+    scaled from the sample's bytes; median of 3 timings each."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    oracle.build()
+    ncores = affinity_cores()
+    legs = []
+    inputs = {kind: _oracle_inputs(kind, wl.out_f, wl.in_f, 1) for kind, wl in arms.items()}
+    for cores in (1, ncores):
+        per_arm = {}
+        for kind, wl in arms.items():
+            out_f, in_f = wl.out_f, wl.in_f
+            x, wn, w, aux = inputs[kind]
+            _, d, qs, _ = oracle.rmsnorm_q8_1(x, wn, 1e-6)
+            # rows per timing: sized from a calibration so the three arms x 3 repeats x 2 legs
+            # take about `seconds`
+            probe = np.arange(min(out_f, 64))
+            t0 = time.perf_counter()
+            _oracle_gemv(oracle, kind, w, aux, qs, d, in_f, probe)
+            per_row = (time.perf_counter() - t0) / len(probe)
+            nrows = int(max(cores, min(out_f, seconds / 18.0 * cores / max(per_row, 1e-9))))
+            rows = np.arange(nrows)
+            chunks = np.array_split(rows, cores)
+            times = []
+            for _ in range(3):
+                t0 = time.perf_counter()
+                oracle.rmsnorm_q8_1(x, wn, 1e-6)
+                if cores == 1:
+                    _oracle_gemv(oracle, kind, w, aux, qs, d, in_f, rows)
+                else:
+                    with ThreadPoolExecutor(cores) as ex:
+                        list(ex.map(lambda r: _oracle_gemv(oracle, kind, w, aux, qs, d, in_f, r),
+                                    chunks))
+                times.append(time.perf_counter() - t0)
+            t = float(np.median(times))
+            # whole-arm time: the sampled rows scaled to out_f (the producer is counted once)
+            per_arm[kind] = {"rows_sampled": nrows, "s_per_launch": t * out_f / nrows}
+        step_s = sum(v["s_per_launch"] for v in per_arm.values())
+        in_f = next(iter(arms.values())).in_f
+        step_bytes = sum(wl.gemv_bytes for wl in arms.values()) + producer_bytes(1, in_f)
+        legs.append({"cores": cores, "value": round(step_bytes / step_s / 1e9, 5), "unit": "GB/s",
+                     "ms_per_step": round(step_s * 1e3, 1),
+                     "arms": {k: round(v["s_per_launch"] * 1e3, 2) for k, v in per_arm.items()},
+                     "rows_sampled": {k: v["rows_sampled"] for k, v in per_arm.items()}})
+    best = legs[-1]
+    return {"value": best["value"], "unit": "GB/s", "cores": best["cores"], "kind": "oracle",
+            "sample": "f64 C oracle: RMSNorm->q8_1 of the activation row, then each arm's GEMV on "
+                      "a bounded sample of its output rows (the first rows), scaled to the whole "
+                      "step; median of 3 timings", "legs": legs, "cpu_model": cpu_model(),
+            "host_cpus": os.cpu_count()}
+
+
+def _oracle_gemv(oracle, kind, w, aux, qs, d, in_f, rows):
+    if kind == "q8_0":
+        return oracle.gemv_q8_0(w, in_f, qs, d, rows=rows)
+    if kind == "blk":
+        return oracle.gemv_e4m3_blk128(w, aux, qs, d, rows=rows)
+    return oracle.gemv_e4m3(w, aux, qs, d, rows=rows)
+
+
+def run_c3(args, world, rank, local, dev, out_f=C3_OUT_F, in_f=C3_IN_F):
+    """The default workload: the E4M3, block-128 and Q8_0 GEMVs on the 17408 x 5120 projection at
+    m = 1, interleaved (gemv_e4m3_bench.rs, "THE BLOCK-128 ARM" and "PROTOCOL": all arms inside
+    one iteration, each on its own rotated weight copies, medians of per-iteration times).
+
+    A step: the RMSNorm -> q8_1 producer on the 5120-wide row, then for each arm -- in an order
+    that rotates every step -- a CUDA graph of back-to-back launches over that arm's rotated
+    copies (each launch reads weights no launch since has touched: the copies of one arm exceed
+    twice the L2), with CUDA events between the arms.  The K timed steps are queued behind a GPU
+    sleep so host launch latency never lands inside the region."""
+    import torch
+    stream = torch.cuda.Stream(device=dev)
     arms = {}
-    for kind in ("e4m3", "blk", "q8_0"):
+    for kind in ARMS:
         copies = max(4, -(-2 * L2_BYTES // gemv_bytes(kind, out_f, in_f, 1)))
         arms[kind] = DecodeStep(kind, out_f, in_f, 1, copies, dev, fused=False)
-    stream = torch.cuda.Stream(device=dev)
-    graphs, n = {}, {}
+    lead = arms["e4m3"]
+    for wl in arms.values():  # one activation shared by the three arms
+        wl.x, wl.wn, wl.qs, wl.d = lead.x, lead.wn, lead.qs, lead.d
+    n = {k: 4 * wl.copies for k, wl in arms.items()}
     with torch.cuda.stream(stream):
-        for kind, wl in arms.items():
-            wl.producer()
+        lead.producer()
+        for wl in arms.values():
             for i in range(wl.copies):
                 wl.gemv(i)
-            n[kind] = 8 * wl.copies
-            graphs[kind] = capture(wl.gemv, n[kind], stream)
-            for _ in range(max(1, args.warmup // n[kind] + 1)):
-                graphs[kind].replay()
     stream.synchronize()
-    times = {k: [] for k in arms}
+    with torch.cuda.stream(stream):
+        graphs = {k: capture(wl.gemv, n[k], stream) for k, wl in arms.items()}
+        g_prod = capture(lambda i: lead.producer(), 1, stream)
+    stream.synchronize()
+
+    def run_steps(K, record):
+        evs = []
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(2_000_000)  # the host queues ahead while the GPU sleeps
+            for s in range(K):
+                order = ARMS[s % 3:] + ARMS[:s % 3]
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(5)] if record else None
+                if record:
+                    e[0].record(stream)
+                g_prod.replay()
+                if record:
+                    e[1].record(stream)
+                for j, kind in enumerate(order):
+                    graphs[kind].replay()
+                    if record:
+                        e[2 + j].record(stream)
+                if record:
+                    evs.append((order, e))
+        return evs
+
+    K, W = args.steps, args.warmup
+    run_steps(W, False)
+    stream.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
-    for _ in range(rounds):
-        for kind in arms:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                graphs[kind].replay()
-                e1.record(stream)
-            stream.synchronize()
-            times[kind].append(e0.elapsed_time(e1) * 1e3 / n[kind])
+    barrier()
+    torch.cuda.synchronize()
+    evs = run_steps(K, True)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier()
     clocks = sampler.stop()
+    elapsed = evs[0][1][0].elapsed_time(evs[-1][1][4]) / 1e3
+    per_arm = {k: [] for k in ARMS}
+    for order, e in evs:
+        for j, kind in enumerate(order):
+            per_arm[kind].append(e[1 + j].elapsed_time(e[2 + j]) * 1e3 / n[kind])
     peak, peak_kind = measured_peak_hbm()
+    scrub = L2Scrub(dev)
     res = {}
     for kind, wl in arms.items():
-        us = float(np.median(times[kind]))
-        gbs = wl.gemv_bytes / us / 1e3
-        res[kind] = {"us": round(us, 3), "gb_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                     "bytes": wl.gemv_bytes, "spread_us": [round(min(times[kind]), 3),
-                                                           round(max(times[kind]), 3)]}
-    tot_bytes = sum(wl.gemv_bytes for wl in arms.values())
-    tot_us = sum(r["us"] for r in res.values())
-    line = {"metric": METRIC, "value": round(tot_bytes / tot_us / 1e3, 2), "unit": "GB/s",
-            "n_gpus": world, "steps": rounds * sum(n.values()), "warmup": args.warmup,
-            "ms_per_step": tot_us / 3 / 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8+int8", "data": "synthetic",
-            "config": {"workload": f"c3: E4M3, block-128 and Q8_0 GEMV {out_f}x{in_f} m=1, "
-                                   f"interleaved arms, rotated weight copies (DRAM-cold)",
-                       "timing": "per arm: median over rounds of the launch period of a graph "
-                                 "of back-to-back launches"},
-            "arms": res,
-            "q8_0_to_e4m3_time_ratio": round(res["q8_0"]["us"] / res["e4m3"]["us"], 4),
-            "q8_0_to_blk128_time_ratio": round(res["q8_0"]["us"] / res["blk"]["us"], 4),
-            "blk128_to_e4m3_time_ratio": round(res["blk"]["us"] / res["e4m3"]["us"], 4),
-            "byte_ratio": round(arms["q8_0"].gemv_bytes / arms["e4m3"].gemv_bytes, 4),
-            "peak": {"hbm_gbs": peak, "source": peak_kind},
-            "gpu_launches": rounds * sum(n.values()), "clocks": clocks}
+        # median period on this rank; across ranks the slowest replica's period with every
+        # replica's bytes (replicas only: no data-path collective)
+        us_max, bytes_all = aggregate(float(np.median(per_arm[kind])), float(wl.gemv_bytes))
+        us = float(np.median(per_arm[kind]))
+        iso = time_isolated(wl.gemv, max(8, 2 * wl.copies), stream)
+        iso_scrub = time_isolated_scrubbed(wl.gemv, scrub, 12, stream)
+        gbs = bytes_all / us_max / 1e3
+        res[kind] = {"arm": ARM_NAMES[kind], "us": round(us, 3), "gb_s": round(gbs, 1),
+                     "frac_of_measured_peak": round(gbs / peak, 4),
+                     "pct_of_nominal_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+                     "spread_us": [round(min(per_arm[kind]), 3), round(max(per_arm[kind]), 3)],
+                     "bytes_per_launch": wl.gemv_bytes, "weight_copies": wl.copies,
+                     "launches_per_step": n[kind],
+                     "isolated_launch_us": round(iso, 3),
+                     "isolated_gb_s": round(wl.gemv_bytes / iso / 1e3, 1),
+                     "isolated_after_l2_scrub_us": round(iso_scrub, 3),
+                     "rotation_vs_scrub": round(iso / iso_scrub, 4),
+                     "traffic": profiled_traffic(f"{kind if kind != 'blk' else 'blk128'}_{out_f}x{in_f}_m1")}
+    low = min(ARMS, key=lambda k: res[k]["gb_s"])
+    dom = max(ARMS, key=lambda k: res[k]["us"])
+    value = res[low]["gb_s"]
+    step_bytes = sum(wl.gemv_bytes * n[k] for k, wl in arms.items()) + producer_bytes(1, in_f)
+    t_max, tot_units = aggregate(elapsed, float(K * step_bytes))
+
+    e2e = time_e2e_arms(arms, lead, stream, steps=min(K, args.e2e_steps), graphs=True)
+    eager = time_e2e_arms(arms, lead, stream, steps=min(K, args.e2e_steps), graphs=False)
+    c2 = c2_step(args, dev, stream)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": t_max / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8+int8",
+        "data": "synthetic",
+        "config": {
+            "workload": f"c3: E4M3, block-128 and Q8_0 GEMV out_f={out_f} in_f={in_f} m=1 on one "
+                        f"q8_1 activation (RMSNorm->q8_1 of a {in_f}-wide row), arms interleaved "
+                        f"in a rotating order, each on its own rotated weight copies",
+            "value": "the lowest of the three arms' GB/s (each arm: algorithmic bytes per launch / "
+                     "median back-to-back launch period over the K steps)",
+            "timing": "per step: producer, then per arm a CUDA graph of back-to-back launches "
+                      "(programmatic dependent launch) bracketed by CUDA events; K steps queued "
+                      "behind a GPU sleep; ms_per_step = the whole region / K",
+            "l2": "inputs larger than L2: each arm rotates through copies totalling more than "
+                  "twice the 129 MB L2, so every launch reads its weights from DRAM",
+            "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+            "step_bytes": step_bytes,
+            "target": ">= 80% of the measured HBM peak per arm (back-to-back period); "
+                      "t_q8_0 / t_e4m3 within 0.02 of the 34/32 byte ratio",
+        },
+        "arms": res,
+        "step_gbs": round(tot_units / t_max / 1e9, 2),
+        "q8_0_to_e4m3_time_ratio": round(res["q8_0"]["us"] / res["e4m3"]["us"], 4),
+        "q8_0_to_blk128_time_ratio": round(res["q8_0"]["us"] / res["blk"]["us"], 4),
+        "blk128_to_e4m3_time_ratio": round(res["blk"]["us"] / res["e4m3"]["us"], 4),
+        "byte_ratio": round(arms["q8_0"].gemv_bytes / arms["e4m3"].gemv_bytes, 4),
+        "isolated_q8_0_to_e4m3_time_ratio": round(res["q8_0"]["isolated_launch_us"] /
+                                                  res["e4m3"]["isolated_launch_us"], 4),
+        "pct_of_peak": round(100.0 * value / peak, 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
+        "roofline": {
+            "bound": "hbm",
+            "achieved": res[dom]["gb_s"],
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(res[dom]["gb_s"] / peak, 4),
+            "traffic": res[dom]["traffic"],
+            "kernel": f"gemv_stream_kernel<{dom}, m=1> (the step's slowest arm)",
+            "bytes_per_launch": arms[dom].gemv_bytes,
+            "launch_us": res[dom]["us"],
+            "launch_timing": "median back-to-back launch period (CUDA events around a graph of "
+                             "launches on the launch stream)",
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                           else "fallback 6.8 TB/s",
+            "isolated_launch_us": res[dom]["isolated_launch_us"],
+        },
+        "e2e": e2e | {"eager": eager},
+        "c2_decode_step": c2,
+        "gpu_launches": K * (1 + sum(n.values())),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_arms(arms, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_e2e_arms(arms, lead, stream, steps, graphs):
+    """The public API with host buffers: per step the host->device copy of the activation row
+    (pinned), the producer, one launch of each arm, the device->host copy of the three outputs
+    and a host wait.  graphs=True replays one CUDA graph per rotated copy holding exactly those
+    calls; graphs=False issues them from Python."""
+    import torch
+    x_pin = torch.from_numpy(lead.x_host.copy()).pin_memory()
+    y_pin = {k: torch.empty(wl.y.shape, dtype=torch.float32).pin_memory() for k, wl in arms.items()}
+    h2d = x_pin.numel() * 4
+    d2h = sum(v.numel() * 4 for v in y_pin.values())
+    copies = min(wl.copies for wl in arms.values())
+
+    def one(i):
+        lead.x.copy_(x_pin, non_blocking=True)
+        lead.producer()
+        for k, wl in arms.items():
+            wl.gemv(i)
+            y_pin[k].copy_(wl.y, non_blocking=True)
+
+    run = one
+    if graphs:
+        gs = []
+        with torch.cuda.stream(stream):
+            for c in range(copies):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                    one(c)
+                gs.append(g)
+        run = lambda i: gs[i % len(gs)].replay()  # noqa: E731
+    step_bytes = sum(wl.gemv_bytes for wl in arms.values()) + producer_bytes(1, lead.in_f)
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            run(i)
+            stream.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            run(i)
+            stream.synchronize()
+        wall = time.perf_counter() - t0
+    t_max, units = aggregate(wall, float(steps * step_bytes))
+    return {"value": round(units / t_max / 1e9, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "us_per_step": round(t_max / steps * 1e6, 2),
+            "mode": ("per step: one replay of a CUDA graph holding the public-API calls "
+                     if graphs else "per step: the public-API calls issued from Python ")
+                    + "(H2D of x from pinned memory, producer, the three GEMVs, D2H of the "
+                      "three y), then a host wait; host wall clock"}
+
+
+def c2_step(args, dev, stream, copies=16, reps=64):
+    """The Q8_0 4096 x 4096 decode step (RMSNorm->q8_1 of a 4096-wide row, then the GEMV), 16
+    rotated weight copies: `reps` steps as one CUDA graph replay (queued behind a GPU sleep),
+    plus the GEMV's back-to-back period and its isolated launch."""
+    import torch
+    wl = DecodeStep("q8_0", 4096, 4096, 1, copies, dev, fused=False)
+    with torch.cuda.stream(stream):
+        for i in range(copies):
+            wl.step(i)
+        g = capture(wl.step, reps, stream)
+        g.replay()
+    stream.synchronize()
+    times = []
+    for _ in range(5):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(1_000_000)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        stream.synchronize()
+        times.append(a.elapsed_time(b) / 1e3 / reps)
+    step_s = float(np.median(times))
+    b2b = time_gemv_back_to_back(wl, stream, n=16 * copies)
+    iso = time_isolated(wl.gemv, 2 * copies, stream)
+    peak, _ = measured_peak_hbm()
+    return {"workload": "q8_0_4096x4096_m1: RMSNorm->q8_1 (1x4096) then Q8_0 GEMV 4096x4096, "
+                        "16 rotated copies",
+            "step_us": round(step_s * 1e6, 3),
+            "step_gbs": round(wl.step_bytes / step_s / 1e9, 2),
+            "gemv_back_to_back_us": round(b2b * 1e6, 3),
+            "gemv_gbs": round(wl.gemv_bytes / b2b / 1e9, 2),
+            "gemv_frac_of_measured_peak": round(wl.gemv_bytes / b2b / 1e9 / peak, 4),
+            "gemv_isolated_launch_us": round(iso, 3)}
 
 
 class MlaStep:
@@ -1154,11 +1496,63 @@ def cpu_baseline_mla(kernel, t, kv, seconds):
             "host_cpus": os.cpu_count()}
 
 
+def run_reference_c3(args, world):
+    """The oracle as the timed arm of the default workload: every step is the producer on the
+    5120-wide row plus each arm's GEMV on a bounded sample of its 17408 rows, sized from a
+    calibration so that warm-up + K steps take about a minute; GB/s scaled from the sample."""
+    import oracle
+    oracle.build()
+    out_f, in_f = C3_OUT_F, C3_IN_F
+    data = {k: _oracle_inputs(k, out_f, in_f, 1) for k in ARMS}
+    x, wn = data["e4m3"][0], data["e4m3"][1]
+    _, d, qs, _ = oracle.rmsnorm_q8_1(x, wn, 1e-6)
+    t0 = time.perf_counter()
+    for k in ARMS:
+        _oracle_gemv(oracle, k, data[k][2], data[k][3], qs, d, in_f, np.arange(64))
+    per_row = (time.perf_counter() - t0) / 64  # one row of each arm
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    nrows = int(max(1, min(out_f, budget / max(per_row, 1e-9))))
+    rng = np.random.default_rng(7)
+    samples = [np.sort(rng.choice(out_f, size=nrows, replace=False)) for _ in range(8)]
+
+    def step(i):
+        _, dd, qq, _ = oracle.rmsnorm_q8_1(x, wn, 1e-6)
+        for k in ARMS:
+            _oracle_gemv(oracle, k, data[k][2], data[k][3], qq, dd, in_f, samples[i % 8])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    sample_bytes = producer_bytes(1, in_f) + sum(
+        gemv_bytes(k, nrows, in_f, 1) - (4 if k == "e4m3" else 0) for k in ARMS)
+    v = args.steps * sample_bytes / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"c3: f64 C oracle of the same step (producer + E4M3, block-128 and "
+                               f"Q8_0 GEMV out_f={out_f} in_f={in_f} m=1)",
+                   "sample_rows_per_step": nrows},
+        "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: producer 1x{in_f} + {nrows} of {out_f} rows of "
+                                   f"each arm's GEMV, f64 C oracle, single thread"},
+        "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """The oracle as the timed arm: every step is the producer plus a bounded row sample of the
     GEMV, sized from a calibration step so that warm-up + K steps take about a minute."""
     if rank != 0:
         return
+    if args.workload == "c3":
+        return run_reference_c3(args, world)
     import oracle
     oracle.build()
     kind, out_f, in_f, m, copies = parse_workload(args.workload)
@@ -1207,8 +1601,10 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100000)
-    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 50 for c3, whose step is ~50 launches; 100000 "
+                         "for the single-launch workloads)")
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="one of %s, or <e4m3|blk128|q8_0>_<out_f>x<in_f>_m<m>, c3, "
@@ -1230,6 +1626,10 @@ def main(argv=None):
     ap.add_argument("--ncu-launches", type=int, default=0,
                     help="profiling entry: run one producer and N GEMV launches, no timing")
     args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = 50 if args.workload == "c3" else 100000
+    if args.warmup is None:
+        args.warmup = 5 if args.workload == "c3" else 1000
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()

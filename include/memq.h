@@ -159,8 +159,8 @@ int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps, cons
  * entries (device pointers / row counts), read during the call only.  Per matrix the
  * single-call rules apply; every out_f must be >= 1.  If any matrix is off the fast path (an
  * unaligned pointer, Q8_0 rows not 16-byte aligned) the call falls back to one launch per
- * matrix.  Part of the "dual gate+up GEMV sharing one activation read" named among the unfused
- * sites of q8_fuse_gate.rs (`main`).
+ * matrix.  It serves the gate and up projections, which read the same activation (q8_fuse_gate.rs,
+ * `main`, lists that site among those not yet fused).
  * Errors: MEMQ_ERR_SHAPE (count outside [1, 4], an empty matrix, a bad size), MEMQ_ERR_NULL,
  * MEMQ_ERR_ALIGN, MEMQ_ERR_M_RANGE, MEMQ_ERR_LAUNCH.
  */
@@ -190,8 +190,8 @@ int memq_silu_mul_q8_1(const float *gate, const float *up, float *z, int8_t *qs,
 
 /*
  * memq_repack_e4m3_q8_0 / memq_repack_e4m3_blk128_q8_0 -- load-time conversion of E4M3
- * weights into a ggml block_q8_0 slab (gemv_e4m3_bench.rs, module doc "QUESTION": the ship
- * path "dequants FP8 checkpoints to a Q8_0 slab at load", ARM B').  For each row r and 32-block
+ * weights into ggml block_q8_0 records (gemv_e4m3_bench.rs, module doc "QUESTION": the
+ * shipping path converts FP8 weights into Q8_0 once, at load time, ARM B').  For each row r and 32-block
  * b of the row, with W[i] = e4m3(w[r][i]) * s in f32 (s = *w_scale, or grid[r/128][i/128]):
  *     d = max_{i in b} |W[i]| / 127  (f32),  stored as f16 (round to nearest even)
  *     qs[i] = round(W[i] / d)  (f32 quotient, ties away from zero; 0 when d == 0)
@@ -255,7 +255,9 @@ const char *memq_status_string(int status);
  * memq_device_fault -- read and clear the current device's fault word.
  * Synchronizes `stream`, then stores the word in *fault_out (0 = no fault) and resets it.
  * Bit 0: a GEMV consumer's bounded wait on a shared-memory barrier expired; bit 1: the GEMV
- * producer's.  The kernel that gave up wrote nothing more and returned.  Bit 2: an
+ * producer's.  A CTA that gave up stores no output for the tile it was on or any later one
+ * (rows it finished before may already be stored), waits (bounded) for its copies in flight
+ * and returns; the call's outputs are invalid.  Bit 2: an
  * memq_mla_attn_gathered CTA's bounded wait for its gathered rows expired; bit 3: the same in
  * memq_mla_absorb_q / memq_mla_decompress_v.  That CTA stopped streaming, waited (bounded) for
  * its copies in flight and returned; the call's outputs are invalid.

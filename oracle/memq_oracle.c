@@ -43,7 +43,7 @@
  *
  * Also from the pages: q8_fuse_gate.rs, `main` -- the silu(gate)*up -> q8_1 activation producer
  * named for the 1536-wide expert site; gemv_e4m3_bench.rs, module doc "QUESTION" -- the ship
- * path that dequantizes FP8 weights to a Q8_0 slab at load ("ARM B'"); mla_decode_arm_gate.rs,
+ * path converts FP8 weights into a Q8_0 copy once, at load time ("ARM B'"); mla_decode_arm_gate.rs,
  * module doc and `main` -- the t <= 8 MLA decode attention kernels absorb_q, decompress_v and
  * attn_gathered.
  */
@@ -263,7 +263,7 @@ void memq_oracle_silu_mul(const float *g, const float *u, int64_t n, double *z)
 
 /* ---------------------------------------------------------------------------------------------
  * Load-time repack of E4M3 weights into a Q8_0 slab (gemv_e4m3_bench.rs, module doc
- * "QUESTION": the ship path "dequants FP8 checkpoints to a Q8_0 slab at load").
+ * "QUESTION": the shipping path converts FP8 weights into Q8_0 once, at load time).
  *
  * The pages fix the two formats but not the arithmetic of the conversion; the reading taken is
  * the q8_1 rule applied to the dequantized weights, per 32-block of a row:

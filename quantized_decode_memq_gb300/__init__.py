@@ -11,8 +11,8 @@ Stage 1 -- ``memq_rmsnorm_q8_1``: q8_fuse_gate.rs (memra-engine 0.125.0), the fu
 ``memq_gemv_q8_0``: gemv_e4m3_bench.rs, the E4M3 / block-128 / Q8_0 arms.  The fused decode
 step ``memq_rmsnorm_q8_1_gemv_*`` runs both stages in one launch.  Around them:
 ``memq_silu_mul_q8_1`` (the silu(gate) * up -> q8_1 producer named in q8_fuse_gate.rs, ``main``)
-and ``memq_repack_e4m3[_blk128]_q8_0`` (gemv_e4m3_bench.rs, "QUESTION": E4M3 weights -> a Q8_0
-slab at load).  The MLA decode attention kernels ``memq_mla_absorb_q``,
+and ``memq_repack_e4m3[_blk128]_q8_0`` (gemv_e4m3_bench.rs, "QUESTION": E4M3 weights converted to
+Q8_0 once at load).  The MLA decode attention kernels ``memq_mla_absorb_q``,
 ``memq_mla_attn_gathered`` and ``memq_mla_decompress_v``: mla_decode_arm_gate.rs (module doc).
 """
 from __future__ import annotations

@@ -77,8 +77,10 @@ inline bool q80_on_tensor_cores(int64_t out_f, int64_t in_f, int m) {
 }
 
 // Stream-kernel geometry per container.  A stage holds 32 blocks of every tile row.
-//   E4M3 / block-128: 16-row tiles (one m16 MMA row tile); row slots padded to 1040 bytes so the
-//   8-byte fragment loads of 8 different rows fall in distinct bank groups.
+//   E4M3 / block-128: 16-row tiles (one m16 MMA row tile); row slots padded to 1056 bytes (a row
+//   stride of 32 bytes modulo the 128-byte bank period): a warp's 8-byte fragment loads cover
+//   rows g = 0..7 at byte 8t of a block, and each group of 16 lanes (rows 4i..4i+3) then hits
+//   32 distinct banks, so the loads are conflict-free.
 //   Q8_0 (dp4a): 8-row tiles, 1088-byte row slots (34-byte blocks).
 //   Q8_0 (tensor cores): 16-row tiles, row slots padded to 1104 bytes.
 template <int KIND>
@@ -87,24 +89,24 @@ struct Geo {
     static constexpr int kBlockBytes = is_q80(KIND) ? 34 : 32;
     static constexpr int kTileRows = kMma ? 16 : kWarps;  // Q8_0: one row per consumer warp
     static constexpr int kChunkBlocks = 32;
-    static constexpr int kSlot = kChunkBlocks * kBlockBytes + (kMma ? 16 : 0);
+    static constexpr int kSlot = kChunkBlocks * kBlockBytes + (!kMma ? 0 : is_q80(KIND) ? 16 : 32);
     static constexpr int kStage = kTileRows * kSlot;
     static constexpr int kMinStages = 3;
-    // Register budget: three (E4M3 / block-128) or four (Q8_0) CTAs per SM.  More CTAs per SM
-    // keep more weight bytes in flight per SM; the tensor-core kernels need more registers per
-    // thread than Q8_0's.
-    static constexpr int kMinCtasPerSm = kMma ? 3 : 4;
+    // CTAs per SM (the register budget of the launch bounds, and the most one launch uses):
+    // E4M3 / block-128 two, Q8_0 on the tensor cores three, Q8_0 with dp4a four.  Measured on
+    // 17408 x 5120 (back-to-back launches): E4M3 two CTAs with a ring of 5-6 stages each
+    // 15.2 us against 16.5 us with three CTAs of 3 stages and 18.8 us with one CTA of 12 stages:
+    // CTAs of one launch sharing an SM do not stream at equal rates (the last one's tail costs),
+    // while a single CTA's consumer warps cannot hide the MMA latency alone.
+    static constexpr int kMinCtasPerSm = KIND == kE4M3 || KIND == kBlk ? 2 : KIND == kQ80T ? 3 : 4;
     // CTAs per SM one launch uses (at most kMinCtasPerSm).
     static constexpr int kCtasPerLaunch = kMinCtasPerSm;
-    static constexpr int kMaxStages = 8;
+    static constexpr int kMaxStages = 12;
     static constexpr int kWarpBlocks = kChunkBlocks / kWarps;  // E4M3: blocks per warp per stage
 };
 
 // Weight matrices one launch may cover (sharing the activation: gate / up, q / k / v).
 constexpr int kMaxGroup = 4;
-// Block-128: the per-CTA d * grid table is used up to this many activation rows (measured: it
-// saves the consumers a multiply per scale at m <= 2; at m = 8 its size costs ring stages).
-constexpr int kDgMaxM = 2;
 
 struct StreamArgs {
     const uint8_t *w;
@@ -127,9 +129,6 @@ struct StreamArgs {
     float *z_out;
     // Shared-memory layout (bytes); barriers at 0.
     uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_red, off_ring;
-    // Block-128 with a staged activation: the per-(grid row, token, block) scale
-    // d[token][block] * grid[row][block / 4], formed once per CTA (0 = not used).
-    uint32_t off_dg;
     int use_tma;  // 1: full tiles (and 8-row halves) come as one tensor copy each
     int ctas_per_sm;  // host: CTAs per SM the plan sized shared memory for
     // The launch's matrices: matrix i owns CTAs [mat_cta[i], mat_cta[i+1]); each CTA takes w,
@@ -170,6 +169,20 @@ __device__ __forceinline__ void named_barrier_consumers() {
     asm volatile("bar.sync %0, %1;" ::"n"(kBarConsumers), "n"(kConsumerThreads) : "memory");
 }
 
+// The consumer barrier that also ORs a predicate over the consumer threads.
+__device__ __forceinline__ bool named_barrier_consumers_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(kBarConsumers), "n"(kConsumerThreads)
+        : "memory");
+    return r != 0;
+}
+
 
 // ---------------------------------------------------------------------------------------------
 // E4M3 / block-128 stage: tensor-core inner products.
@@ -195,19 +208,7 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
     const uint4 *bfrag = reinterpret_cast<const uint4 *>(sm + a.off_bfrag);
     const int8_t *s_qs = reinterpret_cast<const int8_t *>(sm + a.off_qs);
     const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
-    const float *grow0 = nullptr, *grow8 = nullptr, *dg0 = nullptr, *dg8 = nullptr;
-    if (KIND == kBlk) {
-        // Grid rows of this thread's two tile rows, from the CTA's staged grid rows (or their
-        // d * grid tables).
-        const int64_t r0 = row0 + g > row_last ? row_last : row0 + g;
-        const int64_t r8 = row0 + g + 8 > row_last ? row_last : row0 + g + 8;
-        const float *s_grid = reinterpret_cast<const float *>(sm + a.off_grid);
-        grow0 = s_grid + ((r0 >> 7) - grow_base) * a.gcols;
-        grow8 = s_grid + ((r8 >> 7) - grow_base) * a.gcols;
-        const float *s_dg = reinterpret_cast<const float *>(sm + a.off_dg);
-        dg0 = s_dg + ((r0 >> 7) - grow_base) * M * a.nb;
-        dg8 = s_dg + ((r8 >> 7) - grow_base) * M * a.nb;
-    }
+    float grp[4] = {0.f, 0.f, 0.f, 0.f};  // block-128: the sum over this 128-column group
 #pragma unroll
     for (int b = 0; b < G::kWarpBlocks; ++b) {
         if (FULL || b < nblk) {
@@ -229,35 +230,13 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
                     s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
                 }
             }
-            float k0 = 0.f, k1 = 0.f, k2 = 0.f, k3 = 0.f;
-            if (KIND == kBlk && MODE != kActGlobal && M <= kDgMaxM) {
-                // the CTA's d * grid table: one load per scale, no multiply
-                if (2 * t < M) {
-                    k0 = dg0[(2 * t) * a.nb + kb];
-                    k2 = dg8[(2 * t) * a.nb + kb];
-                }
-                if (2 * t + 1 < M) {
-                    k1 = dg0[(2 * t + 1) * a.nb + kb];
-                    k3 = dg8[(2 * t + 1) * a.nb + kb];
-                }
+            float k0 = 0.f, k1 = 0.f;
+            if (MODE == kActGlobal) {
+                if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
+                if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
             } else {
-                if (MODE == kActGlobal) {
-                    if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
-                    if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
-                } else {
-                    if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
-                    if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
-                }
-                k2 = k0;
-                k3 = k1;
-                if (KIND == kBlk) {
-                    const float gg = grow0[kb >> 2];
-                    const float gg8 = grow8[kb >> 2];
-                    k0 *= gg;
-                    k1 *= gg;
-                    k2 *= gg8;
-                    k3 *= gg8;
-                }
+                if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
+                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
             }
             const uint8_t *pa = stage + g * G::kSlot + 32 * b + 8 * t;
             const uint2 wa = lds64(pa);
@@ -270,11 +249,26 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
             e4m3x4_to_f16x2x2(wa.y, a0, a2);
             e4m3x4_to_f16x2x2(wb.y, a1, a3);
             mma_f16_16816(c, a0, a1, a2, a3, bq[2], bq[3]);
-            acc[0] = fmaf(c[0], k0, acc[0]);
-            acc[1] = fmaf(c[1], k1, acc[1]);
-            acc[2] = fmaf(c[2], k2, acc[2]);
-            acc[3] = fmaf(c[3], k3, acc[3]);
+            float(&dst)[4] = KIND == kBlk ? grp : acc;
+            dst[0] = fmaf(c[0], k0, dst[0]);
+            dst[1] = fmaf(c[1], k1, dst[1]);
+            dst[2] = fmaf(c[2], k0, dst[2]);
+            dst[3] = fmaf(c[3], k1, dst[3]);
         }
+    }
+    if (KIND == kBlk) {
+        // The grid entries of this thread's two tile rows for the warp's 128-column group (kb0 is
+        // a multiple of 4, so a warp's blocks never straddle two groups), from the CTA's staged
+        // grid rows.
+        const int64_t r0 = row0 + g > row_last ? row_last : row0 + g;
+        const int64_t r8 = row0 + g + 8 > row_last ? row_last : row0 + g + 8;
+        const float *s_grid = reinterpret_cast<const float *>(sm + a.off_grid);
+        const float g0 = s_grid[((r0 >> 7) - grow_base) * a.gcols + (kb0 >> 2)];
+        const float g8 = s_grid[((r8 >> 7) - grow_base) * a.gcols + (kb0 >> 2)];
+        acc[0] = fmaf(grp[0], g0, acc[0]);
+        acc[1] = fmaf(grp[1], g0, acc[1]);
+        acc[2] = fmaf(grp[2], g8, acc[2]);
+        acc[3] = fmaf(grp[3], g8, acc[3]);
     }
 }
 
@@ -592,6 +586,10 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
             int tile = 0, ch = 0, s = 0;
             uint32_t eph = 0;  // parity of the empty-barrier phase awaited before a reuse
             for (int it = 0; it < items; ++it) {
+                // The first S stages go out before the preceding grid has finished; the bounded
+                // waits for released stages start only once it has, so that a long predecessor
+                // never counts against this launch's own progress.
+                if (it == S) griddep_wait();
                 if (it >= S && !thread_wait_bounded(&empty[s], eph)) {
                     fault(2u);
                     break;
@@ -690,23 +688,6 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
             bfrag[i] = v;
         }
     }
-    if (KIND == kBlk && MODE != kActGlobal && M <= kDgMaxM) {
-        // d * grid for every (grid row of this CTA, token, block): the same f32 products the
-        // consumers would otherwise form per block.  (s_d and the grid rows are complete:
-        // written by this thread's own copies / waits or before the barrier below.)
-        named_barrier_consumers();
-        const float *s_d = reinterpret_cast<const float *>(smem + a.off_d);
-        const float *s_grid = reinterpret_cast<const float *>(smem + a.off_grid);
-        float *s_dg = reinterpret_cast<float *>(smem + a.off_dg);
-        const int nrows = static_cast<int>(((R1 - 1) >> 7) - grow_base + 1);
-        const int per_row = M * a.nb;
-        for (int i = threadIdx.x; i < nrows * per_row; i += kConsumerThreads) {
-            const int gr = i / per_row;
-            const int rem = i - gr * per_row;
-            const int kb = rem % a.nb;
-            s_dg[i] = __fmul_rn(s_d[rem], s_grid[gr * a.gcols + (kb >> 2)]);
-        }
-    }
     named_barrier_consumers();
 
     int c_stage = 0;
@@ -782,8 +763,9 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
                 pw[g * M + 2 * t + 1] = acc_m[1];
                 pw[(g + 8) * M + 2 * t + 1] = acc_m[3];
             }
-            named_barrier_consumers();
-            for (int idx = threadIdx.x; idx < rc * M; idx += kConsumerThreads) {
+            // A tile that any consumer warp gave up on is not stored (its sums are incomplete).
+            const bool bad = named_barrier_consumers_or(!ok);
+            for (int idx = threadIdx.x; !bad && idx < rc * M; idx += kConsumerThreads) {
                 const int row = idx / M, tok = idx - row * M;
                 const float *pt = part + (tile & 1) * kWarps * TR * M + row * M + tok;
                 float v = 0.f;
@@ -795,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
 #pragma unroll
             for (int j = 0; j < M; ++j) {
                 const float v = warp_sum(acc_q[j]);
-                if (lane == 0) a.y[static_cast<int64_t>(j) * a.out_f + r0 + warp] = v;
+                if (lane == 0 && ok) a.y[static_cast<int64_t>(j) * a.out_f + r0 + warp] = v;
             }
         }
     }
@@ -865,6 +847,62 @@ std::once_flag g_dev_once[kMaxDevices];
 std::atomic<uint64_t> g_attr_set[4][kMaxDevices];  // [kind]: bit per (M, mode, fused) set
 
 bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+// A small direct-mapped cache of per-call host results (occupancy answers, tensor maps), guarded
+// by a mutex.  An entry is only reused for an identical key: everything the value depends on is
+// part of the key, so nothing goes stale.
+template <class Key, class Val, int N>
+class HostCache {
+  public:
+    bool get(const Key &k, uint64_t h, Val &v) {
+        std::lock_guard<std::mutex> lock(mu_);
+        const Slot &e = slot_[h % N];
+        if (!e.used || !(e.key == k)) return false;
+        v = e.val;
+        return true;
+    }
+    void put(const Key &k, uint64_t h, const Val &v) {
+        std::lock_guard<std::mutex> lock(mu_);
+        Slot &e = slot_[h % N];
+        e.used = true;
+        e.key = k;
+        e.val = v;
+    }
+
+  private:
+    struct Slot {
+        bool used = false;
+        Key key{};
+        Val val{};
+    };
+    std::mutex mu_;
+    Slot slot_[N];
+};
+
+inline uint64_t mix_hash(uint64_t h, uint64_t v) {
+    h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+    return h;
+}
+
+struct OccKey {
+    const void *fn;
+    uint32_t smem;
+    int dev;
+    bool operator==(const OccKey &o) const { return fn == o.fn && smem == o.smem && dev == o.dev; }
+};
+HostCache<OccKey, int, 256> g_occ_cache;
+
+// cudaOccupancyMaxActiveBlocksPerMultiprocessor for kThreads-thread CTAs, cached per (kernel,
+// dynamic shared memory, device).
+template <class Kern>
+cudaError_t occupancy(int &per_sm, Kern kern, uint32_t smem, int dev) {
+    const OccKey k{reinterpret_cast<const void *>(kern), smem, dev};
+    const uint64_t h = mix_hash(mix_hash(reinterpret_cast<uintptr_t>(k.fn), smem), static_cast<uint64_t>(dev));
+    if (g_occ_cache.get(k, h, per_sm)) return cudaSuccess;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e == cudaSuccess) g_occ_cache.put(k, h, per_sm);
+    return e;
+}
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 cudaError_t device_info(int &dev, DeviceInfo &info) {
@@ -906,12 +944,36 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
+struct MapKey {
+    int kind;
+    const void *w;
+    int64_t out_f;
+    int64_t row_bytes;
+    int dev;
+    bool operator==(const MapKey &o) const {
+        return kind == o.kind && w == o.w && out_f == o.out_f && row_bytes == o.row_bytes &&
+               dev == o.dev;
+    }
+};
+// Tensor maps of recently used weight planes (a decode loop reuses the same few hundred).
+HostCache<MapKey, TmaMaps, 1024> g_map_cache;
+
 // Builds the two tensor maps of the weight plane (see TmaMaps) and sets a.use_tma; on any
-// failure the producer copies every row with its own bulk copy instead.
+// failure the producer copies every row with its own bulk copy instead.  Encoded maps are
+// cached per (container, weight pointer, rows, row bytes, device).
 template <int KIND>
-void make_maps(StreamArgs &a, TmaMaps &tm) {
+void make_maps(StreamArgs &a, TmaMaps &tm, int dev) {
     using G = Geo<KIND>;
     a.use_tma = 0;
+    const MapKey key{KIND, a.w, a.out_f, a.row_bytes, dev};
+    const uint64_t h = mix_hash(mix_hash(mix_hash(reinterpret_cast<uintptr_t>(a.w),
+                                                  static_cast<uint64_t>(a.out_f)),
+                                         static_cast<uint64_t>(a.row_bytes)),
+                                static_cast<uint64_t>(KIND * 64 + dev));
+    if (g_map_cache.get(key, h, tm)) {
+        a.use_tma = 1;
+        return;
+    }
     const EncodeTiledFn enc = encode_tiled();
     if (!enc || a.row_bytes % 16 != 0 || a.out_f > (1ll << 31) - 1) return;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.row_bytes / 8),
@@ -929,13 +991,14 @@ void make_maps(StreamArgs &a, TmaMaps &tm) {
             return;
     }
     a.use_tma = 1;
+    g_map_cache.put(key, h, tm);
 }
 
 template <int KIND, int M, int MODE, bool FUSE>
 cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const DeviceInfo &info,
                           cudaStream_t st) {
     auto kern = gemv_stream_kernel<KIND, M, MODE, FUSE>;
-    const uint64_t bit = 1ull << ((M - 1) + 8 * MODE + (FUSE ? 24 : 0));
+    const uint64_t bit = 1ull << ((M - 1) + 8 * MODE + (FUSE ? 32 : 0));
     if (!(g_attr_set[KIND][dev].load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              info.smem_optin);
@@ -947,8 +1010,7 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     using G = Geo<KIND>;
     const uint32_t fixed = smem_bytes;  // everything except the ring and its barriers
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, kern, kThreads, fixed + G::kMinStages * (G::kStage + 16) + 128);
+    cudaError_t e = occupancy(per_sm, kern, fixed + G::kMinStages * (G::kStage + 16) + 128, dev);
     if (e != cudaSuccess) return e;
     per_sm = std::max(std::min({per_sm, G::kMinCtasPerSm, a.ctas_per_sm}), 1);
     int S = G::kMinStages;
@@ -971,9 +1033,8 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
     a.off_d += bars;
     a.off_red += bars;
     a.off_ring += bars;
-    if (a.off_dg) a.off_dg += bars;
     smem_bytes = fixed + bars + static_cast<uint32_t>(S * G::kStage);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes);
+    e = occupancy(per_sm, kern, smem_bytes, dev);
     if (e != cudaSuccess) return e;
     per_sm = std::max(per_sm, 1);
     // One wave of CTAs, split over the launch's matrices in proportion to their rows (rounded
@@ -1005,7 +1066,7 @@ cudaError_t launch_stream(StreamArgs a, uint32_t smem_bytes, int dev, const Devi
         StreamArgs ai = a;
         ai.w = a.mat_w[i];
         ai.out_f = a.mat_out_f[i];
-        make_maps<KIND>(ai, tg.m[i]);
+        make_maps<KIND>(ai, tg.m[i], dev);
         tma_ok &= ai.use_tma;
     }
     a.use_tma = tma_ok;
@@ -1063,7 +1124,6 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
     const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
     // block-128 with a staged activation: the CTA's d * grid table
-    const uint32_t dgb = (KIND == kBlk && m <= kDgMaxM) ? align_up(static_cast<uint32_t>(grid_rows * m * nb * 4), 128) : 0u;
     const uint32_t red = fuse ? align_up((kWarps + 1) * 8, 128) : 0u;
     const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
     const uint32_t base = part + gridb + red + ring_min;
@@ -1079,9 +1139,9 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     for (int k = k_rows; k >= 1; --k) {
         // Shared memory one CTA may use and still leave room for k CTAs per SM.
         const uint32_t budget = std::min(optin, static_cast<uint32_t>(info.smem_sm / k - 1024));
-        if (G::kMma && base + qsb + db + dgb + frag <= budget) {
+        if (G::kMma && base + qsb + db + frag <= budget) {
             mode = kActFrag;
-        } else if (base + qsb + db + dgb <= budget) {
+        } else if (base + qsb + db <= budget) {
             mode = kActSmem;
         } else {
             continue;
@@ -1101,11 +1161,6 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     if (mode != kActGlobal) off += qsb;
     a.off_d = off;
     if (mode != kActGlobal) off += db;
-    a.off_dg = 0;
-    if (KIND == kBlk && mode != kActGlobal && m <= kDgMaxM) {
-        a.off_dg = off;
-        off += align_up(static_cast<uint32_t>(grid_rows * m * nb * 4), 128);
-    }
     a.off_red = off;
     off += red;  // cross-warp scratch of the fused prologue
     a.off_ring = off;

@@ -153,6 +153,10 @@ __global__ void __launch_bounds__(kHeadThreads)
         int st = 0;
         for (; st < nst && ok; ++st) {
             const int slot = st % S;
+            // The first S copies go out before the preceding grid has finished; the bounded
+            // waits for released stages start only once it has, so that a long predecessor
+            // never counts against this launch's own progress.
+            if (st == S) griddep_wait();
             if (st >= S) ok = warp_wait_bounded(&empty[slot], static_cast<uint32_t>((st / S - 1) & 1));
             if (!ok) break;
             const int nrs = min(kHeadRows, r1 - r0 - st * kHeadRows);

@@ -3,7 +3,7 @@
 //
 // Operations: q8_fuse_gate.rs (memra-engine 0.125.0), `main` -- the expert-ff site's
 // "silu/gate*up -> q8_1" producer (width 1536); gemv_e4m3_bench.rs, module doc "QUESTION" --
-// the ship path that "dequants FP8 checkpoints to a Q8_0 slab at load" (ARM B').
+// the shipping path converts FP8 weights into a Q8_0 copy once, when the model loads (ARM B').
 //
 // silu_mul_q8_1_kernel: elementwise, one thread per float4 of a row; a 32-element block is 8
 // adjacent threads, so its amax is a 3-step xor shuffle (as in the RMSNorm producer).  In the

@@ -29,3 +29,23 @@ def test_cpu_baseline_mla(oracle, kernel, t, kv):
     cb = bench.cpu_baseline_mla(kernel, t, kv, 0.05)
     assert cb["kind"] == "oracle" and cb["unit"] == "us" and cb["value"] > 0
     assert "of 64 heads" in cb["sample"]
+
+
+def test_cpu_baseline_arms_legs(oracle):
+    """The default workload's CPU baseline on a small shape: a single-threaded leg and an
+    all-cores leg (rows split over the affinity mask), each GB/s of the three-arm step."""
+    from types import SimpleNamespace
+    arms = {k: SimpleNamespace(out_f=256, in_f=512, gemv_bytes=bench.gemv_bytes(k, 256, 512, 1))
+            for k in bench.ARMS}
+    cb = bench.cpu_baseline_arms(arms, 0.2)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    cores = [leg["cores"] for leg in cb["legs"]]
+    assert cores[0] == 1 and cores[-1] == bench.affinity_cores() == cb["cores"]
+    assert all(leg["value"] > 0 and set(leg["arms"]) == set(bench.ARMS) for leg in cb["legs"])
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+
+
+def test_default_workload_is_the_three_arm_target():
+    assert bench.DEFAULT_WORKLOAD == "c3"
+    assert (bench.C3_OUT_F, bench.C3_IN_F) == (17408, 5120)
+    assert bench.ARMS == ("e4m3", "blk", "q8_0")
