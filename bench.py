@@ -179,8 +179,8 @@ class ClockSampler:
 
 # Source files each committed traffic record depends on (the kernel and its building blocks).
 TRAFFIC_SOURCES = {
-    "gemv_traffic.json": ("memq_dev.cuh", "memq_gemv_kernels.cuh", "memq_gemv_e4m3.cu",
-                          "memq_gemv_blk128.cu", "memq_gemv_q8_0.cu"),
+    "gemv_traffic.json": ("memq_dev.cuh", "memq_gemv_kernels.cuh", "memq_gemv_kouter.cuh",
+                          "memq_gemv_e4m3.cu", "memq_gemv_blk128.cu", "memq_gemv_q8_0.cu"),
     "mla_traffic.json": ("memq_dev.cuh", "memq_mla.cu"),
 }
 

@@ -117,6 +117,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, int x, i
         : "memory");
 }
 
+// As tma_load_2d, with the default L2 policy.
+__device__ __forceinline__ void tma_load_2d_plain(void *dst, const void *map, int x, int y,
+                                                  uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const void *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -92,13 +92,9 @@ struct Geo {
     static constexpr int kSlot = kChunkBlocks * kBlockBytes + (!kMma ? 0 : is_q80(KIND) ? 16 : 32);
     static constexpr int kStage = kTileRows * kSlot;
     static constexpr int kMinStages = 3;
-    // CTAs per SM (the register budget of the launch bounds, and the most one launch uses):
-    // E4M3 / block-128 two, Q8_0 on the tensor cores three, Q8_0 with dp4a four.  Measured on
-    // 17408 x 5120 (back-to-back launches): E4M3 two CTAs with a ring of 5-6 stages each
-    // 15.2 us against 16.5 us with three CTAs of 3 stages and 18.8 us with one CTA of 12 stages:
-    // CTAs of one launch sharing an SM do not stream at equal rates (the last one's tail costs),
-    // while a single CTA's consumer warps cannot hide the MMA latency alone.
-    static constexpr int kMinCtasPerSm = KIND == kE4M3 || KIND == kBlk ? 2 : KIND == kQ80T ? 3 : 4;
+    // Register budget: three (tensor-core kernels) or four (Q8_0 with dp4a) CTAs per SM; the
+    // plan (plan_stream) may use fewer.
+    static constexpr int kMinCtasPerSm = kMma ? 3 : 4;
     // CTAs per SM one launch uses (at most kMinCtasPerSm).
     static constexpr int kCtasPerLaunch = kMinCtasPerSm;
     static constexpr int kMaxStages = 12;
@@ -160,7 +156,9 @@ struct TmaGroup {
 enum ActMode : int {
     kActGlobal = 0,  // qs and d straight from global memory (L1/L2)
     kActSmem = 1,    // qs (int8) and d staged in shared memory once per CTA
-    kActFrag = 2,    // E4M3 / block-128: f16 MMA B fragments and d staged in shared memory
+    kActFrag = 2,    // E4M3 / block-128 / Q8_0 on the tensor cores: f16 MMA B fragments and d
+                     // staged in shared memory; Q8_0 with dp4a: the activation staged in the
+                     // record-aligned layout of q80_stage (and d)
 };
 
 __device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bit); }
@@ -361,11 +359,67 @@ __device__ __forceinline__ void mma_stage_q80(const StreamArgs &a, const uint8_t
 // 34-byte record, so they are re-aligned from 4-byte shared loads with funnel shifts; dp4a then
 // gives the exact int32 dot product with the activation block.
 // ---------------------------------------------------------------------------------------------
+// kActFrag (the default for dp4a): the activation is staged once per CTA in a layout that
+// matches the 34-byte records as they sit in the stage, so no weight word needs realigning.
+// Lane l reads the nine 4-byte words of its row slot that cover its record, from byte
+// (34*l) & ~3: for an even block the record starts on a word (word 0 = f16 scale, then
+// q0 q1; word 8 = q30 q31 and the next record's scale), for an odd block two bytes into one
+// (word 0 = the previous record's last two codes, then the scale; words 1..8 = q0..q31).  The
+// staged activation of block kb (12 words per (token, block), 9 used) has the activation bytes
+// under the weight bytes of that layout and zeros under everything else, so nine dp4a give the
+// block's exact int32 dot product, and the scale comes out of word 0.
+constexpr int kQ8ActWords = 12;  // words per (token, block) of the staged dp4a activation
+
+__device__ __forceinline__ void q80_act_layout(const uint32_t *q, bool odd, uint32_t *dst) {
+    // q: the block's 8 activation words; dst: 9 words (see above)
+    if (odd) {
+        dst[0] = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i + 1] = q[i];
+    } else {
+        dst[0] = q[0] << 16;
+#pragma unroll
+        for (int i = 1; i < 8; ++i) dst[i] = __funnelshift_r(q[i - 1], q[i], 16);
+        dst[8] = q[7] >> 16;
+    }
+}
+
 template <int M, int MODE>
 __device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *slot,
                                           const uint8_t *sm, int kb0, int nblk, int lane,
                                           float (&acc)[M]) {
     if (lane >= nblk) return;
+    if constexpr (MODE == kActFrag) {
+        const int kb = kb0 + lane;
+        const bool odd = lane & 1;  // kb0 is even: block parity = lane parity
+        const uint8_t *rec = slot + ((34 * lane) & ~3);
+        uint32_t w[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) w[i] = lds32(rec + 4 * i);
+        const uint32_t dbits = odd ? (w[0] >> 16) : (w[0] & 0xffffu);
+        const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+        const uint32_t *act = reinterpret_cast<const uint32_t *>(sm + a.off_bfrag);
+        const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+            const uint32_t *aj = act + (j * a.nb + kb) * kQ8ActWords;
+            const uint4 x0 = lds128(aj);
+            const uint4 x1 = lds128(aj + 4);
+            const uint32_t x2 = lds32(aj + 8);
+            int s0 = 0, s1 = 0;
+            s0 = __dp4a(static_cast<int>(w[0]), static_cast<int>(x0.x), s0);
+            s1 = __dp4a(static_cast<int>(w[1]), static_cast<int>(x0.y), s1);
+            s0 = __dp4a(static_cast<int>(w[2]), static_cast<int>(x0.z), s0);
+            s1 = __dp4a(static_cast<int>(w[3]), static_cast<int>(x0.w), s1);
+            s0 = __dp4a(static_cast<int>(w[4]), static_cast<int>(x1.x), s0);
+            s1 = __dp4a(static_cast<int>(w[5]), static_cast<int>(x1.y), s1);
+            s0 = __dp4a(static_cast<int>(w[6]), static_cast<int>(x1.z), s0);
+            s1 = __dp4a(static_cast<int>(w[7]), static_cast<int>(x1.w), s1);
+            s0 = __dp4a(static_cast<int>(w[8]), static_cast<int>(x2), s0);
+            acc[j] = fmaf(static_cast<float>(s0 + s1), dw * s_d[j * a.nb + kb], acc[j]);
+        }
+        return;
+    }
     const int kb = kb0 + lane;
     const int qstart = 34 * lane + 2;
     const int abase = qstart & ~3;
@@ -672,7 +726,21 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
             ok = false;
         }
     }
-    if (MODE == kActFrag) {
+    if (MODE == kActFrag && KIND == kQ80) {
+        // The dp4a layout of the whole activation (q80_stage): per (token, block) nine words.
+        uint32_t *dst = reinterpret_cast<uint32_t *>(smem + a.off_bfrag);
+        const int n = a.nb * M;
+        for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
+            const int j = i / a.nb, kb = i - j * a.nb;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(smem + a.off_qs + j * a.in_f + 32 * kb);
+            uint32_t q[8], o[9];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q[k] = src[k];
+            q80_act_layout(q, kb & 1, o);
+#pragma unroll
+            for (int k = 0; k < 9; ++k) dst[i * kQ8ActWords + k] = o[k];
+        }
+    } else if (MODE == kActFrag) {
         // f16 MMA B fragments of the whole activation: entry (kb, g, t) holds
         // q[g][32kb + 8t .. 8t+7] as four f16x2 registers.
         uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);
@@ -1120,7 +1188,7 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     const int grid_rows = static_cast<int>(rows_cta / 128 + 2);
     const int gcols = static_cast<int>((in_f + 127) / 128);
     const uint32_t gridb = KIND == kBlk ? align_up(static_cast<uint32_t>(grid_rows * gcols * 4), 128) : 0u;
-    const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * 64), 128);
+    const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * (KIND == kQ80 ? 4 * kQ8ActWords : 64)), 128);
     const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
     const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
     // block-128 with a staged activation: the CTA's d * grid table
@@ -1132,14 +1200,27 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     // (measured: 1024 x 5120 runs 20-30% faster at one CTA per SM than with 2-3 rows per CTA;
     // from about 7 rows per CTA up, more CTAs per SM are faster).
     constexpr int64_t kMinRowsPerCta = 4;
+    // Preferred CTAs per SM, measured on GB300 (back-to-back launches, DRAM-cold):
+    //  * E4M3 / block-128: two when every CTA then gets at least two full 16-row tiles (17408 x
+    //    5120: 15.0 us against 16.1 us with three), else three (5120 x 5120: 6.3 against 7.9 us;
+    //    5120 x 17408: 17.2 against 21.8 us).  CTAs of one launch sharing an SM do not stream at
+    //    equal rates, so fewer and larger CTAs shorten the tail -- unless a CTA's rows make only
+    //    one full tile and a ragged one, or its staged activation leaves a shallow ring.
+    //  * Q8_0 with dp4a: four, three when the staged activation is large (5120 x 17408: 17.5
+    //    against 19.1 us).
+    int pref = G::kMinCtasPerSm;
+    if (KIND == kE4M3 || KIND == kBlk)
+        pref = out_f >= static_cast<int64_t>(info.sms) * 2 * 2 * G::kTileRows ? 2 : 3;
+    else if (KIND == kQ80)
+        pref = static_cast<int64_t>(m) * in_f > 8192 ? 3 : 4;
     const int k_rows = static_cast<int>(std::min<int64_t>(
-        G::kMinCtasPerSm, std::max<int64_t>(1, out_f / (static_cast<int64_t>(info.sms) * kMinRowsPerCta))));
+        pref, std::max<int64_t>(1, out_f / (static_cast<int64_t>(info.sms) * kMinRowsPerCta))));
     int ctas = k_rows;
     mode = kActGlobal;
     for (int k = k_rows; k >= 1; --k) {
         // Shared memory one CTA may use and still leave room for k CTAs per SM.
         const uint32_t budget = std::min(optin, static_cast<uint32_t>(info.smem_sm / k - 1024));
-        if (G::kMma && base + qsb + db + frag <= budget) {
+        if (base + qsb + db + frag <= budget) {
             mode = kActFrag;
         } else if (base + qsb + db <= budget) {
             mode = kActSmem;
@@ -1171,13 +1252,19 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
 template <int KIND, bool FUSE>
 cudaError_t launch_planned(int m, int mode, StreamArgs a, uint32_t smem, int dev,
                            const DeviceInfo &info, cudaStream_t st) {
-    if constexpr (Geo<KIND>::kMma) {
-        if (mode == kActFrag) return launch_stream_m<KIND, kActFrag, FUSE>(m, a, smem, dev, info, st);
-    }
+    if (mode == kActFrag) return launch_stream_m<KIND, kActFrag, FUSE>(m, a, smem, dev, info, st);
     if (mode == kActSmem) return launch_stream_m<KIND, kActSmem, FUSE>(m, a, smem, dev, info, st);
     if constexpr (!FUSE) return launch_stream_m<KIND, kActGlobal, false>(m, a, smem, dev, info, st);
     return cudaErrorInvalidValue;
 }
+
+}  // namespace
+}  // namespace memq
+
+#include "memq_gemv_kouter.cuh"
+
+namespace memq {
+namespace {
 
 template <int KIND>
 int check_gemv_args(const uint8_t *w, const float *aux, const int8_t *qs, const float *d,
@@ -1229,6 +1316,12 @@ int gemv_entry(const uint8_t *w, const float *aux, const int8_t *qs, const float
     DeviceInfo info;
     if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if constexpr (KIND == kE4M3 || KIND == kBlk) {
+        if (fast_path_ok<KIND>(w, qs, in_f)) {
+            const cudaError_t ek = launch_kouter_m<KIND>(m, 1, &w, &aux, &y, &out_f, qs, d, in_f, dev, info, st);
+            if (ek != cudaErrorNotSupported) return ek == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+        }
+    }
     StreamArgs a = base_args<KIND>(w, aux, qs, d, y, out_f, in_f);
     uint32_t smem = 0;
     int mode = kActGlobal;
@@ -1275,6 +1368,11 @@ int group_entry(int count, const uint8_t *const *w, const float *const *aux, flo
     int dev = 0;
     DeviceInfo info;
     if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
+    if constexpr (KIND == kE4M3 || KIND == kBlk) {
+        const cudaError_t ek = launch_kouter_m<KIND>(m, count, w, aux, y, out_f, qs, d, in_f, dev,
+                                                     info, static_cast<cudaStream_t>(stream));
+        if (ek != cudaErrorNotSupported) return ek == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+    }
     StreamArgs a = base_args<KIND>(w[0], is_q80(KIND) ? nullptr : aux[0], qs, d, y[0], out_f[0], in_f);
     a.nmat = count;
     for (int i = 0; i < count; ++i) {
