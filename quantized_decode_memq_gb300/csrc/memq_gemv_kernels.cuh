@@ -76,18 +76,22 @@ inline bool q80_on_tensor_cores(int64_t out_f, int64_t in_f, int m) {
     return m >= kQ80MmaMinM && m * in_f <= 40960 && out_f >= 2048;
 }
 
+// Q8_0 with dp4a: rows per consumer warp in a tile (q80_pair_row: the two half-warps take two
+// adjacent rows).
+constexpr int kQ8RowsPerWarp = 2;
+
 // Stream-kernel geometry per container.  A stage holds 32 blocks of every tile row.
 //   E4M3 / block-128: 16-row tiles (one m16 MMA row tile); row slots padded to 1056 bytes (a row
 //   stride of 32 bytes modulo the 128-byte bank period): a warp's 8-byte fragment loads cover
 //   rows g = 0..7 at byte 8t of a block, and each group of 16 lanes (rows 4i..4i+3) then hits
 //   32 distinct banks, so the loads are conflict-free.
-//   Q8_0 (dp4a): 8-row tiles, 1088-byte row slots (34-byte blocks).
+//   Q8_0 (dp4a): 8 * kQ8RowsPerWarp-row tiles, 1088-byte row slots (34-byte blocks).
 //   Q8_0 (tensor cores): 16-row tiles, row slots padded to 1104 bytes.
 template <int KIND>
 struct Geo {
     static constexpr bool kMma = KIND != kQ80;
     static constexpr int kBlockBytes = is_q80(KIND) ? 34 : 32;
-    static constexpr int kTileRows = kMma ? 16 : kWarps;  // Q8_0: one row per consumer warp
+    static constexpr int kTileRows = kMma ? 16 : kWarps * kQ8RowsPerWarp;
     static constexpr int kChunkBlocks = 32;
     static constexpr int kSlot = kChunkBlocks * kBlockBytes + (!kMma ? 0 : is_q80(KIND) ? 16 : 32);
     static constexpr int kStage = kTileRows * kSlot;
@@ -158,7 +162,7 @@ enum ActMode : int {
     kActSmem = 1,    // qs (int8) and d staged in shared memory once per CTA
     kActFrag = 2,    // E4M3 / block-128 / Q8_0 on the tensor cores: f16 MMA B fragments and d
                      // staged in shared memory; Q8_0 with dp4a: the activation staged in the
-                     // record-aligned layout of q80_stage (and d)
+                     // record-aligned layout of q80_stage_lane (and d)
 };
 
 __device__ __forceinline__ void fault(unsigned bit) { atomicOr(&g_memq_fault, bit); }
@@ -384,44 +388,20 @@ __device__ __forceinline__ void q80_act_layout(const uint32_t *q, bool odd, uint
     }
 }
 
+// Q8_0 with dp4a and the record-aligned activation (kActFrag): the rows of a 16-row tile a lane
+// works on.  Warp w takes rows 2w and 2w + 1: lanes 0-15 read row 2w and lanes 16-31 row 2w + 1,
+// lane l blocks l % 16 and l % 16 + 16.  Lane k of a half-warp reads the words of record k from
+// word floor(8.5 k) of its row: for k < 16 these fall on 16 distinct banks, and the next row
+// lies one 1088-byte slot (272 words, 16 banks) away -- on the complementary 16 banks -- so every
+// 4-byte load of the warp is conflict-free (the same holds for blocks 16-31).
+__device__ __forceinline__ int q80_pair_row(int warp, int lane) { return 2 * warp + (lane >> 4); }
+
 template <int M, int MODE>
-__device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *slot,
-                                          const uint8_t *sm, int kb0, int nblk, int lane,
-                                          float (&acc)[M]) {
-    if (lane >= nblk) return;
-    if constexpr (MODE == kActFrag) {
-        const int kb = kb0 + lane;
-        const bool odd = lane & 1;  // kb0 is even: block parity = lane parity
-        const uint8_t *rec = slot + ((34 * lane) & ~3);
-        uint32_t w[9];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) w[i] = lds32(rec + 4 * i);
-        const uint32_t dbits = odd ? (w[0] >> 16) : (w[0] & 0xffffu);
-        const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
-        const uint32_t *act = reinterpret_cast<const uint32_t *>(sm + a.off_bfrag);
-        const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
-#pragma unroll
-        for (int j = 0; j < M; ++j) {
-            const uint32_t *aj = act + (j * a.nb + kb) * kQ8ActWords;
-            const uint4 x0 = lds128(aj);
-            const uint4 x1 = lds128(aj + 4);
-            const uint32_t x2 = lds32(aj + 8);
-            int s0 = 0, s1 = 0;
-            s0 = __dp4a(static_cast<int>(w[0]), static_cast<int>(x0.x), s0);
-            s1 = __dp4a(static_cast<int>(w[1]), static_cast<int>(x0.y), s1);
-            s0 = __dp4a(static_cast<int>(w[2]), static_cast<int>(x0.z), s0);
-            s1 = __dp4a(static_cast<int>(w[3]), static_cast<int>(x0.w), s1);
-            s0 = __dp4a(static_cast<int>(w[4]), static_cast<int>(x1.x), s0);
-            s1 = __dp4a(static_cast<int>(w[5]), static_cast<int>(x1.y), s1);
-            s0 = __dp4a(static_cast<int>(w[6]), static_cast<int>(x1.z), s0);
-            s1 = __dp4a(static_cast<int>(w[7]), static_cast<int>(x1.w), s1);
-            s0 = __dp4a(static_cast<int>(w[8]), static_cast<int>(x2), s0);
-            acc[j] = fmaf(static_cast<float>(s0 + s1), dw * s_d[j * a.nb + kb], acc[j]);
-        }
-        return;
-    }
-    const int kb = kb0 + lane;
-    const int qstart = 34 * lane + 2;
+__device__ __forceinline__ void q80_block_plain(const StreamArgs &a, const uint8_t *slot,
+                                                const uint8_t *sm, int kb0, int b,
+                                                float (&acc)[M]) {
+    const int kb = kb0 + b;
+    const int qstart = 34 * b + 2;
     const int abase = qstart & ~3;
     const uint32_t sh = static_cast<uint32_t>(qstart & 3) * 8u;  // 0 or 16
     uint32_t wv[9];
@@ -431,7 +411,7 @@ __device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *sl
     uint32_t qw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) qw[i] = __funnelshift_r(wv[i], wv[i + 1], sh);
-    const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(slot + 34 * lane))));
+    const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(slot + 34 * b))));
     const int8_t *s_qs = reinterpret_cast<const int8_t *>(sm + a.off_qs);
     const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
 #pragma unroll
@@ -458,6 +438,55 @@ __device__ __forceinline__ void q80_stage(const StreamArgs &a, const uint8_t *sl
         s = __dp4a(static_cast<int>(qw[6]), static_cast<int>(x1.z), s);
         s = __dp4a(static_cast<int>(qw[7]), static_cast<int>(x1.w), s);
         acc[j] = fmaf(static_cast<float>(s), dw * dj, acc[j]);
+    }
+}
+
+// The lane's share of a Q8_0 stage (q80_pair_row): blocks k and k + 16 (k = lane % 16) of its
+// row, whose slot is `slot`, accumulated into acc in block order.  The block products are exact
+// integers and the f32 operations per (row, token) are the same in every activation mode, so the
+// modes give bit-identical outputs.
+template <int M, int MODE>
+__device__ __forceinline__ void q80_stage_lane(const StreamArgs &a, const uint8_t *slot,
+                                               const uint8_t *sm, int kb0, int nblk, int lane,
+                                               float (&acc)[M]) {
+    const int k = lane & 15;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int b = k + 16 * h;
+        if (b >= nblk) break;
+        if constexpr (MODE == kActFrag) {
+            // record-aligned activation: nine dp4a over the record's word window
+            const bool odd = k & 1;  // kb0 is even; blocks k and k + 16 share k's parity
+            const int kb = kb0 + b;
+            const uint32_t *act = reinterpret_cast<const uint32_t *>(sm + a.off_bfrag);
+            const float *s_d = reinterpret_cast<const float *>(sm + a.off_d);
+            const uint8_t *rec = slot + ((34 * b) & ~3);
+            uint32_t w[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) w[i] = lds32(rec + 4 * i);
+            const uint32_t dbits = odd ? (w[0] >> 16) : (w[0] & 0xffffu);
+            const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+#pragma unroll
+            for (int j = 0; j < M; ++j) {
+                const uint32_t *aj = act + (j * a.nb + kb) * kQ8ActWords;
+                const uint4 x0 = lds128(aj);
+                const uint4 x1 = lds128(aj + 4);
+                const uint32_t x2 = lds32(aj + 8);
+                int s0 = 0, s1 = 0;
+                s0 = __dp4a(static_cast<int>(w[0]), static_cast<int>(x0.x), s0);
+                s1 = __dp4a(static_cast<int>(w[1]), static_cast<int>(x0.y), s1);
+                s0 = __dp4a(static_cast<int>(w[2]), static_cast<int>(x0.z), s0);
+                s1 = __dp4a(static_cast<int>(w[3]), static_cast<int>(x0.w), s1);
+                s0 = __dp4a(static_cast<int>(w[4]), static_cast<int>(x1.x), s0);
+                s1 = __dp4a(static_cast<int>(w[5]), static_cast<int>(x1.y), s1);
+                s0 = __dp4a(static_cast<int>(w[6]), static_cast<int>(x1.z), s0);
+                s1 = __dp4a(static_cast<int>(w[7]), static_cast<int>(x1.w), s1);
+                s0 = __dp4a(static_cast<int>(w[8]), static_cast<int>(x2), s0);
+                acc[j] = fmaf(static_cast<float>(s0 + s1), dw * s_d[j * a.nb + kb], acc[j]);
+            }
+        } else {
+            q80_block_plain<M, MODE>(a, slot, sm, kb0, b, acc);
+        }
     }
 }
 
@@ -727,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
         }
     }
     if (MODE == kActFrag && KIND == kQ80) {
-        // The dp4a layout of the whole activation (q80_stage): per (token, block) nine words.
+        // The dp4a layout of the whole activation (q80_stage_lane): per (token, block) nine words.
         uint32_t *dst = reinterpret_cast<uint32_t *>(smem + a.off_bfrag);
         const int n = a.nb * M;
         for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
@@ -805,8 +834,10 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
                         mma_stage<KIND, M, MODE, true>(a, st, smem, r0, R1 - 1, grow_base, kb0, n, lane, acc_m);
                     else if (n > 0)
                         mma_stage<KIND, M, MODE, false>(a, st, smem, r0, R1 - 1, grow_base, kb0, n, lane, acc_m);
-                } else if (warp < rc) {
-                    q80_stage<M, MODE>(a, stage + warp * G::kSlot, smem, kbc, nblk, lane, acc_q);
+                } else {
+                    const int row = q80_pair_row(warp, lane);
+                    if (row < rc)
+                        q80_stage_lane<M, MODE>(a, stage + row * G::kSlot, smem, kbc, nblk, lane, acc_q);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[c_stage]);
@@ -841,11 +872,15 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
                 for (int w = 0; w < kWarps; ++w) v += pt[w * TR * M];
                 a.y[static_cast<int64_t>(tok) * a.out_f + r0 + row] = v * scale;
             }
-        } else if (warp < rc) {
+        } else {
+            // sum over the 16 lanes of each half-warp: the warp's two rows
+            const int row = q80_pair_row(warp, lane);
 #pragma unroll
             for (int j = 0; j < M; ++j) {
-                const float v = warp_sum(acc_q[j]);
-                if (lane == 0 && ok) a.y[static_cast<int64_t>(j) * a.out_f + r0 + warp] = v;
+                float v = acc_q[j];
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+                if ((lane & 15) == 0 && row < rc && ok) a.y[static_cast<int64_t>(j) * a.out_f + r0 + row] = v;
             }
         }
     }
