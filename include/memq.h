@@ -97,6 +97,12 @@ int memq_rmsnorm_q8_1(const float *x, const float *w, float *z, int8_t *qs, floa
  *   is a no-op that accepts NULL pointers.
  * The fast path wants w and qs 16-byte aligned; other alignments take a slower generic kernel
  * with the same results contract.
+ * Numerics (all three containers): each 32-block product of weights and activation codes is
+ * exact (products of exactly represented values; Q8_0 an int32 dot product), scaled by d (and
+ * the grid entry / f16 block scale) and summed in f32 in a fixed order per (row, token).  On the
+ * fast path that order does not depend on m, on how the launch splits the rows, or on which of
+ * the library's kernels serves the call: a row's outputs are bit-identical whether it is
+ * computed alone, in an m-batch, or in a group.
  */
 int memq_gemv_e4m3(const uint8_t *w, const float *w_scale, const int8_t *qs, const float *d,
                    float *y, int64_t out_f, int64_t in_f, int m, void *stream);

@@ -68,12 +68,16 @@ constexpr bool is_q80(int kind) { return kind == kQ80 || kind == kQ80T; }
 // activation rows on it is bound by shared-memory bandwidth; the tensor-core path reads it once
 // per 16-row block step but needs 16-row tiles and a larger staged activation.  Measured on
 // GB300 (back-to-back, DRAM-cold): tensor cores win from m = 6 on every shape (17408 x 5120,
-// m = 8: 23 us against 51 us) and from m = 3 when the activation is small enough to keep
-// several CTAs per SM and there are enough rows (17408 x 5120, m = 4: 23 against 30 us); with
-// a 17408-wide activation at m = 3-4, or 1024 rows, dp4a stays faster.
+// m = 8: 23 us against 49 us; 5120 x 17408, m = 6: 38 against 47 us) and from m = 3 when the
+// activation is small enough to keep several CTAs per SM and there are many rows (17408 x
+// 5120, m = 3: 23.4 against 25.2 us; m = 4: 22.7 against 30.2 us).  With 5120 rows the
+// tensor-core launch has a floor of ~12.4 us (16-row tiles leave CTAs with one full and one
+// ragged tile), so dp4a stays ahead up to m = 4 there (10.9 against 12.5 us at m = 4); with a
+// 17408-wide activation at m = 3-5, or 1024 rows, dp4a is as fast or faster.
 inline bool q80_on_tensor_cores(int64_t out_f, int64_t in_f, int m) {
     if (m >= 6) return true;
-    return m >= kQ80MmaMinM && m * in_f <= 40960 && out_f >= 2048;
+    if (m < kQ80MmaMinM || m * in_f > 40960 || out_f < 2048) return false;
+    return m >= 5 || out_f >= 8192;
 }
 
 // Q8_0 with dp4a: rows per consumer warp in a tile (q80_pair_row: the two half-warps take two
@@ -218,7 +222,7 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
             if (g < M) {
                 if (MODE == kActFrag) {
-                    const uint4 v = bfrag[(kb * M + g) * 4 + t];
+                    const uint4 v = bfrag[(g * (a.nb | 1) + kb) * 4 + t];
                     bq[0] = v.x;
                     bq[1] = v.y;
                     bq[2] = v.z;
@@ -314,7 +318,7 @@ __device__ __forceinline__ void mma_stage_q80(const StreamArgs &a, const uint8_t
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
             if (g < M) {
                 if (MODE == kActFrag) {
-                    const uint4 v = bfrag[(kb * M + g) * 4 + t];
+                    const uint4 v = bfrag[(g * (a.nb | 1) + kb) * 4 + t];
                     bq[0] = v.x;
                     bq[1] = v.y;
                     bq[2] = v.z;
@@ -770,19 +774,38 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
             for (int k = 0; k < 9; ++k) dst[i * kQ8ActWords + k] = o[k];
         }
     } else if (MODE == kActFrag) {
-        // f16 MMA B fragments of the whole activation: entry (kb, g, t) holds
-        // q[g][32kb + 8t .. 8t+7] as four f16x2 registers.
+        // f16 MMA B fragments of the whole activation, built in place: entry (g, kb, t) = uint4
+        // (g * (nb | 1) + kb) * 4 + t holds q[g][32kb + 8t .. 8t+7] as four f16x2 registers
+        // (token rows of an odd number of 64-byte blocks, so the two tokens of a quarter-warp's
+        // 16-byte loads fall on different bank halves).  The int8 activation was staged at the
+        // top of the same region: item j = (g * nb + kb) * 4 + t reads 8 bytes at
+        // off_qs + 8j = off_bfrag + 8n + 64PM + 8j (n = 4 nb M items, P = (nb | 1) - nb) and
+        // writes 16 bytes at off_bfrag + 16j + 64Pg; that write can only overlap the sources of
+        // items j' <= j.  So items are converted in increasing order, in chunks whose sources
+        // are all read into registers before the chunk's first write.
         uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);
+        const uint8_t *src = smem + a.off_qs;
         const int n = a.nb * M * 4;
-        for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
-            const int t = i & 3;
-            const int g = (i >> 2) % M;
-            const int kb = (i >> 2) / M;
-            const uint2 qv = lds64(smem + a.off_qs + g * a.in_f + 32 * kb + 8 * t);
-            uint4 v;
-            s8x4_to_f16x2x2(qv.x, v.x, v.y);
-            s8x4_to_f16x2x2(qv.y, v.z, v.w);
-            bfrag[i] = v;
+        const int pad = 4 * ((a.nb | 1) - a.nb);
+        constexpr int kR = 4;
+        for (int j0 = 0; j0 < n; j0 += kR * kConsumerThreads) {
+            uint2 qv[kR];
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const int j = j0 + r * kConsumerThreads + threadIdx.x;
+                qv[r] = j < n ? lds64(src + 8 * j) : make_uint2(0u, 0u);
+            }
+            named_barrier_consumers();
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const int j = j0 + r * kConsumerThreads + threadIdx.x;
+                if (j < n) {
+                    uint4 v;
+                    s8x4_to_f16x2x2(qv[r].x, v.x, v.y);
+                    s8x4_to_f16x2x2(qv[r].y, v.z, v.w);
+                    bfrag[j + pad * (j / (4 * a.nb))] = v;
+                }
+            }
         }
     }
     named_barrier_consumers();
@@ -1223,8 +1246,13 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     const int grid_rows = static_cast<int>(rows_cta / 128 + 2);
     const int gcols = static_cast<int>((in_f + 127) / 128);
     const uint32_t gridb = KIND == kBlk ? align_up(static_cast<uint32_t>(grid_rows * gcols * 4), 128) : 0u;
-    const uint32_t frag = align_up(static_cast<uint32_t>(nb * m * (KIND == kQ80 ? 4 * kQ8ActWords : 64)), 128);
+    // Activation staging: the dp4a layout (Q8_0) sits beside the staged int8 qs; the f16 MMA
+    // fragments (E4M3 / block-128 / Q8_0 on the tensor cores) are built in place over it, so
+    // their region holds the qs at its top and no separate qs region is needed.
+    const uint32_t frag = G::kMma ? align_up(static_cast<uint32_t>(m * (nb | 1) * 64), 128)
+                                  : align_up(static_cast<uint32_t>(nb * m * 4 * kQ8ActWords), 128);
     const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
+    const uint32_t frag_act = G::kMma ? frag : frag + qsb;
     const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
     // block-128 with a staged activation: the CTA's d * grid table
     const uint32_t red = fuse ? align_up((kWarps + 1) * 8, 128) : 0u;
@@ -1255,7 +1283,7 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     for (int k = k_rows; k >= 1; --k) {
         // Shared memory one CTA may use and still leave room for k CTAs per SM.
         const uint32_t budget = std::min(optin, static_cast<uint32_t>(info.smem_sm / k - 1024));
-        if (base + qsb + db + frag <= budget) {
+        if (base + frag_act + db <= budget) {
             mode = kActFrag;
         } else if (base + qsb + db <= budget) {
             mode = kActSmem;
@@ -1273,8 +1301,13 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     uint32_t off = a.off_grid + gridb;
     a.off_bfrag = off;
     if (mode == kActFrag) off += frag;
-    a.off_qs = off;
-    if (mode != kActGlobal) off += qsb;
+    if (G::kMma && mode == kActFrag) {
+        // the int8 qs at the top of the fragment region (16-byte aligned: 32 nb m + 64 P m)
+        a.off_qs = a.off_bfrag + static_cast<uint32_t>(m * (nb | 1) * 64 - m * in_f);
+    } else {
+        a.off_qs = off;
+        if (mode != kActGlobal) off += qsb;
+    }
     a.off_d = off;
     if (mode != kActGlobal) off += db;
     a.off_red = off;

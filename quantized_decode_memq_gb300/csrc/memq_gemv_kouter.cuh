@@ -214,34 +214,44 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
             tma_prefetch_map(&maps.w8[mi]);
             tma_prefetch_map(&maps.qs);
             tma_prefetch_map(&maps.d);
-            // Bytes item `it`'s weight copies complete: boxed rows whole slots (box = slot
-            // bytes), the 1-7 rows left over only the chunk's weight bytes.
-            auto weight_bytes = [&](int it) -> uint32_t {
-                const int p = it / nch, ch = it - p * nch;
+            // The item cursor walks (pass, K-chunk) in order without divisions: the single
+            // producer thread shares its SM sub-partition with busy consumer warps, so a long
+            // dependent chain per stage (64-bit divisions) would delay every copy it issues.
+            const int last_nbytes = (a.nb - (nch - 1) * kKoKw) * 32;
+            const int box_rows = a.box_rows[mi];
+            struct Cursor {
+                int p, ch, rows, boxed;
+                int64_t P0;
+            };
+            auto start_pass = [&](Cursor &c, int p) {
                 int64_t P0, P1;
                 ko_pass_rows(R0, R1, npass, p, P0, P1);
-                const int rows = static_cast<int>(P1 - P0);
-                const int boxed = min(rows, a.box_rows[mi]);
-                const uint32_t nbytes = static_cast<uint32_t>(min(kKoKw, a.nb - ch * kKoKw) * 32);
-                return static_cast<uint32_t>(boxed * kKoSlot) + nbytes * static_cast<uint32_t>(rows - boxed);
+                c.p = p;
+                c.ch = 0;
+                c.P0 = P0;
+                c.rows = static_cast<int>(P1 - P0);
+                c.boxed = min(c.rows, box_rows);
             };
-            auto issue_weights = [&](int it, int s) {
-                const int p = it / nch, ch = it - p * nch;
-                int64_t P0, P1;
-                ko_pass_rows(R0, R1, npass, p, P0, P1);
-                const int rows = static_cast<int>(P1 - P0);
-                const int kb = ch * kKoKw;
-                uint8_t *dst = ring + static_cast<int64_t>(s) * a.stage;
-                const int boxed = min(rows, a.box_rows[mi]);
-                tma_load_2d(dst, &maps.w8[mi], kb * 4, static_cast<int>(P0), &full[s], pol);
-                const uint32_t nbytes = static_cast<uint32_t>(min(kKoKw, a.nb - kb) * 32);
-                for (int r = boxed; r < rows; ++r)
-                    bulk_g2s(dst + r * kKoSlot, w + (P0 + r) * a.row_bytes + static_cast<int64_t>(kb) * 32,
-                             nbytes, &full[s], pol);
+            auto advance = [&](Cursor &c) {
+                if (++c.ch == nch) start_pass(c, c.p + 1);
             };
-            auto issue_act = [&](int it, int s) {
-                const int ch = it % nch;
-                uint8_t *dst = ring + static_cast<int64_t>(s) * a.stage;
+            // Bytes the item's weight copies complete: boxed rows whole slots (box = slot bytes),
+            // the rows left over only the chunk's weight bytes.
+            auto weight_bytes = [&](const Cursor &c) -> uint32_t {
+                const int nbytes = c.ch == nch - 1 ? last_nbytes : kKoKw * 32;
+                return static_cast<uint32_t>(c.boxed * kKoSlot + nbytes * (c.rows - c.boxed));
+            };
+            auto issue_weights = [&](const Cursor &c, int s) {
+                const int kb = c.ch * kKoKw;
+                uint8_t *dst = ring + s * a.stage;
+                tma_load_2d(dst, &maps.w8[mi], kb * 4, static_cast<int>(c.P0), &full[s], pol);
+                const uint32_t nbytes = static_cast<uint32_t>(c.ch == nch - 1 ? last_nbytes : kKoKw * 32);
+                const uint8_t *src = w + c.P0 * a.row_bytes + static_cast<int64_t>(kb) * 32;
+                for (int r = c.boxed; r < c.rows; ++r)
+                    bulk_g2s(dst + r * kKoSlot, src + r * a.row_bytes, nbytes, &full[s], pol);
+            };
+            auto issue_act = [&](int ch, int s) {
+                uint8_t *dst = ring + s * a.stage;
                 tma_load_2d_plain(dst + a.act_qs, &maps.qs, ch * kKoKw * 4, 0, &full[s]);
                 tma_load_2d_plain(dst + a.act_d, &maps.d, ch * kKoKw, 0, &full[s]);
             };
@@ -250,25 +260,36 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
             // activation chunks follow with the arrival.  The bounded waits for released stages
             // start only after that, so a long predecessor never counts against this launch.
             const int pre = min(S, items);
+            Cursor c;
+            start_pass(c, 0);
             for (int it = 0; it < pre; ++it) {
-                mbar_expect_tx(&full[it], weight_bytes(it));
-                issue_weights(it, it);
+                mbar_expect_tx(&full[it], weight_bytes(c));
+                issue_weights(c, it);
+                advance(c);
             }
             griddep_wait();
-            for (int it = 0; it < pre; ++it) {
+            for (int it = 0, ch = 0; it < pre; ++it) {
                 mbar_arrive_expect_tx(&full[it], static_cast<uint32_t>(a.act_bytes));
-                issue_act(it, it);
+                issue_act(ch, it);
+                if (++ch == nch) ch = 0;
             }
+            // Item it >= S goes to stage it % S once its use it / S - 1 has been released
+            // (empty-barrier phase it / S - 1, parity ep).
+            int s = 0;
+            uint32_t ep = 0;
             for (int it = pre; it < items; ++it) {
-                // stage it % S, use it / S: waits for phase it / S - 1 of its empty barrier
-                const int s = it % S;
-                if (!thread_wait_bounded(&empty[s], static_cast<uint32_t>((it / S - 1) & 1))) {
+                if (!thread_wait_bounded(&empty[s], ep)) {
                     fault(2u);
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], weight_bytes(it) + static_cast<uint32_t>(a.act_bytes));
-                issue_weights(it, s);
-                issue_act(it, s);
+                mbar_arrive_expect_tx(&full[s], weight_bytes(c) + static_cast<uint32_t>(a.act_bytes));
+                issue_weights(c, s);
+                issue_act(c.ch, s);
+                advance(c);
+                if (++s == S) {
+                    s = 0;
+                    ep ^= 1u;
+                }
             }
         }
         return;
@@ -369,15 +390,15 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
 // per pass, K-chunks of 32 blocks, one tensor copy per stage), and an activation of at least
 // kKoMinAct = m * in_f bytes -- the size from which the tile kernel's per-CTA staging (1.125 to
 // 3.125 bytes per activation byte) costs ring stages or CTAs per SM.  Measured on GB300
-// (back-to-back launches, us, K-outer against the tile kernel): 5120 x 17408 m = 1 21.5 / 17.2,
-// m = 2 21.8 / 25.8, m = 4 21.8 / 30.1, m = 8 22.7 / 27.0; 5120 x 5120 m = 2 8.1 / 7.1, m = 4
-// 7.7 / 10.1, m = 8 8.1 / 9.7.  Below the threshold the tile kernel's once-per-CTA activation
-// fragments beat K-outer's per-stage fragment conversion.  Larger CTAs stay on the tile
-// kernel: with 57-row CTAs the narrow chunks a stage then needs (256 bytes per row, ten copies
-// per stage) stream at only 57% of the copy peak even with the compute removed.
+// (back-to-back launches, E4M3, us, K-outer against the tile kernel): 5120 x 17408 m = 1 16.7 /
+// 17.2, m = 2 17.5 / 25.8, m = 4 17.4 / 26.2; 5120 x 5120 m = 1 7.6 / 6.5, m = 2 7.8 / 7.3,
+// m = 4 7.4 / 9.6.  Below the threshold the tile kernel's once-per-CTA activation fragments
+// beat K-outer's per-stage fragment conversion.  Larger CTAs stay on the tile kernel: 17408 x
+// 5120 in 16-row passes at three CTAs per SM gives m = 4 16.9 / 17.0 but m = 8 19.6 / 18.0, at
+// two CTAs per SM 17.9 / 17.0 and 18.4 / 18.0.
 constexpr int kKoCtasPerSm = 3;
 constexpr int kKoTiles = 1;
-constexpr int64_t kKoMinAct = 18432;
+constexpr int64_t kKoMinAct = 16384;
 std::atomic<uint64_t> g_ko_attr[2][kMaxDevices];  // [E4M3, block-128]: bit per m set
 
 // Encodes (or finds in the cache) a 2-D tensor map over `base` viewed as [rows][cols] elements

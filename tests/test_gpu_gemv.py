@@ -150,6 +150,21 @@ def test_m_batched_bit_parity(memq, oracle, kind):
             assert torch.equal(y8[j].view(torch.int32), y1[0].view(torch.int32))
 
 
+@pytest.mark.parametrize("kind", ["e4m3", "blk"])
+def test_m_batched_bit_parity_across_kernels(memq, oracle, kind):
+    """5120 x 5120: m = 1 runs the tile kernel and m = 8 the K-outer kernel (11-row CTAs, the
+    activation streamed with the weights); every row of the m = 8 call equals the m = 1 call
+    on that activation row, bit for bit.  Also 5120 x 17408, where m = 1 and m = 4 both run
+    K-outer."""
+    for out_f, in_f, mb in ((5120, 5120, 8), (5120, 17408, 4)):
+        w, aux = weights(kind, out_f, in_f, 21)
+        qs, d = act(oracle, mb, in_f, 77)
+        yb = gpu_gemv(memq, kind, w, aux, qs, d)
+        for j in (0, mb - 1):
+            y1 = gpu_gemv(memq, kind, w, aux, qs[j:j + 1], d[j:j + 1])
+            assert torch.equal(yb[j].view(torch.int32), y1[0].view(torch.int32))
+
+
 def test_page_generators(memq, oracle):
     """The pages' own generators: LCG E4M3 (no NaN), the discrete 2^-6..2^-2 grid, and the
     fixed-scale Q8_0 whose qs cover the full int8 range including -128."""
