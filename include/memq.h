@@ -97,12 +97,17 @@ int memq_rmsnorm_q8_1(const float *x, const float *w, float *z, int8_t *qs, floa
  *   is a no-op that accepts NULL pointers.
  * The fast path wants w and qs 16-byte aligned; other alignments take a slower generic kernel
  * with the same results contract.
- * Numerics (all three containers): each 32-block product of weights and activation codes is
- * exact (products of exactly represented values; Q8_0 an int32 dot product), scaled by d (and
- * the grid entry / f16 block scale) and summed in f32 in a fixed order per (row, token).  On the
- * fast path that order does not depend on m, on how the launch splits the rows, or on which of
- * the library's kernels serves the call: a row's outputs are bit-identical whether it is
- * computed alone, in an m-batch, or in a group.
+ * Numerics (all three containers): a 32-block's product of weights and activation codes is
+ * formed on the tensor cores from exactly converted operands (E4M3 -> f16 and int8 -> f16 are
+ * exact, products exact in f32, f32 accumulation), or for Q8_0 at small m as an exact int32
+ * dp4a dot product; it is scaled by d (and the grid entry / f16 block scale) and summed in f32
+ * in a fixed order per (row, token).  E4M3 and block-128: on the fast path that order does not
+ * depend on m, on how the launch splits the rows, or on which of the library's kernels serves
+ * the call, so a row's outputs are bit-identical whether it is computed alone, in an m-batch,
+ * or in a group.
+ * Q8_0: the same holds within each of its two paths (dp4a; tensor cores from m = 3 on large
+ * shapes, m = 5 or 6 on others); across them the block sums are the same exact integers added
+ * in another order, and results agree within the GEMV tolerance.
  */
 int memq_gemv_e4m3(const uint8_t *w, const float *w_scale, const int8_t *qs, const float *d,
                    float *y, int64_t out_f, int64_t in_f, int m, void *stream);

@@ -787,6 +787,9 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
         const uint8_t *src = smem + a.off_qs;
         const int n = a.nb * M * 4;
         const int pad = 4 * ((a.nb | 1) - a.nb);
+        // token of item j: j / (4 nb) as a multiply-high by ceil(2^32 / (4 nb)), exact here since
+        // j * 4nb < 2^32 (n <= 14.5K items fit the shared memory)
+        const uint32_t magic = 0xFFFFFFFFu / static_cast<uint32_t>(4 * a.nb) + 1u;
         constexpr int kR = 4;
         for (int j0 = 0; j0 < n; j0 += kR * kConsumerThreads) {
             uint2 qv[kR];
@@ -803,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
                     uint4 v;
                     s8x4_to_f16x2x2(qv[r].x, v.x, v.y);
                     s8x4_to_f16x2x2(qv[r].y, v.z, v.w);
-                    bfrag[j + pad * (j / (4 * a.nb))] = v;
+                    bfrag[j + pad * static_cast<int>(__umulhi(static_cast<uint32_t>(j), magic))] = v;
                 }
             }
         }
@@ -1462,6 +1465,78 @@ int group_entry(int count, const uint8_t *const *w, const float *const *aux, flo
     const cudaError_t e = launch_planned<KIND, false>(m, mode, a, smem, dev, info,
                                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+}
+
+// Q8_0 calls choose between two arithmetics: the tensor-core paths (the K-outer kernel and the
+// tile kernel's kQ80T, bit-identical to each other) and dp4a.  The tensor cores serve a call
+// when K-outer applies (q80_kouter_applies: m >= 3 on CTAs of 8 to 16 rows) or when
+// q80_on_tensor_cores says so; K-outer is tried first.
+inline bool q80_tensor_path(int nmat, const int64_t *out_f, int64_t rows_all, int64_t in_f, int m,
+                            const int8_t *qs, const float *d, const DeviceInfo &info) {
+    return q80_kouter_applies(nmat, out_f, in_f, m, qs, d, info) ||
+           q80_on_tensor_cores(rows_all, in_f, m);
+}
+
+inline int q80_gemv_entry(const uint8_t *w, const int8_t *qs, const float *d, float *y,
+                          int64_t out_f, int64_t in_f, int m, void *stream) {
+    const int rc = check_gemv_args<kQ80>(w, nullptr, qs, d, y, out_f, in_f, m);
+    if (rc >= 0) return rc;
+    int dev = 0;
+    DeviceInfo info;
+    if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
+    if (fast_path_ok<kQ80T>(w, qs, in_f) && q80_kouter_applies(1, &out_f, in_f, m, qs, d, info)) {
+        const float *aux = nullptr;
+        const cudaError_t ek = launch_kouter_m<kQ80T>(m, 1, &w, &aux, &y, &out_f, qs, d, in_f, dev,
+                                                      info, static_cast<cudaStream_t>(stream));
+        if (ek != cudaErrorNotSupported) return ek == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+        // a ring too shallow for the K-outer plan: the tile kernel's tensor-core path
+        return gemv_entry<kQ80T>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
+    }
+    if (q80_on_tensor_cores(out_f, in_f, m))
+        return gemv_entry<kQ80T>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
+    return gemv_entry<kQ80>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
+}
+
+// A Q8_0 group runs as one launch only if its path (tensor cores or dp4a) is the one each of its
+// matrices takes alone, so that every output equals the single call bit for bit; otherwise it
+// runs one call per matrix.
+inline int q80_group_entry(int count, const uint8_t *const *w, float *const *y,
+                           const int64_t *out_f, const int8_t *qs, const float *d, int64_t in_f,
+                           int m, void *stream) {
+    if (count < 1 || count > kMaxGroup) return MEMQ_ERR_SHAPE;
+    if (!w || !y || !out_f) return MEMQ_ERR_NULL;
+    int64_t rows_all = 0;
+    bool fast = true;
+    for (int i = 0; i < count; ++i) {
+        const int rc = check_gemv_args<kQ80>(w[i], nullptr, qs, d, y[i], out_f[i], in_f, m);
+        if (rc > 0) return rc;
+        if (rc == MEMQ_OK) return MEMQ_ERR_SHAPE;  // an empty matrix in a group
+        rows_all += out_f[i];
+        fast = fast && fast_path_ok<kQ80T>(w[i], qs, in_f);
+    }
+    int dev = 0;
+    DeviceInfo info;
+    if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
+    const bool tensor = q80_tensor_path(count, out_f, rows_all, in_f, m, qs, d, info);
+    bool same = fast;
+    for (int i = 0; i < count && same; ++i)
+        same = q80_tensor_path(1, &out_f[i], out_f[i], in_f, m, qs, d, info) == tensor;
+    if (same && tensor && q80_kouter_applies(count, out_f, in_f, m, qs, d, info)) {
+        const float *aux[kMaxGroup] = {};
+        const cudaError_t ek = launch_kouter_m<kQ80T>(m, count, w, aux, y, out_f, qs, d, in_f, dev,
+                                                      info, static_cast<cudaStream_t>(stream));
+        if (ek != cudaErrorNotSupported) return ek == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
+        same = m >= kQ80MmaMinM;
+    }
+    if (!same) {
+        for (int i = 0; i < count; ++i) {
+            const int rc = q80_gemv_entry(w[i], qs, d, y[i], out_f[i], in_f, m, stream);
+            if (rc != MEMQ_OK) return rc;
+        }
+        return MEMQ_OK;
+    }
+    if (tensor) return group_entry<kQ80T>(count, w, nullptr, y, out_f, qs, d, in_f, m, stream);
+    return group_entry<kQ80>(count, w, nullptr, y, out_f, qs, d, in_f, m, stream);
 }
 
 // The fused decode step: RMSNorm -> q8_1 of x (m rows) and the GEMV in one launch when the plan

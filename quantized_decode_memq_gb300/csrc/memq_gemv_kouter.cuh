@@ -38,7 +38,16 @@ constexpr int kKoMaxTiles = 4;
 constexpr int kKoMinStages = 3;
 constexpr int kKoMaxStages = 12;
 constexpr int kKoKw = 32;                // 32-blocks per stage: the tile kernel's chunk
-constexpr int kKoSlot = kKoKw * 32 + 32;  // bytes per weight row in a stage
+// Per container: bytes of a 32-weight block, of a row's K-chunk, and of a row slot in a stage
+// (the chunk plus padding that keeps the consumers' fragment loads bank-conflict free: E4M3 /
+// block-128 rows 32 bytes apart modulo the 128-byte bank period, Q8_0 rows 80, as in the tile
+// kernel).
+template <int KIND>
+struct KoGeo {
+    static constexpr int kBlockBytes = KIND == kQ80T ? 34 : 32;
+    static constexpr int kChunk = kKoKw * kBlockBytes;
+    static constexpr int kSlot = kChunk + (KIND == kQ80T ? 16 : 32);
+};
 
 struct KoArgs {
     int nmat;
@@ -93,11 +102,70 @@ __device__ __forceinline__ void ko_pass_rows(int64_t R0, int64_t R1, int npass, 
 // ro[rt][0 / 1]: byte offsets of this thread's rows 16rt + g and 16rt + g + 8 in the stage, both
 // clamped to the pass's last row (rows past it are computed from a valid row and never stored,
 // and no load leaves the stage's weight region).
+// Q8_0 on the tensor cores: the same share of a stage with A = the int8 weights of the pass's
+// rows (int8 -> f16 exact) and each block's (row, token) result scaled by d_w[row] * d_x[token]
+// -- per (row, token) exactly the tile kernel's Q8_0 tensor-core operations in its order
+// (mma_stage_q80), so either kernel may serve a call.  The warp's four records start 136w bytes
+// into each 1104-byte row slot, so a record's weight bytes are 4-byte aligned for odd blocks and
+// 2 mod 4 for even ones (q80_weights8).
+template <int M, int TILES, bool FULL>
+__device__ __forceinline__ void ko_stage_q80(const KoArgs &a, const uint8_t *stage, int T,
+                                             const int (&ro)[TILES][2], int kbc, int warp,
+                                             int lane, float (&acc)[TILES][4]) {
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int j0 = 4 * warp;
+    const int nblk = FULL ? 4 : min(4, a.nb - kbc - j0);
+    if (!FULL && nblk <= 0) return;
+    const uint8_t *aq = stage + a.act_qs + g * (kKoKw * 32) + 32 * j0 + 8 * t;
+    const float *ad = reinterpret_cast<const float *>(stage + a.act_d) + 2 * t * kKoKw + j0;
+    const uint8_t *pa = stage + 34 * j0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        if (FULL || b < nblk) {
+            uint32_t bq[4] = {0u, 0u, 0u, 0u};
+            if (g < M) {
+                const uint2 qv = lds64(aq + 32 * b);
+                s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
+                s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
+            }
+            const float k0 = 2 * t < M ? ad[b] : 0.f;
+            const float k1 = 2 * t + 1 < M ? ad[kKoKw + b] : 0.f;
+#pragma unroll
+            for (int rt = 0; rt < TILES; ++rt) {
+                if (TILES == 1 || rt < T) {
+                    const uint8_t *r0 = pa + ro[rt][0] + 34 * b;
+                    const uint8_t *r8 = pa + ro[rt][1] + 34 * b;
+                    const float dw0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(r0))));
+                    const float dw8 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16(r8))));
+                    const uint2 wa = q80_weights8(r0 + 8 * t, b & 1);
+                    const uint2 wb = q80_weights8(r8 + 8 * t, b & 1);
+                    uint32_t a0, a1, a2, a3;
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+                    s8x4_to_f16x2x2(wa.x, a0, a2);
+                    s8x4_to_f16x2x2(wb.x, a1, a3);
+                    mma_f16_16816(c, a0, a1, a2, a3, bq[0], bq[1]);
+                    s8x4_to_f16x2x2(wa.y, a0, a2);
+                    s8x4_to_f16x2x2(wb.y, a1, a3);
+                    mma_f16_16816(c, a0, a1, a2, a3, bq[2], bq[3]);
+                    acc[rt][0] = fmaf(c[0], dw0 * k0, acc[rt][0]);
+                    acc[rt][1] = fmaf(c[1], dw0 * k1, acc[rt][1]);
+                    acc[rt][2] = fmaf(c[2], dw8 * k0, acc[rt][2]);
+                    acc[rt][3] = fmaf(c[3], dw8 * k1, acc[rt][3]);
+                }
+            }
+        }
+    }
+}
+
 template <int KIND, int M, int TILES, bool FULL>
 __device__ __forceinline__ void ko_stage(const KoArgs &a, const uint8_t *stage, const float *s_grid,
                                          int64_t P0, int64_t P1, int64_t grow_base, int T,
                                          const int (&ro)[TILES][2], int kbc, int warp, int lane,
                                          float (&acc)[TILES][4]) {
+    if constexpr (KIND == kQ80T) {
+        ko_stage_q80<M, TILES, FULL>(a, stage, T, ro, kbc, warp, lane, acc);
+    } else {
     const int g = lane >> 2;
     const int t = lane & 3;
     const int j0 = 4 * warp;
@@ -160,6 +228,7 @@ __device__ __forceinline__ void ko_stage(const KoArgs &a, const uint8_t *stage, 
             }
         }
     }
+    }  // E4M3 / block-128
 }
 
 template <int KIND, int M, int TILES>
@@ -217,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
             // The item cursor walks (pass, K-chunk) in order without divisions: the single
             // producer thread shares its SM sub-partition with busy consumer warps, so a long
             // dependent chain per stage (64-bit divisions) would delay every copy it issues.
-            const int last_nbytes = (a.nb - (nch - 1) * kKoKw) * 32;
+            using KG = KoGeo<KIND>;
+            const int last_nbytes = (a.nb - (nch - 1) * kKoKw) * KG::kBlockBytes;
             const int box_rows = a.box_rows[mi];
             struct Cursor {
                 int p, ch, rows, boxed;
@@ -238,17 +308,17 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
             // Bytes the item's weight copies complete: boxed rows whole slots (box = slot bytes),
             // the rows left over only the chunk's weight bytes.
             auto weight_bytes = [&](const Cursor &c) -> uint32_t {
-                const int nbytes = c.ch == nch - 1 ? last_nbytes : kKoKw * 32;
-                return static_cast<uint32_t>(c.boxed * kKoSlot + nbytes * (c.rows - c.boxed));
+                const int nbytes = c.ch == nch - 1 ? last_nbytes : KG::kChunk;
+                return static_cast<uint32_t>(c.boxed * KG::kSlot + nbytes * (c.rows - c.boxed));
             };
             auto issue_weights = [&](const Cursor &c, int s) {
                 const int kb = c.ch * kKoKw;
                 uint8_t *dst = ring + s * a.stage;
-                tma_load_2d(dst, &maps.w8[mi], kb * 4, static_cast<int>(c.P0), &full[s], pol);
-                const uint32_t nbytes = static_cast<uint32_t>(c.ch == nch - 1 ? last_nbytes : kKoKw * 32);
-                const uint8_t *src = w + c.P0 * a.row_bytes + static_cast<int64_t>(kb) * 32;
+                tma_load_2d(dst, &maps.w8[mi], kb * KG::kBlockBytes / 8, static_cast<int>(c.P0), &full[s], pol);
+                const uint32_t nbytes = static_cast<uint32_t>(c.ch == nch - 1 ? last_nbytes : KG::kChunk);
+                const uint8_t *src = w + c.P0 * a.row_bytes + static_cast<int64_t>(kb) * KG::kBlockBytes;
                 for (int r = c.boxed; r < c.rows; ++r)
-                    bulk_g2s(dst + r * kKoSlot, src + r * a.row_bytes, nbytes, &full[s], pol);
+                    bulk_g2s(dst + r * KG::kSlot, src + r * a.row_bytes, nbytes, &full[s], pol);
             };
             auto issue_act = [&](int ch, int s) {
                 uint8_t *dst = ring + s * a.stage;
@@ -318,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
         int ro[TILES][2];
 #pragma unroll
         for (int rt = 0; rt < TILES; ++rt) {
-            ro[rt][0] = min(16 * rt + (lane >> 2), rows - 1) * kKoSlot;
-            ro[rt][1] = min(16 * rt + (lane >> 2) + 8, rows - 1) * kKoSlot;
+            ro[rt][0] = min(16 * rt + (lane >> 2), rows - 1) * KoGeo<KIND>::kSlot;
+            ro[rt][1] = min(16 * rt + (lane >> 2) + 8, rows - 1) * KoGeo<KIND>::kSlot;
         }
         float acc[TILES][4];
 #pragma unroll
@@ -399,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
 constexpr int kKoCtasPerSm = 3;
 constexpr int kKoTiles = 1;
 constexpr int64_t kKoMinAct = 16384;
-std::atomic<uint64_t> g_ko_attr[2][kMaxDevices];  // [E4M3, block-128]: bit per m set
+std::atomic<uint64_t> g_ko_attr[3][kMaxDevices];  // [E4M3, block-128, Q8_0]: bit per m set
 
 // Encodes (or finds in the cache) a 2-D tensor map over `base` viewed as [rows][cols] elements
 // of `esize` bytes (row stride `stride` bytes), box (bx, by).  `tag` separates the map kinds in
@@ -430,8 +500,35 @@ inline bool ko_map(CUtensorMap &map, int tag, const void *base, int64_t rows, in
     return true;
 }
 
-// Plans and launches the K-outer kernel for a group of nmat E4M3 / block-128 matrices sharing
-// one activation.  Returns cudaErrorNotSupported (nothing launched) when the K-outer path does
+// The most rows a CTA of the K-outer split holds: kKoCtasPerSm CTAs per SM, shared by the
+// matrices in proportion to their rows (the split launch_kouter makes).
+inline int64_t ko_rmax(int nmat, const int64_t *out_f, const DeviceInfo &info) {
+    const int64_t total = static_cast<int64_t>(info.sms) * kKoCtasPerSm;
+    int64_t rows_all = 0, rmax = 0;
+    for (int i = 0; i < nmat; ++i) rows_all += out_f[i];
+    for (int i = 0; i < nmat; ++i) {
+        int64_t n = (total * out_f[i] + rows_all - 1) / rows_all;
+        n = std::max<int64_t>(1, std::min<int64_t>(n, out_f[i]));
+        rmax = std::max(rmax, (out_f[i] + n - 1) / n);
+    }
+    return rmax;
+}
+
+// Whether a Q8_0 call (or group) runs K-outer on the tensor cores: m >= 3 and the activation
+// and CTA-size conditions of launch_kouter.  The Q8_0 entry points decide their path (tensor
+// cores or dp4a) with it before launching.  Measured on GB300 (back-to-back, us, K-outer against
+// dp4a): 5120 x 17408 m = 2 23.8 / 23.1, m = 3 25.3 / 29.2, m = 4 23.4 / 35.9, m = 8 26.9 /
+// 62.2; 5120 x 5120 m = 4 9.1 / 10.9, m = 8 9.5 / 19.9.
+inline bool q80_kouter_applies(int nmat, const int64_t *out_f, int64_t in_f, int m,
+                               const int8_t *qs, const float *d, const DeviceInfo &info) {
+    if (m < 3 || in_f % 128 != 0 || !aligned(qs, 16) || !aligned(d, 16) || m * in_f < kKoMinAct)
+        return false;
+    const int64_t r = ko_rmax(nmat, out_f, info);
+    return r >= 8 && r <= 16 * kKoTiles;
+}
+
+// Plans and launches the K-outer kernel for a group of nmat E4M3 / block-128 / Q8_0 matrices
+// sharing one activation.  Returns cudaErrorNotSupported (nothing launched) when the K-outer path does
 // not apply -- a CTA would get more than 16 rows, the activation scales cannot be copied as
 // tensor boxes (in_f % 128 != 0, or qs / d not 16-byte aligned), or the ring would be too
 // shallow -- and the caller falls back to the tile kernel.
@@ -439,14 +536,16 @@ template <int KIND, int M>
 cudaError_t launch_kouter(int nmat, const uint8_t *const *w, const float *const *aux,
                           float *const *y, const int64_t *out_f, const int8_t *qs, const float *d,
                           int64_t in_f, int dev, const DeviceInfo &info, cudaStream_t st) {
-    static_assert(KIND == kE4M3 || KIND == kBlk, "K-outer path: E4M3 and block-128 only");
+    static_assert(KIND == kE4M3 || KIND == kBlk || KIND == kQ80T,
+                  "K-outer path: E4M3, block-128 and Q8_0 on the tensor cores");
+    using KG = KoGeo<KIND>;
     constexpr int TILES = kKoTiles;
     constexpr int kPassRows = 16 * TILES;
     if (in_f % 128 != 0 || !aligned(d, 16) || !aligned(qs, 16) || M * in_f < kKoMinAct)
         return cudaErrorNotSupported;
     KoArgs a = {};
     a.nmat = nmat;
-    a.row_bytes = in_f;
+    a.row_bytes = in_f / 32 * KG::kBlockBytes;
     a.in_f = static_cast<int>(in_f);
     a.nb = static_cast<int>(in_f / 32);
     a.gcols = static_cast<int>((in_f + 127) / 128);
@@ -481,7 +580,7 @@ cudaError_t launch_kouter(int nmat, const uint8_t *const *w, const float *const 
     // CTAs of 8 to 16 rows: fewer rows leave stages mostly activation and tiles mostly padding
     // (1024 x 5120, m = 4: 8.2 us against 4.4 us on the tile kernel, which uses fewer CTAs there)
     if (rmax > kPassRows || rmax < 8) return cudaErrorNotSupported;
-    a.act_qs = static_cast<int>(align_up(static_cast<uint32_t>(pass_rows * kKoSlot), 128));
+    a.act_qs = static_cast<int>(align_up(static_cast<uint32_t>(pass_rows * KG::kSlot), 128));
     a.act_d = a.act_qs + static_cast<int>(align_up(static_cast<uint32_t>(M * kKoKw * 32), 128));
     a.stage = a.act_d + static_cast<int>(align_up(static_cast<uint32_t>(M * kKoKw * 4), 128));
     a.act_bytes = M * kKoKw * 32 + M * kKoKw * 4;
@@ -502,14 +601,15 @@ cudaError_t launch_kouter(int nmat, const uint8_t *const *w, const float *const 
 
     KoMaps maps = {};
     for (int i = 0; i < nmat; ++i)
-        if (!ko_map(maps.w8[i], 1, w[i], out_f[i], in_f / 8, in_f, 8, kKoSlot / 8, a.box_rows[i], dev))
+        if (!ko_map(maps.w8[i], 1, w[i], out_f[i], a.row_bytes / 8, a.row_bytes, 8, KG::kSlot / 8,
+                    a.box_rows[i], dev))
             return cudaErrorNotSupported;
     if (!ko_map(maps.qs, 2, qs, M, in_f / 8, in_f, 8, kKoKw * 4, M, dev) ||
         !ko_map(maps.d, 3, d, M, in_f / 32, in_f / 8, 4, kKoKw, M, dev))
         return cudaErrorNotSupported;
 
     auto kern = gemv_kouter_kernel<KIND, M, TILES>;
-    const int ki = KIND == kBlk ? 1 : 0;
+    const int ki = KIND == kBlk ? 1 : KIND == kQ80T ? 2 : 0;
     const uint64_t bit = 1ull << (M - 1);
     if (!(g_ko_attr[ki][dev].load(std::memory_order_acquire) & bit)) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -536,8 +636,13 @@ cudaError_t launch_kouter_m(int m, int nmat, const uint8_t *const *w, const floa
                             const float *d, int64_t in_f, int dev, const DeviceInfo &info,
                             cudaStream_t st) {
     switch (m) {
-        case 1: return launch_kouter<KIND, 1>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
-        case 2: return launch_kouter<KIND, 2>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
+        // Q8_0 at m <= 2 stays on dp4a (q80_kouter_applies)
+        case 1:
+            if constexpr (KIND == kQ80T) return cudaErrorNotSupported;
+            else return launch_kouter<KIND, 1>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
+        case 2:
+            if constexpr (KIND == kQ80T) return cudaErrorNotSupported;
+            else return launch_kouter<KIND, 2>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
         case 3: return launch_kouter<KIND, 3>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
         case 4: return launch_kouter<KIND, 4>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
         case 5: return launch_kouter<KIND, 5>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);

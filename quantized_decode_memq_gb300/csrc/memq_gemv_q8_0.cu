@@ -5,10 +5,7 @@
 
 extern "C" int memq_gemv_q8_0(const void *w, const int8_t *qs, const float *d, float *y,
                               int64_t out_f, int64_t in_f, int m, void *stream) {
-    const uint8_t *w8 = static_cast<const uint8_t *>(w);
-    if (memq::q80_on_tensor_cores(out_f, in_f, m))
-        return memq::gemv_entry<memq::kQ80T>(w8, nullptr, qs, d, y, out_f, in_f, m, stream);
-    return memq::gemv_entry<memq::kQ80>(w8, nullptr, qs, d, y, out_f, in_f, m, stream);
+    return memq::q80_gemv_entry(static_cast<const uint8_t *>(w), qs, d, y, out_f, in_f, m, stream);
 }
 
 extern "C" int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps,
@@ -29,14 +26,8 @@ extern "C" int memq_gemv_q8_0_group(int count, const void *const *w, float *cons
     if (count < 1 || count > memq::kMaxGroup) return MEMQ_ERR_SHAPE;
     if (!w || !out_f) return MEMQ_ERR_NULL;
     const uint8_t *w8[memq::kMaxGroup];
-    int64_t rows = 0;
-    for (int i = 0; i < count; ++i) {
-        w8[i] = static_cast<const uint8_t *>(w[i]);
-        rows += out_f[i];
-    }
-    if (memq::q80_on_tensor_cores(rows, in_f, m))
-        return memq::group_entry<memq::kQ80T>(count, w8, nullptr, y, out_f, qs, d, in_f, m, stream);
-    return memq::group_entry<memq::kQ80>(count, w8, nullptr, y, out_f, qs, d, in_f, m, stream);
+    for (int i = 0; i < count; ++i) w8[i] = static_cast<const uint8_t *>(w[i]);
+    return memq::q80_group_entry(count, w8, y, out_f, qs, d, in_f, m, stream);
 }
 
 // Internal: this translation unit's device fault word (not part of the public header).

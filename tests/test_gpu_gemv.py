@@ -150,19 +150,24 @@ def test_m_batched_bit_parity(memq, oracle, kind):
             assert torch.equal(y8[j].view(torch.int32), y1[0].view(torch.int32))
 
 
-@pytest.mark.parametrize("kind", ["e4m3", "blk"])
+@pytest.mark.parametrize("kind", KINDS)
 def test_m_batched_bit_parity_across_kernels(memq, oracle, kind):
-    """5120 x 5120: m = 1 runs the tile kernel and m = 8 the K-outer kernel (11-row CTAs, the
-    activation streamed with the weights); every row of the m = 8 call equals the m = 1 call
-    on that activation row, bit for bit.  Also 5120 x 17408, where m = 1 and m = 4 both run
-    K-outer."""
-    for out_f, in_f, mb in ((5120, 5120, 8), (5120, 17408, 4)):
+    """Rows of an m-batched call equal a smaller call on those activation rows, bit for bit,
+    where the two calls run different kernels.  E4M3 / block-128: 5120 x 5120 at m = 8 runs the
+    K-outer kernel (11-row CTAs, the activation streamed with the weights) and at m = 1 the
+    tile kernel; 5120 x 17408 runs K-outer at m = 4 and m = 1.  Q8_0 (tensor-core path, K-outer):
+    5120 x 5120 m = 8 against m = 4, 5120 x 17408 m = 4 against m = 3."""
+    cases = ((5120, 5120, 8, 1), (5120, 17408, 4, 1))
+    if kind == "q8_0":
+        cases = ((5120, 5120, 8, 4), (5120, 17408, 4, 3))
+    for out_f, in_f, mb, ms in cases:
         w, aux = weights(kind, out_f, in_f, 21)
         qs, d = act(oracle, mb, in_f, 77)
         yb = gpu_gemv(memq, kind, w, aux, qs, d)
         for j in (0, mb - 1):
-            y1 = gpu_gemv(memq, kind, w, aux, qs[j:j + 1], d[j:j + 1])
-            assert torch.equal(yb[j].view(torch.int32), y1[0].view(torch.int32))
+            sel = [(j + i) % mb for i in range(ms)]
+            ys = gpu_gemv(memq, kind, w, aux, qs[sel], d[sel])
+            assert torch.equal(yb[j].view(torch.int32), ys[0].view(torch.int32)), (out_f, in_f, j)
 
 
 def test_page_generators(memq, oracle):

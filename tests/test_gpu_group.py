@@ -62,7 +62,8 @@ def ref(oracle, kind, w, aux, qs, d, in_f, rows):
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("m", [1, 2, 8])
 @pytest.mark.parametrize("shapes,in_f", [((6144, 5120), 5120), ((17408, 17408), 5120),
-                                         ((37, 130, 1000), 1024 + 256), ((5120, 33, 700, 1), 2048)])
+                                         ((37, 130, 1000), 1024 + 256), ((5120, 33, 700, 1), 2048),
+                                         ((5120, 5120), 17408)])
 def test_group_equals_single_calls_and_oracle(memq, oracle, kind, m, shapes, in_f):
     x = synth.uniform_pm4(0x7700 + m, m * in_f).reshape(m, in_f)
     _, d, qs, _ = oracle.rmsnorm_q8_1(x, synth.uniform_pm4(0x7701, in_f))
