@@ -731,24 +731,64 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
     griddep_wait();
     bool ok = true;
     // The activation (written by the preceding launch): qs and d into shared memory with one
-    // bulk copy each (one L2 round trip), or computed here in the fused decode step.
+    // bulk copy each (one L2 round trip), or computed here in the fused decode step.  For the
+    // f16 MMA fragments (E4M3 / block-128 / Q8_0 on the tensor cores) of an activation of at most
+    // kDirectItems items the consumers read qs straight from global memory (at most three rounds
+    // of loads per thread) and write the fragments while d is copied; a larger one is staged and
+    // converted in place (measured on GB300: 4096 x 4096 m = 1 5.17 -> 4.98 us with the direct
+    // read, 1024 x 5120 m = 8 4.68 -> 4.86 us).
+    //
+    // Fragment layout: entry (g, kb, t) = uint4 (g * (nb | 1) + kb) * 4 + t holds
+    // q[g][32kb + 8t .. 8t+7] as four f16x2 registers (token rows of an odd number of 64-byte
+    // blocks, so the two tokens of a quarter-warp's 16-byte loads fall on different bank halves).
+    // Item j = (g * nb + kb) * 4 + t is 8 bytes of qs at byte 8j of [M][in_f].
+    constexpr bool kFragMma = G::kMma && MODE == kActFrag;
+    constexpr int kR = 4;  // items per thread in flight
+    constexpr int kDirectItems = 3 * kR * kConsumerThreads;
+    const int n_items = a.nb * M * 4;
+    const bool direct = kFragMma && !FUSE && n_items <= kDirectItems;
+    const int pad = 4 * ((a.nb | 1) - a.nb);
+    // token of item j: j / (4 nb) as a multiply-high by ceil(2^32 / (4 nb)), exact here since
+    // j * 4nb < 2^32 (n <= 14.5K items fit the shared memory)
+    const uint32_t magic = 0xFFFFFFFFu / static_cast<uint32_t>(4 * a.nb) + 1u;
+    uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);
+    auto frag_store = [&](int j, uint2 qv) {
+        uint4 v;
+        s8x4_to_f16x2x2(qv.x, v.x, v.y);
+        s8x4_to_f16x2x2(qv.y, v.z, v.w);
+        bfrag[j + pad * static_cast<int>(__umulhi(static_cast<uint32_t>(j), magic))] = v;
+    };
     if (FUSE) {
         double *s_red = reinterpret_cast<double *>(smem + a.off_red);  // [kWarps] + r
         fused_quantize<M>(a, reinterpret_cast<int8_t *>(smem + a.off_qs),
                           reinterpret_cast<float *>(smem + a.off_d), s_red,
                           reinterpret_cast<float *>(s_red + kWarps));
     } else if (MODE != kActGlobal) {
-        const uint32_t qbytes = static_cast<uint32_t>(M * a.in_f);
+        const uint32_t qbytes = direct ? 0u : static_cast<uint32_t>(M * a.in_f);
         const uint32_t dbytes = static_cast<uint32_t>(M * a.nb * 4);
         const bool d_bulk = (dbytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.d) & 15u) == 0;
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(act_bar, qbytes + (d_bulk ? dbytes : 0u));
-            bulk_g2s_plain(smem + a.off_qs, a.qs, qbytes, act_bar);
+            if (qbytes) bulk_g2s_plain(smem + a.off_qs, a.qs, qbytes, act_bar);
             if (d_bulk) bulk_g2s_plain(smem + a.off_d, a.d, dbytes, act_bar);
         }
         if (!d_bulk) {
             float *dst = reinterpret_cast<float *>(smem + a.off_d);
             for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldcg(a.d + i);
+        }
+        if (direct) {
+            const uint2 *src = reinterpret_cast<const uint2 *>(a.qs);
+            for (int j0 = threadIdx.x; j0 < n_items; j0 += kR * kConsumerThreads) {
+                uint2 qv[kR];
+#pragma unroll
+                for (int r = 0; r < kR; ++r) {
+                    const int j = j0 + r * kConsumerThreads;
+                    qv[r] = j < n_items ? __ldcg(src + j) : make_uint2(0u, 0u);
+                }
+#pragma unroll
+                for (int r = 0; r < kR; ++r)
+                    if (j0 + r * kConsumerThreads < n_items) frag_store(j0 + r * kConsumerThreads, qv[r]);
+            }
         }
         if (!warp_wait_bounded(act_bar, 0)) {
             // Record the fault; give the activation copy and the ring's first stages a bounded
@@ -773,41 +813,26 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
 #pragma unroll
             for (int k = 0; k < 9; ++k) dst[i * kQ8ActWords + k] = o[k];
         }
-    } else if (MODE == kActFrag) {
-        // f16 MMA B fragments of the whole activation, built in place: entry (g, kb, t) = uint4
-        // (g * (nb | 1) + kb) * 4 + t holds q[g][32kb + 8t .. 8t+7] as four f16x2 registers
-        // (token rows of an odd number of 64-byte blocks, so the two tokens of a quarter-warp's
-        // 16-byte loads fall on different bank halves).  The int8 activation was staged at the
-        // top of the same region: item j = (g * nb + kb) * 4 + t reads 8 bytes at
+    } else if (kFragMma && !direct) {
+        // qs (staged, or computed by the fused step) is at the top of the fragment region: item j
+        // reads 8 bytes at
         // off_qs + 8j = off_bfrag + 8n + 64PM + 8j (n = 4 nb M items, P = (nb | 1) - nb) and
-        // writes 16 bytes at off_bfrag + 16j + 64Pg; that write can only overlap the sources of
-        // items j' <= j.  So items are converted in increasing order, in chunks whose sources
-        // are all read into registers before the chunk's first write.
-        uint4 *bfrag = reinterpret_cast<uint4 *>(smem + a.off_bfrag);
+        // writes 16 bytes at off_bfrag + 16j + 64Pg, which can only overlap the sources of items
+        // j' <= j.  So items are converted in increasing order, in chunks whose sources are all
+        // read into registers before the chunk's first write.
         const uint8_t *src = smem + a.off_qs;
-        const int n = a.nb * M * 4;
-        const int pad = 4 * ((a.nb | 1) - a.nb);
-        // token of item j: j / (4 nb) as a multiply-high by ceil(2^32 / (4 nb)), exact here since
-        // j * 4nb < 2^32 (n <= 14.5K items fit the shared memory)
-        const uint32_t magic = 0xFFFFFFFFu / static_cast<uint32_t>(4 * a.nb) + 1u;
-        constexpr int kR = 4;
-        for (int j0 = 0; j0 < n; j0 += kR * kConsumerThreads) {
+        for (int j0 = 0; j0 < n_items; j0 += kR * kConsumerThreads) {
             uint2 qv[kR];
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
                 const int j = j0 + r * kConsumerThreads + threadIdx.x;
-                qv[r] = j < n ? lds64(src + 8 * j) : make_uint2(0u, 0u);
+                qv[r] = j < n_items ? lds64(src + 8 * j) : make_uint2(0u, 0u);
             }
             named_barrier_consumers();
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
                 const int j = j0 + r * kConsumerThreads + threadIdx.x;
-                if (j < n) {
-                    uint4 v;
-                    s8x4_to_f16x2x2(qv[r].x, v.x, v.y);
-                    s8x4_to_f16x2x2(qv[r].y, v.z, v.w);
-                    bfrag[j + pad * static_cast<int>(__umulhi(static_cast<uint32_t>(j), magic))] = v;
-                }
+                if (j < n_items) frag_store(j, qv[r]);
             }
         }
     }
