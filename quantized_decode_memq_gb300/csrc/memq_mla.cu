@@ -363,11 +363,29 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
     if (bulk)
         for (int c = 0; c < S - 1; ++c) issue_next();
 
-    float2 acc[KP][H];
+    // Output accumulators.  Blocked (H % 4 == 0 and at least 16 outputs per thread): thread tid
+    // owns heads 4 hg .. 4 hg + 3 (hg = tid / kTpg) and the dim quads dq + q kTpg (dq = tid %
+    // kTpg, q < kDq), so per gathered row one 16-byte load of the row and one of the 4 weights
+    // feed 16 FMAs per quad.  Otherwise thread tid owns the dim pairs 2(tid + 256 k) of every
+    // head.  The f32 operations per (head, dim) are the same either way.
+    constexpr bool kBlocked = H % 4 == 0 && H * KV >= 32;
+    constexpr int kNg = kBlocked ? H / 4 : 1;               // head groups of 4
+    constexpr int kTpg = kMlaThreads / kNg;                 // threads per head group
+    constexpr int kDq = kBlocked ? kv_rank / (4 * kTpg) : 1;  // dim quads per thread
+    const int hg = tid / kTpg, dq = tid - hg * kTpg;
+    float4 acc4[kDq][kBlocked ? 4 : 1];
+    float2 acc[kBlocked ? 1 : KP][kBlocked ? 1 : H];
+    if constexpr (kBlocked) {
 #pragma unroll
-    for (int k = 0; k < KP; ++k)
+        for (int q = 0; q < kDq; ++q)
 #pragma unroll
-        for (int hh = 0; hh < H; ++hh) acc[k][hh] = make_float2(0.f, 0.f);
+            for (int hh = 0; hh < 4; ++hh) acc4[q][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+#pragma unroll
+        for (int k = 0; k < KP; ++k)
+#pragma unroll
+            for (int hh = 0; hh < H; ++hh) acc[k][hh] = make_float2(0.f, 0.f);
+    }
 
     bool failed = false;  // this thread's wait for a stage gave up
     for (int c = 0; c < nchunks; ++c) {
@@ -375,13 +393,12 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
         const int nj = min(kRowsC, j_end - j0);
         const float *rows = ring + (bulk ? (c % S) * stage_f : 0);
         if (bulk) {
-            // stage (c - 1) % S was released by the barrier that ended chunk c - 1
-            issue_next();
             if (!warp_wait_bounded(&bars[c % S], static_cast<uint32_t>((c / S) & 1))) {
                 failed = true;
                 if (lane == 0) atomicOr(&g_mla_fault, kFaultAttnWait);
             }
         } else {
+            __syncthreads();  // every thread is done with the previous chunk's rows
             float *dst = ring;
             for (int i = tid; i < nj * row_len; i += kMlaThreads) {
                 const int j = i / row_len, k = i - j * row_len;
@@ -435,6 +452,9 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
         // The chunk's scores are complete; a wait that gave up anywhere stops every warp here,
         // together (the barrier's OR is the same in every thread).
         if (__syncthreads_or(failed)) break;
+        // Every thread has also finished chunk c - 1 (its accumulate precedes these scores), so
+        // stage (c - 1) % S is free: chunk c + S - 1 goes there.
+        if (bulk) issue_next();
         // Online softmax step: warp hh < H updates head hh, lane j < nj holding score j.  The
         // chunk's max is a shuffle max (exact), its weight sum a fixed xor tree over lanes 0-15.
         if (warp < H) {
@@ -457,7 +477,39 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
             }
         }
         __syncthreads();
-        // Accumulate: thread tid owns the dim pairs (2p, 2p + 1), p = tid + 256 k; one 8-byte
+        // Accumulate (the rescale by exp(m_old - m_new), then the chunk's rows in order).
+        if constexpr (kBlocked) {
+            const float4 al = reinterpret_cast<const float4 *>(sal)[hg];
+#pragma unroll
+            for (int q = 0; q < kDq; ++q) {
+                acc4[q][0].x *= al.x; acc4[q][0].y *= al.x; acc4[q][0].z *= al.x; acc4[q][0].w *= al.x;
+                acc4[q][1].x *= al.y; acc4[q][1].y *= al.y; acc4[q][1].z *= al.y; acc4[q][1].w *= al.y;
+                acc4[q][2].x *= al.z; acc4[q][2].y *= al.z; acc4[q][2].z *= al.z; acc4[q][2].w *= al.z;
+                acc4[q][3].x *= al.w; acc4[q][3].y *= al.w; acc4[q][3].z *= al.w; acc4[q][3].w *= al.w;
+            }
+            auto row_step = [&](int j) {
+                const float4 pv = reinterpret_cast<const float4 *>(pw + j * H)[hg];
+                const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                for (int q = 0; q < kDq; ++q) {
+                    const float4 rv = reinterpret_cast<const float4 *>(rows + j * row_pad)[dq + q * kTpg];
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        acc4[q][hh].x = fmaf(pj[hh], rv.x, acc4[q][hh].x);
+                        acc4[q][hh].y = fmaf(pj[hh], rv.y, acc4[q][hh].y);
+                        acc4[q][hh].z = fmaf(pj[hh], rv.z, acc4[q][hh].z);
+                        acc4[q][hh].w = fmaf(pj[hh], rv.w, acc4[q][hh].w);
+                    }
+                }
+            };
+            if (nj == kRowsC) {
+#pragma unroll
+                for (int j = 0; j < kRowsC; ++j) row_step(j);
+            } else {
+                for (int j = 0; j < nj; ++j) row_step(j);
+            }
+        } else {
+        // Thread tid owns the dim pairs (2p, 2p + 1), p = tid + 256 k; one 8-byte
         // load per row serves both dims.
 #pragma unroll
         for (int k = 0; k < KP; ++k) {
@@ -499,7 +551,9 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
                 }
             }
         }
-        __syncthreads();  // the stage and the chunk's weights are free again
+        }
+        // No barrier here: the next chunk's score barrier orders this accumulate before the
+        // stage's reuse and before the next softmax step rewrites the weights.
     }
     if (bulk && warp == 0) {
         // Every copy issued (by any warp: all issue in step) must land before the stages take
@@ -509,12 +563,20 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
     }
     __syncthreads();
     float *sacc = ring;  // this part's partial outputs [H][kv_rank] (fits one stage)
+    if constexpr (kBlocked) {
 #pragma unroll
-    for (int k = 0; k < KP; ++k) {
-        const int d = 2 * (tid + k * kMlaThreads);
-        if (d < kv_rank) {
+        for (int q = 0; q < kDq; ++q)
 #pragma unroll
-            for (int hh = 0; hh < H; ++hh) *reinterpret_cast<float2 *>(sacc + hh * kv_rank + d) = acc[k][hh];
+            for (int hh = 0; hh < 4; ++hh)
+                reinterpret_cast<float4 *>(sacc + (4 * hg + hh) * kv_rank)[dq + q * kTpg] = acc4[q][hh];
+    } else {
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+            const int d = 2 * (tid + k * kMlaThreads);
+            if (d < kv_rank) {
+#pragma unroll
+                for (int hh = 0; hh < H; ++hh) *reinterpret_cast<float2 *>(sacc + hh * kv_rank + d) = acc[k][hh];
+            }
         }
     }
     cluster_sync_all();
