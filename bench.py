@@ -219,6 +219,23 @@ def measured_peak_hbm():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# TF32 / bf16 dense tensor throughput ratio (nominal: 1.1 and 2.25 PFLOP/s per GB300)
+TF32_PER_BF16 = 1.1 / 2.25
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_peak_bf16():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = json.load(f).get("bf16_tflops")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 # ------------------------------------------------------------------------------------------
 # Workload
 # ------------------------------------------------------------------------------------------
@@ -1144,11 +1161,16 @@ def run_mla(args, world, rank, local, dev):
     t_launch, _ = aggregate(float(np.mean(per)), 1.0)
     if kernel in ("attn", "step"):
         achieved = wl.flops / t_launch / 1e12
-        peak = F32_FMA_TFLOPS
-        roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+        # The page geometry (d_rope 0, kv_rank 512) runs the tensor-core kernel: three TF32 MMA
+        # products per f32 product, so its peak is the TF32 rate / 3 in f32-equivalent FLOP.
+        bf16, kind = measured_peak_bf16()
+        peak = round(bf16 * TF32_PER_BF16 / 3.0, 1)
+        roof = {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": profiled_traffic(args.workload, "mla_traffic.json"),
-                "peak_kind": "derived: 152 SMs x 128 f32 FMA/clk x 2 FLOP x 2.07 GHz"}
+                "peak_kind": f"{kind} bf16 burst x 1.1/2.25 (TF32) / 3 (3xTF32 products per f32 product)",
+                "f32_alu_peak": F32_FMA_TFLOPS,
+                "f32_alu_frac": round(achieved / F32_FMA_TFLOPS, 4)}
         if kernel == "step":
             # the same kernels one at a time (each after its own scrub), for the overlap gain
             iso = []

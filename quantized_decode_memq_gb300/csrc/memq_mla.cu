@@ -604,6 +604,292 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, H 
     cluster_sync_all();  // no CTA leaves while another still reads its shared memory
 }
 
+// ------------------------------------------------------------------------------------------
+// Gathered attention on the tensor cores (d_rope == 0, kv_rank <= 512): the same cluster
+// schedule, slot ranges, online softmax and merge as attn_gathered_kernel, with both
+// contractions of a 16-row chunk as mma.sync.m16n8k8 TF32 products in three terms
+// (3xTF32): x = hi + lo with hi = x truncated to TF32 (exact) and lo = x - hi (exact in f32; the
+// MMA reads its TF32 part), and x y ~ lo_x hi_y + hi_x lo_y + hi_x hi_y, the dropped lo lo
+// term and the truncation of lo each below 2^-20 |x y|.
+//   scores: S[j][h] = sum_k c_j[k] q_h[k] with M = the chunk's 16 rows, N = 8 heads (the group's
+//     H, the rest zero), K = kv_rank split into 8 contiguous slices, one per warp; the 8 warp
+//     partials of each (j, h) are added in warp order by the softmax step.
+//   outputs: O[d][h] = O[d][h] al_h + sum_j c_j[d] p_j[h] with M = 16 dims (MMA rows g and g + 8
+//     = dims 2g and 2g + 1 of the tile), N = 8 heads, K = the chunk's rows in two k8 steps; warp w
+//     owns dims [w kv_rank / 8, (w + 1) kv_rank / 8).
+// Each output element of an MMA depends only on its own row of A and column of B, and the
+// K slicing, the k8 steps and the partial order do not depend on H, so the split twins stay
+// bit-identical.  Rows are kv_rank + 8 floats apart in shared memory (8 banks), which makes
+// every fragment load conflict-free.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
+    const uint32_t b = __float_as_uint(x) & 0xFFFFE000u;
+    hi = b;
+    lo = __float_as_uint(x - __uint_as_float(b));
+}
+
+__device__ __forceinline__ void mma_tf32_16808(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// c += A B in three TF32 terms, the small cross terms first.
+__device__ __forceinline__ void mma_3xtf32(float (&c)[4], const uint32_t (&ah)[4],
+                                           const uint32_t (&al)[4], uint32_t bh0, uint32_t bh1,
+                                           uint32_t bl0, uint32_t bl1) {
+    mma_tf32_16808(c, al, bh0, bh1);
+    mma_tf32_16808(c, ah, bl0, bl1);
+    mma_tf32_16808(c, ah, bh0, bh1);
+}
+
+constexpr int kTcHeads = 8;  // MMA N: the head columns of a group (H of them in use)
+
+template <int KV, int H>
+__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
+    attn_gathered_tc_kernel(const __grid_constant__ AttnArgs a) {
+    constexpr int kv_rank = KV * 128;
+    constexpr int KS = kv_rank / 64;  // k8 steps of a warp's K slice (kv_rank / 8 wide)
+    constexpr int MT = KV;            // 16-dim tiles of a warp's output dims (kv_rank / 8)
+    constexpr int row_pad = kv_rank + 8;
+    constexpr int stage_f = kRowsC * row_pad;
+    extern __shared__ __align__(16) float sm[];
+    griddep_launch_dependents();
+    const int n_slots = a.n_slots, S = a.stages, nh = a.nh;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm);       // [kMaxStages] rows landed
+    float *ring = sm + 2 * kMaxStages;                        // [S][kRowsC][row_pad]
+    float *red = ring + S * stage_f;                          // [kMlaWarps][kRowsC][8] partials
+    float *pw = red + kMlaWarps * kRowsC * kTcHeads;          // [kRowsC][8] softmax weights
+    float *smm = pw + kRowsC * kTcHeads;                      // [8] running max
+    float *sal = smm + kTcHeads;                              // [8] rescale factor
+    float *sl = sal + kTcHeads;                               // [8] running sum
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int part = static_cast<int>(cluster_ctarank());
+    const int ngrp = (nh + H - 1) / H;
+    const int grp = blockIdx.x / kParts;
+    const int tt = grp / ngrp, h0 = (grp - tt * ngrp) * H;
+
+    const int per = ((n_slots + kParts - 1) / kParts + kRowsC - 1) / kRowsC * kRowsC;
+    const int j_begin = min(part * per, n_slots), j_end = min(j_begin + per, n_slots);
+    const int nchunks = (j_end - j_begin + kRowsC - 1) / kRowsC;
+    const int32_t *ix = a.idx + static_cast<int64_t>(tt) * n_slots;
+    constexpr uint32_t row_bytes = static_cast<uint32_t>(kv_rank) * 4u;
+
+    if (tid == 0) {
+        for (int s = 0; s < kMaxStages; ++s) mbar_init(&bars[s], 1);
+        mbar_init_fence();
+    }
+    if (tid < kRowsC * kTcHeads) pw[tid] = 0.f;  // columns >= H stay zero
+    if (tid < kTcHeads) {
+        smm[tid] = -INFINITY;
+        sal[tid] = 0.f;
+        sl[tid] = 0.f;
+    }
+    // Every input may be the preceding grid's output: wait for it, then read through L2 (or the
+    // async proxy) only.
+    griddep_wait();
+    // Bulk copies of the chunks' rows as in attn_gathered_kernel: every warp issues 2 rows of a
+    // chunk, S - 1 chunks ahead; warp 0 lane 0 announces the chunk's bytes.
+    constexpr int kRowsPerWarp = kRowsC / kMlaWarps;
+    const int my_row = warp * kRowsPerWarp + lane;  // meaningful for lane < kRowsPerWarp
+    int issued = 0;
+    int nidx = 0;
+    if (lane < kRowsPerWarp && j_begin + my_row < j_end) nidx = __ldcg(ix + j_begin + my_row);
+    auto issue_next = [&]() {
+        if (issued >= nchunks) return;
+        const int j0 = j_begin + issued * kRowsC;
+        const int nj = min(kRowsC, j_end - j0);
+        uint64_t *bar = &bars[issued % S];
+        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nj) * row_bytes);
+        if (lane < kRowsPerWarp && my_row < nj)
+            bulk_g2s_plain(ring + (issued % S) * stage_f + my_row * row_pad,
+                           a.cache + static_cast<int64_t>(nidx) * kv_rank, row_bytes, bar);
+        ++issued;
+        const int jn = j0 + kRowsC + my_row;
+        if (lane < kRowsPerWarp && issued < nchunks && jn < j_end) nidx = __ldcg(ix + jn);
+    };
+    for (int c = 0; c < S - 1; ++c) issue_next();
+    // The group's queries, staged in the ring's last stage (no copy writes it before the first
+    // chunk's score barrier), zero for the columns >= H.
+    float *sq = ring + (S - 1) * stage_f;  // [8][row_pad]
+    for (int i = tid; i < kTcHeads * kv_rank; i += kMlaThreads) {
+        const int hh = i / kv_rank, k = i - hh * kv_rank;
+        const int64_t th = static_cast<int64_t>(tt) * nh + min(h0 + hh, nh - 1);
+        sq[hh * row_pad + k] = hh < H ? __ldcg(a.q_lat + th * kv_rank + k) : 0.f;
+    }
+    __syncthreads();
+    // The warp's B fragments of q: lane (g, t) holds q_g[kb + 8s + 2t] and q_g[kb + 8s + 2t + 1]
+    // (MMA k slots t and t + 4; the rows' A fragments use the same pairing).
+    const int kb = warp * (kv_rank / kMlaWarps);
+    uint32_t qh[KS][2], ql[KS][2];
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+        const float2 qv = *reinterpret_cast<const float2 *>(sq + g * row_pad + kb + 8 * s + 2 * t);
+        tf32_split(qv.x, qh[s][0], ql[s][0]);
+        tf32_split(qv.y, qh[s][1], ql[s][1]);
+    }
+    // (the score barrier of chunk 0 orders these reads before chunk S - 1's copy into the stage)
+
+    float acc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    const int d_base = warp * (kv_rank / kMlaWarps);
+    bool failed = false;
+    for (int c = 0; c < nchunks; ++c) {
+        const int j0 = j_begin + c * kRowsC;
+        const int nj = min(kRowsC, j_end - j0);
+        const float *rows = ring + (c % S) * stage_f;
+        if (!warp_wait_bounded(&bars[c % S], static_cast<uint32_t>((c / S) & 1))) {
+            failed = true;
+            if (lane == 0) atomicOr(&g_mla_fault, kFaultAttnWait);
+        }
+        // Scores of the warp's K slice (rows >= nj hold stale data: computed, never used), in
+        // kChains independent MMA chains over the k8 steps s = kChains i + r, added in a fixed
+        // tree at the end (short dependency chains; the same order for every H).
+        {
+            constexpr int kChains = KS >= 4 ? 4 : KS;
+            float sp[kChains][4];
+#pragma unroll
+            for (int r = 0; r < kChains; ++r) sp[r][0] = sp[r][1] = sp[r][2] = sp[r][3] = 0.f;
+            const float *ra = rows + g * row_pad + kb + 2 * t;
+            const float *rb = ra + 8 * row_pad;
+#pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                const float2 va = *reinterpret_cast<const float2 *>(ra + 8 * s);
+                const float2 vb = *reinterpret_cast<const float2 *>(rb + 8 * s);
+                uint32_t ah[4], al[4];
+                tf32_split(va.x, ah[0], al[0]);
+                tf32_split(vb.x, ah[1], al[1]);
+                tf32_split(va.y, ah[2], al[2]);
+                tf32_split(vb.y, ah[3], al[3]);
+                mma_3xtf32(sp[s % kChains], ah, al, qh[s][0], qh[s][1], ql[s][0], ql[s][1]);
+            }
+            float sc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if constexpr (kChains == 4) sc[e] = (sp[0][e] + sp[1][e]) + (sp[2][e] + sp[3][e]);
+                else if constexpr (kChains == 2) sc[e] = sp[0][e] + sp[1][e];
+                else sc[e] = sp[0][e];
+            }
+            float *rw = red + warp * (kRowsC * kTcHeads);
+            *reinterpret_cast<float2 *>(rw + g * kTcHeads + 2 * t) = make_float2(sc[0], sc[1]);
+            *reinterpret_cast<float2 *>(rw + (g + 8) * kTcHeads + 2 * t) = make_float2(sc[2], sc[3]);
+        }
+        // The partials are complete, and every thread is done with chunk c - 1, whose stage
+        // takes chunk c + S - 1.  A wait that gave up anywhere stops every warp here, together.
+        if (__syncthreads_or(failed)) break;
+        issue_next();
+        // Online softmax step: warp hh < H updates head hh, lane j < 16 holding row j's score
+        // (the 8 warp partials added in warp order, then scaled).
+        if (warp < H) {
+            const int hh = warp;
+            const float mo = smm[hh];
+            float s = -INFINITY;
+            if (lane < nj) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kMlaWarps; ++w) v += red[(w * kRowsC + lane) * kTcHeads + hh];
+                s = __fmul_rn(a.scale, v);
+            }
+            float mc = fmaxf(mo, s);
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFullMask, mc, off));
+            const float pj = lane < nj ? expf(s - mc) : 0.f;
+            if (lane < kRowsC) pw[lane * kTcHeads + hh] = pj;
+            float lc = pj;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) lc += __shfl_xor_sync(kFullMask, lc, off);
+            if (lane == 0) {
+                const float alv = mo == -INFINITY ? 0.f : expf(mo - mc);
+                sal[hh] = alv;
+                sl[hh] = fmaf(sl[hh], alv, lc);
+                smm[hh] = mc;
+            }
+        }
+        __syncthreads();
+        // Outputs: rescale, then the chunk's rows in two k8 steps (rows >= nj read as zero).
+        {
+            const float al0 = sal[2 * t], al1 = sal[2 * t + 1];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[mt][0] *= al0;
+                acc[mt][1] *= al1;
+                acc[mt][2] *= al0;
+                acc[mt][3] *= al1;
+            }
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int r0 = 8 * ks + t, r1 = r0 + 4;
+                uint32_t bh0, bl0, bh1, bl1;
+                tf32_split(pw[r0 * kTcHeads + g], bh0, bl0);
+                tf32_split(pw[r1 * kTcHeads + g], bh1, bl1);
+                // rows past the chunk's end read as zero (their weights are zero, their stage
+                // rows stale); a full chunk needs no test
+                const bool ok0 = nj == kRowsC || r0 < nj, ok1 = nj == kRowsC || r1 < nj;
+                // MMA rows g and g + 8 of a 16-dim tile are the adjacent dims 2g and 2g + 1: one
+                // 8-byte load per row
+                const float *p0 = rows + r0 * row_pad + d_base + 2 * g;
+                const float *p1 = rows + r1 * row_pad + d_base + 2 * g;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const float2 v0 = ok0 ? *reinterpret_cast<const float2 *>(p0 + 16 * mt) : make_float2(0.f, 0.f);
+                    const float2 v1 = ok1 ? *reinterpret_cast<const float2 *>(p1 + 16 * mt) : make_float2(0.f, 0.f);
+                    uint32_t ah[4], al[4];
+                    tf32_split(v0.x, ah[0], al[0]);
+                    tf32_split(v0.y, ah[1], al[1]);
+                    tf32_split(v1.x, ah[2], al[2]);
+                    tf32_split(v1.y, ah[3], al[3]);
+                    mma_3xtf32(acc[mt], ah, al, bh0, bh1, bl0, bl1);
+                }
+            }
+        }
+        // No barrier here: the next chunk's score barrier orders this chunk's reads before the
+        // stage's reuse and before the next softmax step rewrites the weights.
+    }
+    if (warp == 0) {
+        // Every copy issued must land before the stages take the partials or the CTA exits.
+        for (int c = max(0, issued - S); c < issued; ++c)
+            (void)warp_wait_bounded(&bars[c % S], static_cast<uint32_t>((c / S) & 1));
+    }
+    __syncthreads();
+    float *sacc = ring;  // this part's partial outputs [H][kv_rank] (fits one stage)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int d = d_base + 16 * mt + 2 * g;  // acc[mt]: dims d, d + 1 x heads 2t, 2t + 1
+        if (2 * t < H)
+            *reinterpret_cast<float2 *>(sacc + (2 * t) * kv_rank + d) = make_float2(acc[mt][0], acc[mt][2]);
+        if (2 * t + 1 < H)
+            *reinterpret_cast<float2 *>(sacc + (2 * t + 1) * kv_rank + d) = make_float2(acc[mt][1], acc[mt][3]);
+    }
+    cluster_sync_all();
+    // Merge: this CTA finalises outputs [c0, c1) of the group's H x kv_rank, parts in order.
+    const int c0 = part * (H * kv_rank) / kParts, c1 = (part + 1) * (H * kv_rank) / kParts;
+    for (int i = c0 + tid; i < c1; i += kMlaThreads) {
+        const int hh = i / kv_rank, d = i - hh * kv_rank;
+        float mq[kParts];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) {
+            mq[q] = ld_dsmem(smm + hh, q);
+            mx = fmaxf(mx, mq[q]);
+        }
+        float lsum = 0.f, o = 0.f;
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) {
+            const float wq = mq[q] == -INFINITY ? 0.f : expf(mq[q] - mx);
+            lsum = fmaf(ld_dsmem(sl + hh, q), wq, lsum);
+            o = fmaf(ld_dsmem(sacc + i, q), wq, o);
+        }
+        if (h0 + hh < nh)
+            a.out[(static_cast<int64_t>(tt) * nh + h0 + hh) * kv_rank + d] = __fdiv_rn(o, lsum);
+    }
+    cluster_sync_all();  // no CTA leaves while another still reads its shared memory
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr int kMaxDevices = 64;
@@ -741,8 +1027,52 @@ int launch_attn(const AttnArgs &args0, int t, cudaStream_t st) {
                                                                                       : MEMQ_ERR_LAUNCH;
 }
 
+// The tensor-core kernel (d_rope == 0): as many 16-row stages as fit beside the fixed part in
+// the share of one of two CTAs per SM, 2 to kMaxStages.
+template <int KV, int H>
+int launch_attn_tc(const AttnArgs &args0, int t, cudaStream_t st) {
+    AttnArgs args = args0;
+    constexpr int row_pad = KV * 128 + 8;
+    const size_t fixed = sizeof(float) * (2 * kMaxStages + (kMlaWarps + 1) * kRowsC * kTcHeads + 3 * kTcHeads);
+    const size_t stage = sizeof(float) * static_cast<size_t>(kRowsC) * row_pad;
+    const int64_t budget = 112 * 1024;
+    int stages = static_cast<int>((budget - static_cast<int64_t>(fixed)) / static_cast<int64_t>(stage));
+    stages = std::max(2, std::min(kMaxStages, stages));
+    args.stages = stages;
+    const size_t smem = fixed + stages * stage;
+    static std::atomic<uint64_t> attr_done{0};
+    if (!allow_max_smem(reinterpret_cast<const void *>(attn_gathered_tc_kernel<KV, H>), attr_done))
+        return MEMQ_ERR_LAUNCH;
+    const unsigned groups = static_cast<unsigned>(t) * static_cast<unsigned>((args.nh + H - 1) / H);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(groups * kParts);
+    cfg.blockDim = dim3(kMlaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_gathered_tc_kernel<KV, H>, args) == cudaSuccess ? MEMQ_OK
+                                                                                         : MEMQ_ERR_LAUNCH;
+}
+
+// Which attention kernel serves a call is fixed by (kv_rank, d_rope), never by the split, so the
+// split twins run the same arithmetic: the tensor-core kernel for d_rope == 0 and kv_rank <= 512,
+// the f32 kernel otherwise.
 template <int KV>
 int launch_attn_h(int H, const AttnArgs &args, int t, cudaStream_t st) {
+    if constexpr (KV <= 4) {
+        if (args.d_rope == 0) {
+            switch (H) {
+                case 8: return launch_attn_tc<KV, 8>(args, t, st);
+                case 4: return launch_attn_tc<KV, 4>(args, t, st);
+                case 2: return launch_attn_tc<KV, 2>(args, t, st);
+                default: return launch_attn_tc<KV, 1>(args, t, st);
+            }
+        }
+    }
     switch (H) {
         case 8: return launch_attn<KV, 8>(args, t, st);
         case 4: return launch_attn<KV, 4>(args, t, st);

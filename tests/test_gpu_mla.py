@@ -88,6 +88,11 @@ def test_head_gemv_ragged(memq, oracle, t, nh, rows, cols):
 
 
 # --------------------------------------------------------------------------- attn_gathered
+def tensor_core_attn(kv_rank, d_rope):
+    """attn_gathered takes its tensor-core kernel (3xTF32) for d_rope == 0 and kv_rank <= 512."""
+    return d_rope == 0 and kv_rank <= 512
+
+
 def attn_bound(q_lat, q_pe, cache, idx, scale, cabs):
     """Per-output bound on |out_gpu - out_oracle| for attn_gathered's f32 arithmetic.
 
@@ -99,13 +104,23 @@ def attn_bound(q_lat, q_pe, cache, idx, scale, cabs):
     per staged chunk).  A relative weight error delta moves the normalised output by at most
     2 delta max_j |c_j[r]|; the numerator and denominator sums (at most per + chunks + 8 roundings
     each, in a part and the 8-way merge) add 2 gamma max_j |c_j[r]|, gamma = (per + chunks + 10) u.
+
+    Tensor-core kernel (3xTF32): a product x y is hi_x hi_y + hi_x lo_y + lo_x hi_y with hi the
+    TF32 truncation (exact) and lo = x - hi taken by the MMA at TF32 precision, so it carries
+    |lo_x lo_y| + the truncation of both lo parts <= 3 2^-20 |x y| = 48 u |x y|.  Every MMA is
+    counted as adding its 8 products to the running sum one rounding at a time (the hardware
+    order is not specified), so a score is a chain of at most 3 kv_rank / 8 additions (one warp's
+    K slice in three terms), 2 for the chain combine, 8 for the warp partials and the scale:
+    k_ops = 48 + 3 kv_rank / 8 + 11.  The output sums likewise: 48 u per product and three terms
+    per row, gamma = (48 + 3 per + chunks + 10) u.
     """
     t, nh, kv_rank = q_lat.shape
     n_slots = idx.shape[1]
     d_rope = cache.shape[1] - kv_rank
     per = -(-(-(-n_slots // 8)) // 16) * 16
     chunks = -(-per // 16)
-    k_ops = kv_rank / 32 + -(-d_rope // 32) + 6
+    tc = tensor_core_attn(kv_rank, d_rope)
+    k_ops = 48 + 3 * kv_rank / 8 + 11 if tc else kv_rank / 32 + -(-d_rope // 32) + 6
     bound = np.empty((t, nh), np.float64)
     for tt in range(t):
         c = np.abs(cache[idx[tt]].astype(np.float64))               # [n_slots, row]
@@ -117,7 +132,7 @@ def attn_bound(q_lat, q_pe, cache, idx, scale, cabs):
         e = k_ops * U * s_abs.max(axis=1)
         r = 2.0 * s_abs.max(axis=1)
         delta = 3.0 * e + (chunks + 2) * (3.0 * U + U * r)
-        gamma = (per + chunks + 10) * U
+        gamma = ((48 + 3 * per) if tc else per) * U + (chunks + 10) * U
         bound[tt] = 2.0 * delta + 2.0 * gamma
     return bound[:, :, None] * cabs
 
@@ -162,14 +177,23 @@ def test_attn_gathered_ragged(memq, oracle, t, nh, kv_rank, d_rope, kv, n_slots)
     run_attn(memq, oracle, q_lat, q_pe, cache, idx, 1.0 / np.sqrt(kv_rank + d_rope))
 
 
-def test_attn_gathered_one_slot_is_the_row(memq):
-    """A single gathered slot has softmax weight 1: the output is the gathered row, exactly."""
-    q_lat, _, cache, idx = synth.mla_attn_inputs(2, 50, nh=3, kv_rank=256, n_slots=1)
-    out = memq.memq_mla_attn_gathered(to_dev(q_lat), None, to_dev(cache), to_dev(idx), 0.1)
+@pytest.mark.parametrize("d_rope", [0, 32])
+def test_attn_gathered_one_slot_is_the_row(memq, d_rope):
+    """A single gathered slot has softmax weight 1: the output is the gathered row.  Exactly with
+    the f32 kernel (d_rope = 32); with the tensor-core kernel (d_rope = 0) the weight-1 product is
+    hi + (x - hi) at TF32 precision, so each element is the row's within 2^-20 relative."""
+    q_lat, q_pe, cache, idx = synth.mla_attn_inputs(2, 50, nh=3, kv_rank=256, d_rope=d_rope,
+                                                     n_slots=1)
+    dpe = None if q_pe is None else to_dev(q_pe)
+    out = memq.memq_mla_attn_gathered(to_dev(q_lat), dpe, to_dev(cache), to_dev(idx), 0.1)
     got = out.cpu().numpy()
     for tt in range(2):
         for h in range(3):
-            assert np.array_equal(got[tt, h], cache[idx[tt, 0]])
+            row = cache[idx[tt, 0], :256]
+            if tensor_core_attn(256, d_rope):
+                assert np.all(np.abs(got[tt, h].astype(np.float64) - row) <= 2.0 ** -20 * np.abs(row))
+            else:
+                assert np.array_equal(got[tt, h], row)
 
 
 def test_attn_gathered_sharp_softmax(memq, oracle):
