@@ -249,6 +249,12 @@ int memq_repack_e4m3_blk128_q8_0(const uint8_t *w, const float *grid, void *out,
  *   each in [0, pool) (not checked: an index outside the pool is outside the contract)
  *   out device [t][nh][kv_rank];  q_lat, q_pe, idx, out 4-byte aligned
  *   kv_rank in {128, 256, 512, 1024};  0 <= d_rope <= 128;  n_slots >= 1;  scale finite.
+ * Numerics of attn_gathered: an online softmax over 8 fixed slot ranges of 16-slot chunks,
+ * merged in range order.  With t >= 2, d_rope == 0 and kv_rank <= 512 (the page geometry) the
+ * scores and outputs are tensor-core products in three TF32 terms (hi = the value truncated to
+ * TF32, lo = the exact remainder at TF32 precision; per-product error below 3 * 2^-20 of
+ * |x y|), otherwise f32 FMAs.  The choice depends on (t, kv_rank, d_rope) only, so the split
+ * twins run the same arithmetic.
  * Errors: MEMQ_ERR_SHAPE, MEMQ_ERR_NULL, MEMQ_ERR_ALIGN, MEMQ_ERR_M_RANGE, MEMQ_ERR_LAUNCH.
  */
 int memq_mla_absorb_q(const float *q_nope, const float *wk_b, float *out, int t, int nh,

@@ -1058,13 +1058,15 @@ int launch_attn_tc(const AttnArgs &args0, int t, cudaStream_t st) {
                                                                                          : MEMQ_ERR_LAUNCH;
 }
 
-// Which attention kernel serves a call is fixed by (kv_rank, d_rope), never by the split, so the
-// split twins run the same arithmetic: the tensor-core kernel for d_rope == 0 and kv_rank <= 512,
-// the f32 kernel otherwise.
+// Which attention kernel serves a call is fixed by (t, kv_rank, d_rope), never by the split, so
+// the split twins run the same arithmetic: the tensor-core kernel for t >= 2, d_rope == 0 and
+// kv_rank <= 512, the f32 kernel otherwise (measured on GB300 at the page geometry, us, tensor
+// cores against f32: t = 1 44.6 / 39.6, t = 2 45.7 / 47.3, t = 4 51.9 / 64.5, t = 8 97 / 121;
+// at t = 1 the 8-head MMA tiles are mostly idle for lack of query rows per SM).
 template <int KV>
 int launch_attn_h(int H, const AttnArgs &args, int t, cudaStream_t st) {
     if constexpr (KV <= 4) {
-        if (args.d_rope == 0) {
+        if (args.d_rope == 0 && t >= 2) {
             switch (H) {
                 case 8: return launch_attn_tc<KV, 8>(args, t, st);
                 case 4: return launch_attn_tc<KV, 4>(args, t, st);

@@ -88,9 +88,10 @@ def test_head_gemv_ragged(memq, oracle, t, nh, rows, cols):
 
 
 # --------------------------------------------------------------------------- attn_gathered
-def tensor_core_attn(kv_rank, d_rope):
-    """attn_gathered takes its tensor-core kernel (3xTF32) for d_rope == 0 and kv_rank <= 512."""
-    return d_rope == 0 and kv_rank <= 512
+def tensor_core_attn(t, kv_rank, d_rope):
+    """attn_gathered takes its tensor-core kernel (3xTF32) for t >= 2, d_rope == 0 and
+    kv_rank <= 512."""
+    return t >= 2 and d_rope == 0 and kv_rank <= 512
 
 
 def attn_bound(q_lat, q_pe, cache, idx, scale, cabs):
@@ -119,7 +120,7 @@ def attn_bound(q_lat, q_pe, cache, idx, scale, cabs):
     d_rope = cache.shape[1] - kv_rank
     per = -(-(-(-n_slots // 8)) // 16) * 16
     chunks = -(-per // 16)
-    tc = tensor_core_attn(kv_rank, d_rope)
+    tc = tensor_core_attn(t, kv_rank, d_rope)
     k_ops = 48 + 3 * kv_rank / 8 + 11 if tc else kv_rank / 32 + -(-d_rope // 32) + 6
     bound = np.empty((t, nh), np.float64)
     for tt in range(t):
@@ -170,6 +171,9 @@ def test_attn_gathered_page_geometry(memq, oracle, t, kv):
     (1, 64, 512, 0, 4096, 2048),    # pool larger than the gather
     (2, 6, 1024, 128, 500, 333),    # the largest row the kernel takes
     (8, 2, 256, 32, 64, 2048),      # indices repeat (gather wider than the pool)
+    (2, 5, 128, 0, 300, 37),        # tensor cores: partial head group, partial chunks, empty parts
+    (4, 9, 256, 0, 100, 130),       # tensor cores: 9 heads (groups of 8 + 1), ragged slots
+    (3, 64, 512, 0, 64, 2048),      # tensor cores: indices repeat
 ])
 def test_attn_gathered_ragged(memq, oracle, t, nh, kv_rank, d_rope, kv, n_slots):
     q_lat, q_pe, cache, idx = synth.mla_attn_inputs(t, kv, nh=nh, kv_rank=kv_rank, d_rope=d_rope,
@@ -190,16 +194,17 @@ def test_attn_gathered_one_slot_is_the_row(memq, d_rope):
     for tt in range(2):
         for h in range(3):
             row = cache[idx[tt, 0], :256]
-            if tensor_core_attn(256, d_rope):
+            if tensor_core_attn(2, 256, d_rope):
                 assert np.all(np.abs(got[tt, h].astype(np.float64) - row) <= 2.0 ** -20 * np.abs(row))
             else:
                 assert np.array_equal(got[tt, h], row)
 
 
-def test_attn_gathered_sharp_softmax(memq, oracle):
+@pytest.mark.parametrize("t", [1, 2])
+def test_attn_gathered_sharp_softmax(memq, oracle, t):
     """Scale 4: scores near 512 spread over tens of units, so the softmax concentrates on a few
-    slots and the running max changes between chunks."""
-    q_lat, _, cache, idx = synth.mla_attn_inputs(1, 2048, nh=8)
+    slots and the running max changes between chunks (t = 1 f32 kernel, t = 2 tensor cores)."""
+    q_lat, _, cache, idx = synth.mla_attn_inputs(t, 2048, nh=8)
     run_attn(memq, oracle, q_lat, None, cache, idx, 4.0)
 
 

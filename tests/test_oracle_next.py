@@ -101,8 +101,10 @@ def test_repack_codes_are_the_nearest(oracle, grid):
     # codes are decided on the f32 quotient, which may land on the tie and round away from zero
     k = np.arange(-127, 128, dtype=np.float64)
     d64 = dd.astype(np.float64)[..., None]
-    err = np.abs(W[..., None] - k * d64[..., None])
-    best = err.min(axis=3)
+    best = np.empty_like(W)
+    for r0 in range(0, out_f, 8):  # in row chunks: the full [rows, blocks, 32, 255] is 1.1 GB
+        err = np.abs(W[r0:r0 + 8, ..., None] - k * d64[r0:r0 + 8, ..., None])
+        best[r0:r0 + 8] = err.min(axis=3)
     mine = np.abs(W - qs.astype(np.float64) * d64)
     t = np.divide(W, d64, out=np.zeros_like(W), where=d64 != 0)
     near_tie = np.abs(np.abs(t - np.trunc(t)) - 0.5) <= 2.0 ** -23 * np.abs(t)
