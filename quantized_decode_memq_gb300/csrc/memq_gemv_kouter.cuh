@@ -42,6 +42,14 @@ constexpr int kKoKw = 32;                // 32-blocks per stage: the tile kernel
 // (the chunk plus padding that keeps the consumers' fragment loads bank-conflict free: E4M3 /
 // block-128 rows 32 bytes apart modulo the 128-byte bank period, Q8_0 rows 80, as in the tile
 // kernel).
+// The stage's activation chunk: token rows of kw 32-blocks of qs padded to 1056 bytes and of kw
+// scales padded to 36 floats (the tensor copies' boxes are that wide and read the next chunk's
+// first bytes, or zeros past the end), so the B-fragment loads of 8 tokens (rows 32 bytes apart
+// modulo the 128-byte bank period) and the scale loads of tokens 2t (rows 8 banks apart) are
+// bank-conflict free.
+constexpr int kKoActRow = kKoKw * 32 + 32;  // bytes per token row of qs in a stage
+constexpr int kKoDRow = kKoKw + 4;          // floats per token row of d in a stage
+
 template <int KIND>
 struct KoGeo {
     static constexpr int kBlockBytes = KIND == kQ80T ? 34 : 32;
@@ -63,8 +71,8 @@ struct KoArgs {
     int box_rows[kMaxGroup];  // per matrix: rows of the weight tensor box (the fewest a pass
                               // holds); a pass with more rows copies the rest row by row
     int stage;      // bytes per stage (weights of the largest pass + activation)
-    int act_qs;     // offset of the stage's qs chunk [m][kw * 32]
-    int act_d;      // offset of the stage's d chunk [m][kw] (f32)
+    int act_qs;     // offset of the stage's qs chunk [m][kKoActRow]
+    int act_d;      // offset of the stage's d chunk [m][kKoDRow] (f32)
     int act_bytes;  // bytes the two activation copies complete per stage
     int stages;
     uint32_t off_part, off_grid, off_ring;
@@ -72,7 +80,8 @@ struct KoArgs {
 
 // Tensor maps: per matrix the weight plane as [out_f][row_bytes / 8] 64-bit elements with boxes
 // of slot bytes x box_rows rows (one copy per stage brings a pass's rows); the activation qs as
-// [m][in_f / 8] 64-bit elements, box kw * 32 bytes x m rows; d as [m][in_f / 32] f32, box kw x m.
+// [m][in_f / 8] 64-bit elements, box kKoActRow bytes x m rows; d as [m][in_f / 32] f32, box
+// kKoDRow x m.
 struct KoMaps {
     CUtensorMap w8[kMaxGroup];
     CUtensorMap qs;
@@ -117,8 +126,8 @@ __device__ __forceinline__ void ko_stage_q80(const KoArgs &a, const uint8_t *sta
     const int j0 = 4 * warp;
     const int nblk = FULL ? 4 : min(4, a.nb - kbc - j0);
     if (!FULL && nblk <= 0) return;
-    const uint8_t *aq = stage + a.act_qs + g * (kKoKw * 32) + 32 * j0 + 8 * t;
-    const float *ad = reinterpret_cast<const float *>(stage + a.act_d) + 2 * t * kKoKw + j0;
+    const uint8_t *aq = stage + a.act_qs + g * kKoActRow + 32 * j0 + 8 * t;
+    const float *ad = reinterpret_cast<const float *>(stage + a.act_d) + 2 * t * kKoDRow + j0;
     const uint8_t *pa = stage + 34 * j0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -130,7 +139,7 @@ __device__ __forceinline__ void ko_stage_q80(const KoArgs &a, const uint8_t *sta
                 s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
             }
             const float k0 = 2 * t < M ? ad[b] : 0.f;
-            const float k1 = 2 * t + 1 < M ? ad[kKoKw + b] : 0.f;
+            const float k1 = 2 * t + 1 < M ? ad[kKoDRow + b] : 0.f;
 #pragma unroll
             for (int rt = 0; rt < TILES; ++rt) {
                 if (TILES == 1 || rt < T) {
@@ -172,8 +181,8 @@ __device__ __forceinline__ void ko_stage(const KoArgs &a, const uint8_t *stage, 
     const int nblk = FULL ? 4 : min(4, a.nb - kbc - j0);
     if (!FULL && nblk <= 0) return;
     // this thread's activation bytes (token g) and scales (tokens 2t, 2t+1) of block j0
-    const uint8_t *aq = stage + a.act_qs + g * (kKoKw * 32) + 32 * j0 + 8 * t;
-    const float *ad = reinterpret_cast<const float *>(stage + a.act_d) + 2 * t * kKoKw + j0;
+    const uint8_t *aq = stage + a.act_qs + g * kKoActRow + 32 * j0 + 8 * t;
+    const float *ad = reinterpret_cast<const float *>(stage + a.act_d) + 2 * t * kKoDRow + j0;
     const uint8_t *pa = stage + 32 * j0 + 8 * t;
     float grp[TILES][4];
 #pragma unroll
@@ -188,7 +197,7 @@ __device__ __forceinline__ void ko_stage(const KoArgs &a, const uint8_t *stage, 
                 s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
             }
             const float k0 = 2 * t < M ? ad[b] : 0.f;
-            const float k1 = 2 * t + 1 < M ? ad[kKoKw + b] : 0.f;
+            const float k1 = 2 * t + 1 < M ? ad[kKoDRow + b] : 0.f;
 #pragma unroll
             for (int rt = 0; rt < TILES; ++rt) {
                 if (TILES == 1 || rt < T) {
@@ -581,9 +590,9 @@ cudaError_t launch_kouter(int nmat, const uint8_t *const *w, const float *const 
     // (1024 x 5120, m = 4: 8.2 us against 4.4 us on the tile kernel, which uses fewer CTAs there)
     if (rmax > kPassRows || rmax < 8) return cudaErrorNotSupported;
     a.act_qs = static_cast<int>(align_up(static_cast<uint32_t>(pass_rows * KG::kSlot), 128));
-    a.act_d = a.act_qs + static_cast<int>(align_up(static_cast<uint32_t>(M * kKoKw * 32), 128));
-    a.stage = a.act_d + static_cast<int>(align_up(static_cast<uint32_t>(M * kKoKw * 4), 128));
-    a.act_bytes = M * kKoKw * 32 + M * kKoKw * 4;
+    a.act_d = a.act_qs + static_cast<int>(align_up(static_cast<uint32_t>(M * kKoActRow), 128));
+    a.stage = a.act_d + static_cast<int>(align_up(static_cast<uint32_t>(M * kKoDRow * 4), 128));
+    a.act_bytes = M * kKoActRow + M * kKoDRow * 4;
     // Shared memory: barriers, the pass partials, the block-128 grid rows, the ring.
     const uint32_t part = align_up(static_cast<uint32_t>(kWarps * kPassRows * M * 4), 128);
     const int grid_rows = static_cast<int>(rmax / 128 + 2);
@@ -604,8 +613,8 @@ cudaError_t launch_kouter(int nmat, const uint8_t *const *w, const float *const 
         if (!ko_map(maps.w8[i], 1, w[i], out_f[i], a.row_bytes / 8, a.row_bytes, 8, KG::kSlot / 8,
                     a.box_rows[i], dev))
             return cudaErrorNotSupported;
-    if (!ko_map(maps.qs, 2, qs, M, in_f / 8, in_f, 8, kKoKw * 4, M, dev) ||
-        !ko_map(maps.d, 3, d, M, in_f / 32, in_f / 8, 4, kKoKw, M, dev))
+    if (!ko_map(maps.qs, 2, qs, M, in_f / 8, in_f, 8, kKoActRow / 8, M, dev) ||
+        !ko_map(maps.d, 3, d, M, in_f / 32, in_f / 8, 4, kKoDRow, M, dev))
         return cudaErrorNotSupported;
 
     auto kern = gemv_kouter_kernel<KIND, M, TILES>;
