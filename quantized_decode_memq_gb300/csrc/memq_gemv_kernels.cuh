@@ -133,6 +133,11 @@ struct StreamArgs {
     float *z_out;
     // Shared-memory layout (bytes); barriers at 0.
     uint32_t off_part, off_bfrag, off_qs, off_d, off_grid, off_red, off_ring;
+    // Row strides of the staged activation: qstr bytes per token row of qs (in_f, or padded to
+    // 32 mod 128 where the tensor-core consumers convert B fragments from it), dstr floats per
+    // token row of d (padded to 4 mod 16, so the scales of tokens 0, 2, 4, 6 one warp loads fall
+    // on different banks).
+    int qstr, dstr;
     int use_tma;  // 1: full tiles (and 8-row halves) come as one tensor copy each
     int ctas_per_sm;  // host: CTAs per SM the plan sized shared memory for
     // The launch's matrices: matrix i owns CTAs [mat_cta[i], mat_cta[i+1]); each CTA takes w,
@@ -220,18 +225,21 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
         if (FULL || b < nblk) {
             const int kb = kb0 + b;
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
-            if (g < M) {
+            {
+                // B column g is token g; columns g >= M load token M - 1 (no divergent branch):
+                // an MMA column depends only on its own B column, and those are never stored
+                const int gq = g < M ? g : M - 1;
                 if (MODE == kActFrag) {
-                    const uint4 v = bfrag[(g * (a.nb | 1) + kb) * 4 + t];
+                    const uint4 v = bfrag[(gq * (a.nb | 1) + kb) * 4 + t];
                     bq[0] = v.x;
                     bq[1] = v.y;
                     bq[2] = v.z;
                     bq[3] = v.w;
                 } else {
                     const uint2 qv = MODE == kActSmem
-                                         ? lds64(s_qs + g * a.in_f + 32 * kb + 8 * t)
+                                         ? lds64(s_qs + gq * a.qstr + 32 * kb + 8 * t)
                                          : __ldcg(reinterpret_cast<const uint2 *>(
-                                               a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+                                               a.qs + static_cast<int64_t>(gq) * a.in_f + 32 * kb + 8 * t));
                     s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
                     s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
                 }
@@ -241,8 +249,8 @@ __device__ __forceinline__ void mma_stage(const StreamArgs &a, const uint8_t *st
                 if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
                 if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
             } else {
-                if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
-                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
+                if (2 * t < M) k0 = s_d[(2 * t) * a.dstr + kb];
+                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.dstr + kb];
             }
             const uint8_t *pa = stage + g * G::kSlot + 32 * b + 8 * t;
             const uint2 wa = lds64(pa);
@@ -316,18 +324,21 @@ __device__ __forceinline__ void mma_stage_q80(const StreamArgs &a, const uint8_t
         if (FULL || b < nblk) {
             const int kb = kb0 + b;
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
-            if (g < M) {
+            {
+                // B column g is token g; columns g >= M load token M - 1 (no divergent branch):
+                // an MMA column depends only on its own B column, and those are never stored
+                const int gq = g < M ? g : M - 1;
                 if (MODE == kActFrag) {
-                    const uint4 v = bfrag[(g * (a.nb | 1) + kb) * 4 + t];
+                    const uint4 v = bfrag[(gq * (a.nb | 1) + kb) * 4 + t];
                     bq[0] = v.x;
                     bq[1] = v.y;
                     bq[2] = v.z;
                     bq[3] = v.w;
                 } else {
                     const uint2 qv = MODE == kActSmem
-                                         ? lds64(s_qs + g * a.in_f + 32 * kb + 8 * t)
+                                         ? lds64(s_qs + gq * a.qstr + 32 * kb + 8 * t)
                                          : __ldcg(reinterpret_cast<const uint2 *>(
-                                               a.qs + static_cast<int64_t>(g) * a.in_f + 32 * kb + 8 * t));
+                                               a.qs + static_cast<int64_t>(gq) * a.in_f + 32 * kb + 8 * t));
                     s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
                     s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
                 }
@@ -337,8 +348,8 @@ __device__ __forceinline__ void mma_stage_q80(const StreamArgs &a, const uint8_t
                 if (2 * t < M) k0 = __ldcg(a.d + (2 * t) * a.nb + kb);
                 if (2 * t + 1 < M) k1 = __ldcg(a.d + (2 * t + 1) * a.nb + kb);
             } else {
-                if (2 * t < M) k0 = s_d[(2 * t) * a.nb + kb];
-                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.nb + kb];
+                if (2 * t < M) k0 = s_d[(2 * t) * a.dstr + kb];
+                if (2 * t + 1 < M) k1 = s_d[(2 * t + 1) * a.dstr + kb];
             }
             const uint8_t *r0 = row0 + 34 * b;
             const uint8_t *r8 = row8 + 34 * b;
@@ -423,9 +434,9 @@ __device__ __forceinline__ void q80_block_plain(const StreamArgs &a, const uint8
         uint4 x0, x1;
         float dj;
         if (MODE == kActSmem) {
-            x0 = lds128(s_qs + j * a.in_f + 32 * kb);
-            x1 = lds128(s_qs + j * a.in_f + 32 * kb + 16);
-            dj = s_d[j * a.nb + kb];
+            x0 = lds128(s_qs + j * a.qstr + 32 * kb);
+            x1 = lds128(s_qs + j * a.qstr + 32 * kb + 16);
+            dj = s_d[j * a.dstr + kb];
         } else {
             const uint4 *qx = reinterpret_cast<const uint4 *>(a.qs + static_cast<int64_t>(j) * a.in_f + 32 * kb);
             x0 = __ldcg(qx);
@@ -486,7 +497,7 @@ __device__ __forceinline__ void q80_stage_lane(const StreamArgs &a, const uint8_
                 s0 = __dp4a(static_cast<int>(w[6]), static_cast<int>(x1.z), s0);
                 s1 = __dp4a(static_cast<int>(w[7]), static_cast<int>(x1.w), s1);
                 s0 = __dp4a(static_cast<int>(w[8]), static_cast<int>(x2), s0);
-                acc[j] = fmaf(static_cast<float>(s0 + s1), dw * s_d[j * a.nb + kb], acc[j]);
+                acc[j] = fmaf(static_cast<float>(s0 + s1), dw * s_d[j * a.dstr + kb], acc[j]);
             }
         } else {
             q80_block_plain<M, MODE>(a, slot, sm, kb0, b, acc);
@@ -584,8 +595,8 @@ __device__ __forceinline__ void fused_quantize(const StreamArgs &a, int8_t *s_qs
                     static_cast<uint32_t>(static_cast<uint8_t>(quant_q8(zz.y, dd))) << 8 |
                     static_cast<uint32_t>(static_cast<uint8_t>(quant_q8(zz.z, dd))) << 16 |
                     static_cast<uint32_t>(static_cast<uint8_t>(quant_q8(zz.w, dd))) << 24;
-                reinterpret_cast<uint32_t *>(s_qs + j * a.in_f)[f] = packed;
-                if ((tid & 7) == 0) s_d[j * a.nb + (f >> 3)] = dd;
+                reinterpret_cast<uint32_t *>(s_qs + j * a.qstr)[f] = packed;
+                if ((tid & 7) == 0) s_d[j * a.dstr + (f >> 3)] = dd;
                 if (publish) {
                     reinterpret_cast<uint32_t *>(const_cast<int8_t *>(a.qs) + static_cast<int64_t>(j) * a.in_f)[f] = packed;
                     if ((tid & 7) == 0) const_cast<float *>(a.d)[j * a.nb + (f >> 3)] = dd;
@@ -764,17 +775,38 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
                           reinterpret_cast<float *>(smem + a.off_d), s_red,
                           reinterpret_cast<float *>(s_red + kWarps));
     } else if (MODE != kActGlobal) {
+        // one bulk copy per activation array, or one per token row where the staged rows are
+        // padded (row sizes and strides are multiples of 16 bytes there)
         const uint32_t qbytes = direct ? 0u : static_cast<uint32_t>(M * a.in_f);
         const uint32_t dbytes = static_cast<uint32_t>(M * a.nb * 4);
-        const bool d_bulk = (dbytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.d) & 15u) == 0;
+        const bool d_bulk = (a.nb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.d) & 15u) == 0;
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(act_bar, qbytes + (d_bulk ? dbytes : 0u));
-            if (qbytes) bulk_g2s_plain(smem + a.off_qs, a.qs, qbytes, act_bar);
-            if (d_bulk) bulk_g2s_plain(smem + a.off_d, a.d, dbytes, act_bar);
+            if (qbytes) {
+                if (a.qstr == a.in_f) {
+                    bulk_g2s_plain(smem + a.off_qs, a.qs, qbytes, act_bar);
+                } else {
+                    for (int j = 0; j < M; ++j)
+                        bulk_g2s_plain(smem + a.off_qs + j * a.qstr, a.qs + static_cast<int64_t>(j) * a.in_f,
+                                       static_cast<uint32_t>(a.in_f), act_bar);
+                }
+            }
+            if (d_bulk) {
+                if (a.dstr == a.nb) {
+                    bulk_g2s_plain(smem + a.off_d, a.d, dbytes, act_bar);
+                } else {
+                    for (int j = 0; j < M; ++j)
+                        bulk_g2s_plain(smem + a.off_d + j * a.dstr * 4, a.d + j * a.nb,
+                                       static_cast<uint32_t>(a.nb * 4), act_bar);
+                }
+            }
         }
         if (!d_bulk) {
             float *dst = reinterpret_cast<float *>(smem + a.off_d);
-            for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) dst[i] = __ldcg(a.d + i);
+            for (int i = threadIdx.x; i < M * a.nb; i += kConsumerThreads) {
+                const int j = i / a.nb;
+                dst[i + j * (a.dstr - a.nb)] = __ldcg(a.d + i);
+            }
         }
         if (direct) {
             const uint2 *src = reinterpret_cast<const uint2 *>(a.qs);
@@ -805,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
         const int n = a.nb * M;
         for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
             const int j = i / a.nb, kb = i - j * a.nb;
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(smem + a.off_qs + j * a.in_f + 32 * kb);
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(smem + a.off_qs + j * a.qstr + 32 * kb);
             uint32_t q[8], o[9];
 #pragma unroll
             for (int k = 0; k < 8; ++k) q[k] = src[k];
@@ -1279,9 +1311,17 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     // their region holds the qs at its top and no separate qs region is needed.
     const uint32_t frag = G::kMma ? align_up(static_cast<uint32_t>(m * (nb | 1) * 64), 128)
                                   : align_up(static_cast<uint32_t>(nb * m * 4 * kQ8ActWords), 128);
+    // Staged rows: from m = 5 (where 3 or 4 tokens' scales meet in one warp load) d padded to 4
+    // mod 16 floats and qs to 32 mod 128 bytes where the tensor-core consumers read it per block
+    // (kActSmem); the in-place fragment build and the dp4a layouts read qs contiguous.  Measured
+    // on GB300, 17408 x 5120: m = 8 E4M3 18.0 -> 16.1 us, Q8_0 23.6 -> 19.1 us; at m <= 4 the
+    // per-row copies cost more than the 2-way conflicts they remove (5120 x 5120 m = 3 +2%).
+    const int dstr = m >= 5 ? nb + ((4 - nb) & 15) : nb;
+    const int qstr_smem = G::kMma && m >= 5 ? static_cast<int>(in_f + ((32 - in_f) & 127)) : static_cast<int>(in_f);
     const uint32_t qsb = align_up(static_cast<uint32_t>(m * in_f), 128);
+    const uint32_t qsb_smem = align_up(static_cast<uint32_t>(m * qstr_smem), 128);
     const uint32_t frag_act = G::kMma ? frag : frag + qsb;
-    const uint32_t db = align_up(static_cast<uint32_t>(m * nb * 4), 128);
+    const uint32_t db = align_up(static_cast<uint32_t>(m * dstr * 4), 128);
     // block-128 with a staged activation: the CTA's d * grid table
     const uint32_t red = fuse ? align_up((kWarps + 1) * 8, 128) : 0u;
     const uint32_t ring_min = static_cast<uint32_t>(G::kMinStages * G::kStage) + 128;
@@ -1313,7 +1353,7 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
         const uint32_t budget = std::min(optin, static_cast<uint32_t>(info.smem_sm / k - 1024));
         if (base + frag_act + db <= budget) {
             mode = kActFrag;
-        } else if (base + qsb + db <= budget) {
+        } else if (base + qsb_smem + db <= budget) {
             mode = kActSmem;
         } else {
             continue;
@@ -1324,6 +1364,8 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     if (fuse && mode == kActGlobal) return false;
     a.grid_rows = grid_rows;
     a.ctas_per_sm = ctas;
+    a.qstr = mode == kActSmem ? qstr_smem : static_cast<int>(in_f);
+    a.dstr = mode == kActGlobal ? nb : dstr;
     a.off_part = 0;
     a.off_grid = a.off_part + part;
     uint32_t off = a.off_grid + gridb;
@@ -1334,7 +1376,7 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
         a.off_qs = a.off_bfrag + static_cast<uint32_t>(m * (nb | 1) * 64 - m * in_f);
     } else {
         a.off_qs = off;
-        if (mode != kActGlobal) off += qsb;
+        if (mode != kActGlobal) off += mode == kActSmem ? qsb_smem : qsb;
     }
     a.off_d = off;
     if (mode != kActGlobal) off += db;
@@ -1381,6 +1423,8 @@ StreamArgs base_args(const uint8_t *w, const float *aux, const int8_t *qs, const
     a.w = w;
     a.aux = aux;
     a.qs = qs;
+    a.qstr = static_cast<int>(in_f);
+    a.dstr = static_cast<int>(in_f / 32);
     a.d = d;
     a.y = y;
     a.out_f = out_f;
@@ -1490,78 +1534,6 @@ int group_entry(int count, const uint8_t *const *w, const float *const *aux, flo
     const cudaError_t e = launch_planned<KIND, false>(m, mode, a, smem, dev, info,
                                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
-}
-
-// Q8_0 calls choose between two arithmetics: the tensor-core paths (the K-outer kernel and the
-// tile kernel's kQ80T, bit-identical to each other) and dp4a.  The tensor cores serve a call
-// when K-outer applies (q80_kouter_applies: m >= 3 on CTAs of 8 to 16 rows) or when
-// q80_on_tensor_cores says so; K-outer is tried first.
-inline bool q80_tensor_path(int nmat, const int64_t *out_f, int64_t rows_all, int64_t in_f, int m,
-                            const int8_t *qs, const float *d, const DeviceInfo &info) {
-    return q80_kouter_applies(nmat, out_f, in_f, m, qs, d, info) ||
-           q80_on_tensor_cores(rows_all, in_f, m);
-}
-
-inline int q80_gemv_entry(const uint8_t *w, const int8_t *qs, const float *d, float *y,
-                          int64_t out_f, int64_t in_f, int m, void *stream) {
-    const int rc = check_gemv_args<kQ80>(w, nullptr, qs, d, y, out_f, in_f, m);
-    if (rc >= 0) return rc;
-    int dev = 0;
-    DeviceInfo info;
-    if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
-    if (fast_path_ok<kQ80T>(w, qs, in_f) && q80_kouter_applies(1, &out_f, in_f, m, qs, d, info)) {
-        const float *aux = nullptr;
-        const cudaError_t ek = launch_kouter_m<kQ80T>(m, 1, &w, &aux, &y, &out_f, qs, d, in_f, dev,
-                                                      info, static_cast<cudaStream_t>(stream));
-        if (ek != cudaErrorNotSupported) return ek == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
-        // a ring too shallow for the K-outer plan: the tile kernel's tensor-core path
-        return gemv_entry<kQ80T>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
-    }
-    if (q80_on_tensor_cores(out_f, in_f, m))
-        return gemv_entry<kQ80T>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
-    return gemv_entry<kQ80>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
-}
-
-// A Q8_0 group runs as one launch only if its path (tensor cores or dp4a) is the one each of its
-// matrices takes alone, so that every output equals the single call bit for bit; otherwise it
-// runs one call per matrix.
-inline int q80_group_entry(int count, const uint8_t *const *w, float *const *y,
-                           const int64_t *out_f, const int8_t *qs, const float *d, int64_t in_f,
-                           int m, void *stream) {
-    if (count < 1 || count > kMaxGroup) return MEMQ_ERR_SHAPE;
-    if (!w || !y || !out_f) return MEMQ_ERR_NULL;
-    int64_t rows_all = 0;
-    bool fast = true;
-    for (int i = 0; i < count; ++i) {
-        const int rc = check_gemv_args<kQ80>(w[i], nullptr, qs, d, y[i], out_f[i], in_f, m);
-        if (rc > 0) return rc;
-        if (rc == MEMQ_OK) return MEMQ_ERR_SHAPE;  // an empty matrix in a group
-        rows_all += out_f[i];
-        fast = fast && fast_path_ok<kQ80T>(w[i], qs, in_f);
-    }
-    int dev = 0;
-    DeviceInfo info;
-    if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
-    const bool tensor = q80_tensor_path(count, out_f, rows_all, in_f, m, qs, d, info);
-    bool same = fast;
-    for (int i = 0; i < count && same; ++i)
-        same = q80_tensor_path(1, &out_f[i], out_f[i], in_f, m, qs, d, info) == tensor;
-    if (same && tensor && q80_kouter_applies(count, out_f, in_f, m, qs, d, info)) {
-        const float *aux[kMaxGroup] = {};
-        const cudaError_t ek = launch_kouter_m<kQ80T>(m, count, w, aux, y, out_f, qs, d, in_f, dev,
-                                                      info, static_cast<cudaStream_t>(stream));
-        if (ek != cudaErrorNotSupported) return ek == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
-        same = m >= kQ80MmaMinM;
-    }
-    if (!same) {
-        for (int i = 0; i < count; ++i) {
-            const int rc = q80_gemv_entry(w[i], qs, d, y[i], out_f[i], in_f, m, stream);
-            if (rc != MEMQ_OK) return rc;
-        }
-        return MEMQ_OK;
-    }
-    if (tensor) return group_entry<kQ80T>(count, w, nullptr, y, out_f, qs, d, in_f, m, stream);
-    return group_entry<kQ80>(count, w, nullptr, y, out_f, qs, d, in_f, m, stream);
 }
 
 // The fused decode step: RMSNorm -> q8_1 of x (m rows) and the GEMV in one launch when the plan

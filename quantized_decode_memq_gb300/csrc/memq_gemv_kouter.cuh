@@ -126,14 +126,16 @@ __device__ __forceinline__ void ko_stage_q80(const KoArgs &a, const uint8_t *sta
     const int j0 = 4 * warp;
     const int nblk = FULL ? 4 : min(4, a.nb - kbc - j0);
     if (!FULL && nblk <= 0) return;
-    const uint8_t *aq = stage + a.act_qs + g * kKoActRow + 32 * j0 + 8 * t;
+    // B column g is token g; columns g >= M read token M - 1 (no divergent branch): an MMA
+    // column depends only on its own B column, and those columns are never stored
+    const uint8_t *aq = stage + a.act_qs + (g < M ? g : M - 1) * kKoActRow + 32 * j0 + 8 * t;
     const float *ad = reinterpret_cast<const float *>(stage + a.act_d) + 2 * t * kKoDRow + j0;
     const uint8_t *pa = stage + 34 * j0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         if (FULL || b < nblk) {
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
-            if (g < M) {
+            {
                 const uint2 qv = lds64(aq + 32 * b);
                 s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
                 s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
@@ -181,7 +183,9 @@ __device__ __forceinline__ void ko_stage(const KoArgs &a, const uint8_t *stage, 
     const int nblk = FULL ? 4 : min(4, a.nb - kbc - j0);
     if (!FULL && nblk <= 0) return;
     // this thread's activation bytes (token g) and scales (tokens 2t, 2t+1) of block j0
-    const uint8_t *aq = stage + a.act_qs + g * kKoActRow + 32 * j0 + 8 * t;
+    // B column g is token g; columns g >= M read token M - 1 (no divergent branch): an MMA
+    // column depends only on its own B column, and those columns are never stored
+    const uint8_t *aq = stage + a.act_qs + (g < M ? g : M - 1) * kKoActRow + 32 * j0 + 8 * t;
     const float *ad = reinterpret_cast<const float *>(stage + a.act_d) + 2 * t * kKoDRow + j0;
     const uint8_t *pa = stage + 32 * j0 + 8 * t;
     float grp[TILES][4];
@@ -191,7 +195,7 @@ __device__ __forceinline__ void ko_stage(const KoArgs &a, const uint8_t *stage, 
     for (int b = 0; b < 4; ++b) {
         if (FULL || b < nblk) {
             uint32_t bq[4] = {0u, 0u, 0u, 0u};
-            if (g < M) {
+            {
                 const uint2 qv = lds64(aq + 32 * b);
                 s8x4_to_f16x2x2(qv.x, bq[0], bq[1]);
                 s8x4_to_f16x2x2(qv.y, bq[2], bq[3]);
