@@ -105,9 +105,10 @@ int memq_rmsnorm_q8_1(const float *x, const float *w, float *z, int8_t *qs, floa
  * depend on m, on how the launch splits the rows, or on which of the library's kernels serves
  * the call, so a row's outputs are bit-identical whether it is computed alone, in an m-batch,
  * or in a group.
- * Q8_0: the same holds within each of its two paths (dp4a; tensor cores from m = 3 on large
- * shapes, m = 5 or 6 on others); across them the block sums are the same exact integers added
- * in another order, and results agree within the GEMV tolerance.
+ * Q8_0: the same holds within each of its two paths (dp4a at m = 1; tensor cores from m = 2
+ * when each CTA gets 8 to 16 rows of a wide activation, from m = 3 to 6 on other shapes); across
+ * them the block sums are the same exact integers added in another order, and results agree
+ * within the GEMV tolerance.
  */
 int memq_gemv_e4m3(const uint8_t *w, const float *w_scale, const int8_t *qs, const float *d,
                    float *y, int64_t out_f, int64_t in_f, int m, void *stream);

@@ -527,14 +527,14 @@ inline int64_t ko_rmax(int nmat, const int64_t *out_f, const DeviceInfo &info) {
     return rmax;
 }
 
-// Whether a Q8_0 call (or group) runs K-outer on the tensor cores: m >= 3 and the activation
+// Whether a Q8_0 call (or group) runs K-outer on the tensor cores: m >= 2 and the activation
 // and CTA-size conditions of launch_kouter.  The Q8_0 entry points decide their path (tensor
 // cores or dp4a) with it before launching.  Measured on GB300 (back-to-back, us, K-outer against
-// dp4a): 5120 x 17408 m = 2 23.8 / 23.1, m = 3 25.3 / 29.2, m = 4 23.4 / 35.9, m = 8 26.9 /
-// 62.2; 5120 x 5120 m = 4 9.1 / 10.9, m = 8 9.5 / 19.9.
+// dp4a): 5120 x 17408 m = 2 22.1 / 23.4, m = 4 22.2 / 35.9, m = 8 22.1 / 62.2; 5120 x 5120
+// m = 4 8.9 / 10.9, m = 8 8.0 / 19.9; at m = 1 dp4a (15.8 us at 5120 x 17408).
 inline bool q80_kouter_applies(int nmat, const int64_t *out_f, int64_t in_f, int m,
                                const int8_t *qs, const float *d, const DeviceInfo &info) {
-    if (m < 3 || in_f % 128 != 0 || !aligned(qs, 16) || !aligned(d, 16) || m * in_f < kKoMinAct)
+    if (m < 2 || in_f % 128 != 0 || !aligned(qs, 16) || !aligned(d, 16) || m * in_f < kKoMinAct)
         return false;
     const int64_t r = ko_rmax(nmat, out_f, info);
     return r >= 8 && r <= 16 * kKoTiles;
@@ -649,13 +649,11 @@ cudaError_t launch_kouter_m(int m, int nmat, const uint8_t *const *w, const floa
                             const float *d, int64_t in_f, int dev, const DeviceInfo &info,
                             cudaStream_t st) {
     switch (m) {
-        // Q8_0 at m <= 2 stays on dp4a (q80_kouter_applies)
+        // Q8_0 at m = 1 stays on dp4a (q80_kouter_applies)
         case 1:
             if constexpr (KIND == kQ80T) return cudaErrorNotSupported;
             else return launch_kouter<KIND, 1>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
-        case 2:
-            if constexpr (KIND == kQ80T) return cudaErrorNotSupported;
-            else return launch_kouter<KIND, 2>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
+        case 2: return launch_kouter<KIND, 2>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
         case 3: return launch_kouter<KIND, 3>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
         case 4: return launch_kouter<KIND, 4>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);
         case 5: return launch_kouter<KIND, 5>(nmat, w, aux, y, out_f, qs, d, in_f, dev, info, st);

@@ -8,7 +8,7 @@ namespace {
 
 // Q8_0 calls choose between two arithmetics: the tensor-core paths (the K-outer kernel and the
 // tile kernel's kQ80T, bit-identical to each other) and dp4a.  The tensor cores serve a call
-// when K-outer applies (q80_kouter_applies: m >= 3 on CTAs of 8 to 16 rows) or when
+// when K-outer applies (q80_kouter_applies: m >= 2 on CTAs of 8 to 16 rows) or when
 // q80_on_tensor_cores says so; K-outer is tried first.
 inline bool q80_tensor_path(int nmat, const int64_t *out_f, int64_t rows_all, int64_t in_f, int m,
                             const int8_t *qs, const float *d, const DeviceInfo &info) {
@@ -28,8 +28,10 @@ inline int q80_gemv_entry(const uint8_t *w, const int8_t *qs, const float *d, fl
         const cudaError_t ek = launch_kouter_m<kQ80T>(m, 1, &w, &aux, &y, &out_f, qs, d, in_f, dev,
                                                       info, static_cast<cudaStream_t>(stream));
         if (ek != cudaErrorNotSupported) return ek == cudaSuccess ? MEMQ_OK : MEMQ_ERR_LAUNCH;
-        // a ring too shallow for the K-outer plan: the tile kernel's tensor-core path
-        return gemv_entry<kQ80T>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
+        // a ring too shallow for the K-outer plan (it always fits at m = 2): the tile kernel's
+        // tensor-core path
+        if (m >= kQ80MmaMinM) return gemv_entry<kQ80T>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
+        return gemv_entry<kQ80>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
     }
     if (q80_on_tensor_cores(out_f, in_f, m))
         return gemv_entry<kQ80T>(w, nullptr, qs, d, y, out_f, in_f, m, stream);
