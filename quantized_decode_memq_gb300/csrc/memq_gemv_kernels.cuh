@@ -758,6 +758,8 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
     constexpr int kDirectItems = 3 * kR * kConsumerThreads;
     const int n_items = a.nb * M * 4;
     const bool direct = kFragMma && !FUSE && n_items <= kDirectItems;
+    // dp4a: the record-aligned layout of up to 512 blocks is built from global memory likewise
+    const bool direct_q80 = KIND == kQ80 && MODE == kActFrag && !FUSE && a.nb * M <= 2 * kConsumerThreads;
     const int pad = 4 * ((a.nb | 1) - a.nb);
     // token of item j: j / (4 nb) as a multiply-high by ceil(2^32 / (4 nb)), exact here since
     // j * 4nb < 2^32 (n <= 14.5K items fit the shared memory)
@@ -777,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
     } else if (MODE != kActGlobal) {
         // one bulk copy per activation array, or one per token row where the staged rows are
         // padded (row sizes and strides are multiples of 16 bytes there)
-        const uint32_t qbytes = direct ? 0u : static_cast<uint32_t>(M * a.in_f);
+        const uint32_t qbytes = direct || direct_q80 ? 0u : static_cast<uint32_t>(M * a.in_f);
         const uint32_t dbytes = static_cast<uint32_t>(M * a.nb * 4);
         const bool d_bulk = (a.nb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.d) & 15u) == 0;
         if (threadIdx.x == 0) {
@@ -832,18 +834,31 @@ __global__ void __launch_bounds__(kThreads, Geo<KIND>::kMinCtasPerSm)
         }
     }
     if (MODE == kActFrag && KIND == kQ80) {
-        // The dp4a layout of the whole activation (q80_stage_lane): per (token, block) nine words.
-        uint32_t *dst = reinterpret_cast<uint32_t *>(smem + a.off_bfrag);
+        // The dp4a layout of the whole activation (q80_stage_lane): per (token, block) nine words
+        // in a 12-word record, read and written as 16-byte vectors (records 48 bytes apart: the
+        // eight 16-byte accesses of a quarter-warp fall on distinct bank groups), from global
+        // memory for small activations, else from the staged qs.
+        uint8_t *dst = smem + a.off_bfrag;
         const int n = a.nb * M;
         for (int i = threadIdx.x; i < n; i += kConsumerThreads) {
             const int j = i / a.nb, kb = i - j * a.nb;
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(smem + a.off_qs + j * a.qstr + 32 * kb);
-            uint32_t q[8], o[9];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) q[k] = src[k];
+            uint4 v0, v1;
+            if (direct_q80) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.qs + static_cast<int64_t>(j) * a.in_f + 32 * kb);
+                v0 = __ldcg(src);
+                v1 = __ldcg(src + 1);
+            } else {
+                const uint8_t *src = smem + a.off_qs + j * a.qstr + 32 * kb;
+                v0 = lds128(src);
+                v1 = lds128(src + 16);
+            }
+            const uint32_t q[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t o[9];
             q80_act_layout(q, kb & 1, o);
-#pragma unroll
-            for (int k = 0; k < 9; ++k) dst[i * kQ8ActWords + k] = o[k];
+            uint8_t *rec = dst + static_cast<size_t>(i) * (kQ8ActWords * 4);
+            *reinterpret_cast<uint4 *>(rec) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(rec + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint32_t *>(rec + 32) = o[8];
         }
     } else if (kFragMma && !direct) {
         // qs (staged, or computed by the fused step) is at the top of the fragment region: item j

@@ -646,6 +646,9 @@ __device__ __forceinline__ void mma_3xtf32(float (&c)[4], const uint32_t (&ah)[4
 }
 
 constexpr int kTcHeads = 8;  // MMA N: the head columns of a group (H of them in use)
+// Row stride of the warp partials of the scores (floats): 10, so the softmax warp's 16 lanes
+// reading one head of 16 rows hit 16 distinct banks (a stride of 8 put 4 rows on each bank).
+constexpr int kRedRow = 10;
 
 template <int KV, int H>
 __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
@@ -660,8 +663,8 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
     const int n_slots = a.n_slots, S = a.stages, nh = a.nh;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm);       // [kMaxStages] rows landed
     float *ring = sm + 2 * kMaxStages;                        // [S][kRowsC][row_pad]
-    float *red = ring + S * stage_f;                          // [kMlaWarps][kRowsC][8] partials
-    float *pw = red + kMlaWarps * kRowsC * kTcHeads;          // [kRowsC][8] softmax weights
+    float *red = ring + S * stage_f;                          // [kMlaWarps][kRowsC][kRedRow] partials
+    float *pw = red + kMlaWarps * kRowsC * kRedRow;           // [kRowsC][8] softmax weights
     float *smm = pw + kRowsC * kTcHeads;                      // [8] running max
     float *sal = smm + kTcHeads;                              // [8] rescale factor
     float *sl = sal + kTcHeads;                               // [8] running sum
@@ -775,9 +778,9 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
                 else if constexpr (kChains == 2) sc[e] = sp[0][e] + sp[1][e];
                 else sc[e] = sp[0][e];
             }
-            float *rw = red + warp * (kRowsC * kTcHeads);
-            *reinterpret_cast<float2 *>(rw + g * kTcHeads + 2 * t) = make_float2(sc[0], sc[1]);
-            *reinterpret_cast<float2 *>(rw + (g + 8) * kTcHeads + 2 * t) = make_float2(sc[2], sc[3]);
+            float *rw = red + warp * (kRowsC * kRedRow);
+            *reinterpret_cast<float2 *>(rw + g * kRedRow + 2 * t) = make_float2(sc[0], sc[1]);
+            *reinterpret_cast<float2 *>(rw + (g + 8) * kRedRow + 2 * t) = make_float2(sc[2], sc[3]);
         }
         // The partials are complete, and every thread is done with chunk c - 1, whose stage
         // takes chunk c + S - 1.  A wait that gave up anywhere stops every warp here, together.
@@ -792,7 +795,7 @@ __global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kMlaThreads, 2)
             if (lane < nj) {
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < kMlaWarps; ++w) v += red[(w * kRowsC + lane) * kTcHeads + hh];
+                for (int w = 0; w < kMlaWarps; ++w) v += red[(w * kRowsC + lane) * kRedRow + hh];
                 s = __fmul_rn(a.scale, v);
             }
             float mc = fmaxf(mo, s);
@@ -1033,7 +1036,8 @@ template <int KV, int H>
 int launch_attn_tc(const AttnArgs &args0, int t, cudaStream_t st) {
     AttnArgs args = args0;
     constexpr int row_pad = KV * 128 + 8;
-    const size_t fixed = sizeof(float) * (2 * kMaxStages + (kMlaWarps + 1) * kRowsC * kTcHeads + 3 * kTcHeads);
+    const size_t fixed = sizeof(float) * (2 * kMaxStages + kMlaWarps * kRowsC * kRedRow + kRowsC * kTcHeads +
+                                          3 * kTcHeads);
     const size_t stage = sizeof(float) * static_cast<size_t>(kRowsC) * row_pad;
     const int64_t budget = 112 * 1024;
     int stages = static_cast<int>((budget - static_cast<int64_t>(fixed)) / static_cast<int64_t>(stage));
