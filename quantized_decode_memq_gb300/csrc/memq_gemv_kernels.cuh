@@ -7,28 +7,28 @@
 // E4M3: raw E4M3 bytes, one per-tensor scale; arm Q8_0: ggml block_q8_0, 34 B per 32 weights)
 // and "THE BLOCK-128 ARM" (E4M3 plus an f32 [ceil(out_f/128), ceil(in_f/128)] scale grid).
 //
-// Fast path ("stream" kernel), one skeleton for all three containers:
-//   * CTA c owns output rows [R0, R1), an equal share (+-1 row) of out_f, so every SM streams
-//     the same number of weight bytes.  The CTA walks its rows tile by tile and each tile's K
-//     dimension chunk by chunk (32 blocks = 1 KB of E4M3, 1088 B of Q8_0, per row).
-//   * One producer warp fills a shared ring of S stages: a stage is one chunk of every row of
-//     the tile, loaded with one 1-D bulk asynchronous copy (cp.async.bulk, L2 evict-first) per
-//     row that completes on the stage's "full" mbarrier.  Eight consumer warps wait on it
-//     (bounded), compute, and release the stage on its "empty" mbarrier.  Copies are 1 KB each:
-//     the bulk-copy instruction is issued per row, so large rows pieces keep its cost per byte
-//     low.
-//   * E4M3 / block-128: 16-row tiles; consumer warp w takes blocks 4w..4w+3 of every stage and
-//     computes them on the tensor cores (mma.sync m16n8k16, f16 operands, f32 accumulation):
-//     E4M3 -> f16 (hardware cvt) and int8 -> f16 are exact and f16 x f16 products are exact in
-//     f32, so this is numerically an f32 dot product.  At the end of a tile each warp leaves its
-//     partial sums in shared memory; after one barrier among the consumers the 8 partials of each
-//     (row, token) are added in warp order (deterministic) and stored.  (A CUDA-core FMA version
-//     of this loop measured issue-bound: 61% issue-active at 35% of DRAM bandwidth.)
-//   * Q8_0: 8-row tiles; consumer warp w owns row w of the tile, lane l owns block l of every
-//     stage, and dp4a gives the exact int32 dot product of each block.
-//   * The producer never reads what the preceding launch writes, so it starts streaming at once;
-//     the consumers wait for the preceding launch (programmatic dependent launch) before they
-//     read the activation.
+// Fast path (the "stream" or tile kernel), one skeleton for all three containers:
+//   * CTA c owns output rows [R0, R1), an equal share (+-1 row) of out_f.  It walks its rows in
+//     16-row tiles and each tile's K dimension in chunks of 32 blocks (1 KB of E4M3, 1088 B of
+//     Q8_0 per row).
+//   * One producer warp fills a shared ring of S stages: a full tile (or the first 8 rows of a
+//     ragged one) arrives as one 2-D tensor copy (cp.async.bulk.tensor, L2 evict-first) into row
+//     slots padded against bank conflicts, leftover rows as 1-D bulk copies, all completing on
+//     the stage's "full" mbarrier.  Eight consumer warps wait on it (bounded), compute, and
+//     release the stage on its "empty" mbarrier.
+//   * E4M3 / block-128, and Q8_0 from a few activation rows on: consumer warp w takes blocks
+//     4w..4w+3 of every stage and computes them on the tensor cores (mma.sync m16n8k16, f16
+//     operands, f32 accumulation); E4M3 -> f16 (hardware cvt) and int8 -> f16 are exact and f16 x
+//     f16 products are exact in f32.  At the end of a tile each warp leaves its partial sums in
+//     shared memory; after one barrier among the consumers the 8 partials of each (row, token)
+//     are added in warp order (deterministic) and stored.
+//   * Q8_0 with dp4a: warp w takes rows 2w and 2w + 1 (one per half-warp), lane l blocks l % 16
+//     and l % 16 + 16 of every stage; dp4a gives the exact int32 dot product of each block.
+//   * The activation is read once per CTA, after the wait for the preceding launch: as f16 MMA
+//     fragments, as staged qs / d, or in the dp4a record-aligned layout.  The producer starts
+//     streaming before that wait (programmatic dependent launch): it never reads what the
+//     preceding launch writes.
+// The K-outer kernel (memq_gemv_kouter.cuh) serves CTAs of 8 to 16 rows with wide activations.
 // Generic path: a plain warp-per-row kernel with byte loads for anything the fast path does not
 // take (unaligned pointers, Q8_0 rows that are not 16-byte aligned).
 #pragma once
