@@ -606,7 +606,13 @@ cudaError_t launch_kouter(int nmat, const uint8_t *const *w, const float *const 
     const uint32_t bars = align_up(static_cast<uint32_t>(2 * kKoMaxStages * 8), 128);
     if (bars + part + gridb + static_cast<uint32_t>(kKoMinStages * a.stage) > budget)
         return cudaErrorNotSupported;
-    a.stages = static_cast<int>(std::min<uint32_t>(kKoMaxStages, (budget - bars - part - gridb) / a.stage));
+    // At most 3 stages when the K sweep is short (<= 8 chunks): a ring holding most of a CTA's
+    // rows is mostly requested before the preceding launch ends and competes with its tail
+    // (measured on GB300, 5120 x 5120 m = 4: 7.07 us with 4 stages, 6.35 with 3; 5120 x 17408,
+    // 17 chunks: no change).
+    const int nch = (a.nb + kKoKw - 1) / kKoKw;
+    const uint32_t cap = nch <= 8 ? 3u : static_cast<uint32_t>(kKoMaxStages);
+    a.stages = static_cast<int>(std::min<uint32_t>(cap, (budget - bars - part - gridb) / a.stage));
     a.off_part = bars;
     a.off_grid = a.off_part + part;
     a.off_ring = a.off_grid + gridb;
