@@ -307,6 +307,16 @@ class DecodeStep:
             self.producer()
             self.gemv(i)
 
+    def host_step(self, i, x_host, y_host):
+        """The whole decode step for host-resident rows in one native call: x_host -> x, the
+        fused step, y -> y_host, and the call's own wait for the stream."""
+        c = i % self.copies
+        container = {"q8_0": self.memq.Container.Q8_0, "blk": self.memq.Container.E4M3_BLK128,
+                     "e4m3": self.memq.Container.E4M3}[self.kind]
+        self.memq.memq_decode_step_host(container, x_host, self.x, self.wn, self.w[c],
+                                        None if self.aux is None else self.aux[c], y_host, 1e-6,
+                                        qs=self.qs, d=self.d, y_dev=self.y)
+
 
 class ProducerStep:
     """The RMSNorm -> q8_1 producer alone on rows x ncols (z written, as the fused producer of
@@ -572,6 +582,10 @@ def run_ours(args, world, rank, local):
     e2e_t, e2e_units = aggregate(e2e["elapsed"], float(e2e["steps"] * wl.step_bytes))
     eager = time_e2e(wl, stream, steps=min(K, args.e2e_steps))
     eager_t, eager_units = aggregate(eager["elapsed"], float(eager["steps"] * wl.step_bytes))
+    hcall = time_e2e_host_call(wl, stream, steps=min(K, args.e2e_steps))
+    hcall_t, hcall_units = aggregate(hcall["elapsed"], float(hcall["steps"] * wl.step_bytes))
+    ccall = time_e2e_c_abi(wl, stream, steps=min(K, args.e2e_steps))
+    ccall_t, ccall_units = aggregate(ccall["elapsed"], float(ccall["steps"] * wl.step_bytes))
 
     line = {
         "metric": METRIC,
@@ -628,6 +642,15 @@ def run_ours(args, world, rank, local):
             "eager": {"value": round(eager_units / eager_t / 1e9, 3),
                       "us_per_step": round(eager_t / eager["steps"] * 1e6, 2),
                       "mode": "the same calls issued from Python every step"},
+            "host_call": {"value": round(hcall_units / hcall_t / 1e9, 3),
+                          "us_per_step": round(hcall_t / hcall["steps"] * 1e6, 2),
+                          "mode": "one memq_decode_step_host call per step: H2D of x from "
+                                  "pinned memory, the fused step, D2H of y and the wait, in "
+                                  "one native call"},
+            "host_call_c_abi": {"value": round(ccall_units / ccall_t / 1e9, 3),
+                                "us_per_step": round(ccall_t / ccall["steps"] * 1e6, 2),
+                                "mode": "the same C entry point called through ctypes with "
+                                        "prepared arguments (no Python argument checks)"},
         },
         "gpu_launches": (1 if fused else 2) * K,
         "clocks": clocks,
@@ -1362,6 +1385,51 @@ def time_gemv_back_to_back(wl, stream, n, fn=None):
         b.record(stream)
     stream.synchronize()
     return a.elapsed_time(b) / 1e3 / (4 * n)
+
+
+def time_e2e_host_call(wl, stream, steps):
+    """Per step one memq_decode_step_host call (pinned x in, fused step, pinned y out, the
+    call's own wait), rotating the weight copies; host wall clock."""
+    import torch
+    x_pin = torch.from_numpy(wl.x_host.copy()).pin_memory()
+    y_pin = torch.empty(wl.y.shape, dtype=torch.float32).pin_memory()
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            wl.host_step(i, x_pin, y_pin)
+        t0 = time.perf_counter()
+        for i in range(steps):
+            wl.host_step(i, x_pin, y_pin)
+        wall = time.perf_counter() - t0
+    return {"elapsed": wall, "steps": steps, "h2d": x_pin.numel() * 4, "d2h": y_pin.numel() * 4}
+
+
+def time_e2e_c_abi(wl, stream, steps):
+    """As time_e2e_host_call, calling the C entry point memq_decode_step_host directly through
+    ctypes with its arguments prepared once per weight copy: the cost of the C-ABI call itself,
+    as a native caller pays it (no Python argument checks)."""
+    import ctypes
+    import torch
+    x_pin = torch.from_numpy(wl.x_host.copy()).pin_memory()
+    y_pin = torch.empty(wl.y.shape, dtype=torch.float32).pin_memory()
+    memq = wl.memq
+    container = {"q8_0": memq.Container.Q8_0, "blk": memq.Container.E4M3_BLK128,
+                 "e4m3": memq.Container.E4M3}[wl.kind]
+    fn = memq.lib().memq_decode_step_host
+    args = [(int(container), x_pin.data_ptr(), wl.x.data_ptr(), wl.wn.data_ptr(),
+             ctypes.c_float(1e-6), wl.w[c].data_ptr(),
+             None if wl.aux is None else wl.aux[c].data_ptr(), wl.qs.data_ptr(), wl.d.data_ptr(),
+             None, wl.y.data_ptr(), y_pin.data_ptr(), wl.out_f, wl.in_f, wl.m, stream.cuda_stream)
+            for c in range(wl.copies)]
+    bad = 0
+    for i in range(8):
+        bad |= fn(*args[i % wl.copies])
+    t0 = time.perf_counter()
+    for i in range(steps):
+        bad |= fn(*args[i % wl.copies])
+    wall = time.perf_counter() - t0
+    if bad:
+        raise RuntimeError("memq_decode_step_host failed in the timed loop")
+    return {"elapsed": wall, "steps": steps, "h2d": x_pin.numel() * 4, "d2h": y_pin.numel() * 4}
 
 
 def time_e2e(wl, stream, steps, graphs=False):

@@ -9,7 +9,7 @@
  *      memq_gemv_q8_0         ggml block_q8_0 weights (f16 scale + 32 int8)     (1.0625 B/weight)
  *
  * Around them: the fused decode steps memq_rmsnorm_q8_1_gemv_* (stage 1 inside the GEMV
- * launch), the grouped GEMVs memq_gemv_*_group, the silu(gate) * up -> q8_1 producer
+ * launch), the decode step for host-resident rows memq_decode_step_host, the grouped GEMVs memq_gemv_*_group, the silu(gate) * up -> q8_1 producer
  * memq_silu_mul_q8_1, the load-time repack of E4M3 weights into a Q8_0 slab,
  * memq_repack_e4m3[_blk128]_q8_0, and the t <= 8 MLA decode attention kernels memq_mla_absorb_q,
  * memq_mla_attn_gathered and memq_mla_decompress_v.
@@ -25,7 +25,8 @@
  *     (cudaMalloc / torch CUDA tensors).  The caller owns every buffer; the library never
  *     allocates, frees or keeps a pointer after the call returns.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue work;
- *     they never synchronize.  Results are ready when the stream reaches the launch.  Launches
+ *     they never synchronize (except memq_decode_step_host and memq_device_fault, which wait
+ *     for the stream).  Results are ready when the stream reaches the launch.  Launches
  *     may begin before the preceding work on the stream has finished (programmatic dependent
  *     launch), but read nothing the stream wrote before that work is complete; callers see
  *     plain stream order.
@@ -162,6 +163,40 @@ int memq_rmsnorm_q8_1_gemv_e4m3_blk128(const float *x, const float *wn, float ep
 int memq_rmsnorm_q8_1_gemv_q8_0(const float *x, const float *wn, float eps, const void *w,
                                 int8_t *qs, float *d, float *z, float *y, int64_t out_f,
                                 int64_t in_f, int m, void *stream);
+
+/* The weight containers of the GEMVs, for the entry points that take one as an argument. */
+typedef enum memq_container {
+    MEMQ_CONTAINER_E4M3 = 0,        /* memq_gemv_e4m3: aux = the per-tensor w_scale */
+    MEMQ_CONTAINER_E4M3_BLK128 = 1, /* memq_gemv_e4m3_blk128: aux = the block-128 grid */
+    MEMQ_CONTAINER_Q8_0 = 2         /* memq_gemv_q8_0: aux is not read (may be NULL) */
+} memq_container;
+
+/*
+ * memq_decode_step_host -- one decode step for a caller whose activation rows and outputs are
+ * in HOST memory (a host-side sampler or scheduler that hands over one token's hidden rows and
+ * reads the projection back): copies x_host to x_dev, runs memq_rmsnorm_q8_1_gemv_<container>
+ * on the device buffers, copies y_dev to y_host, and waits for the stream.  The operation is the
+ * fused step's (q8_fuse_gate.rs, module doc; the GEMV of gemv_e4m3_bench.rs, "THE
+ * COMPARISON"); the copies and the wait are the host path around it, in one native call.
+ *   container  a memq_container; any other value returns MEMQ_ERR_SHAPE
+ *   x_host     host, f32 [m][in_f] (page-locked memory gives the asynchronous, fastest copy;
+ *              pageable memory works)
+ *   x_dev      device, f32 [m][in_f], 16-byte aligned: the caller's device buffer for the copy
+ *   y_dev      device, f32 [m][out_f]: the caller's device buffer for the result
+ *   y_host     host, f32 [m][out_f]; may be NULL when out_f == 0
+ *   wn, eps, w, aux, qs, d, z, out_f, in_f, m: as memq_rmsnorm_q8_1_gemv_<container> (x = x_dev,
+ *              y = y_dev; aux = w_scale or grid, not read for Q8_0), with the same checks
+ * Unlike the other entry points this call WAITS: it returns once the stream has finished
+ * everything enqueued on it up to and including the copy to y_host, so y_host holds the
+ * result, bit-identical to memq_rmsnorm_q8_1_gemv_<container> on x_dev.  Arguments are
+ * checked before anything is enqueued (an error writes nothing); a failing copy, launch or
+ * wait returns MEMQ_ERR_LAUNCH after the stream has been waited for, so no copy still touches
+ * the host buffers.  Not for stream capture (it waits).
+ */
+int memq_decode_step_host(int container, const float *x_host, float *x_dev, const float *wn,
+                          float eps, const void *w, const float *aux, int8_t *qs, float *d,
+                          float *z, float *y_dev, float *y_host, int64_t out_f, int64_t in_f,
+                          int m, void *stream);
 
 /*
  * memq_gemv_*_group -- up to 4 GEMVs of the same container that share one activation (qs, d,

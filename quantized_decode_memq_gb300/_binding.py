@@ -28,6 +28,12 @@ class Status(enum.IntEnum):
     ERR_DEVICE = 6
 
 
+class Container(enum.IntEnum):
+    E4M3 = 0
+    E4M3_BLK128 = 1
+    Q8_0 = 2
+
+
 class MemqError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
@@ -73,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.memq_mla_decompress_v.argtypes = [P, P, P, I32, I32, I32, I32, I32, P]
             L.memq_mla_attn_gathered.argtypes = [P, P, P, P, P, I32, I32, I32, I32, I32,
                                                  ctypes.c_float, I32, P]
+            L.memq_decode_step_host.argtypes = [I32, P, P, P, ctypes.c_float, P, P, P, P, P, P,
+                                                P, I64, I64, I32, P]
             L.memq_device_fault.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             L.memq_status_string.argtypes = [I32]
             L.memq_status_string.restype = ctypes.c_char_p
@@ -82,7 +90,8 @@ def lib() -> ctypes.CDLL:
                          "memq_rmsnorm_q8_1_gemv_e4m3_blk128", "memq_rmsnorm_q8_1_gemv_q8_0",
                          "memq_gemv_e4m3_group", "memq_gemv_e4m3_blk128_group",
                          "memq_gemv_q8_0_group", "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
-                         "memq_repack_e4m3_blk128_q8_0", "memq_device_fault", "memq_version"):
+                         "memq_repack_e4m3_blk128_q8_0", "memq_decode_step_host",
+                         "memq_device_fault", "memq_version"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -297,6 +306,56 @@ def memq_rmsnorm_q8_1_gemv_q8_0(x, wn, w, eps: float = 1e-6, *, qs=None, d=None,
                                            _stream(stream))
     _check("memq_rmsnorm_q8_1_gemv_q8_0", rc)
     return y, qs, d, z
+
+
+def _host(name: str, t: torch.Tensor, shape):
+    if (isinstance(t, torch.Tensor) and t.dtype is torch.float32 and not t.is_cuda
+            and t.is_contiguous() and t.shape == shape):
+        return t
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor, got {t.device}")
+    if t.dtype is not torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 tensor")
+    raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def memq_decode_step_host(container, x_host, x_dev, wn, w, aux, y_host, eps: float = 1e-6, *,
+                          qs, d, y_dev, z=None, stream=None):
+    """Decode step with the activation rows and the result in host memory, in one native call:
+    x_host -> x_dev, the fused step on the device buffers, y_dev -> y_host, then a wait for the
+    stream.
+    `container` is a Container; x_host / y_host are contiguous float32 CPU tensors (pinned for
+    the asynchronous copy), every other buffer a preallocated CUDA tensor.  Returns y_host."""
+    container = int(container)
+    if container not in (0, 1, 2):
+        raise ValueError(f"container must be a Container, got {container}")
+    _cuda("w", w, torch.uint8)
+    out_f, row_bytes = w.shape
+    if container == Container.Q8_0:
+        if row_bytes % 34 != 0:
+            raise ValueError("Q8_0 rows must be a whole number of 34-byte blocks")
+        in_f = row_bytes // 34 * 32
+    else:
+        in_f = row_bytes
+        shape = (1,) if container == Container.E4M3 else ((out_f + 127) // 128, (in_f + 127) // 128)
+        _cuda("aux", aux, torch.float32, shape)
+    x2, m = _fused_in(x_dev, wn, in_f)
+    _host("x_host", x_host if x_host.dim() == 2 else x_host.reshape(1, -1), (m, in_f))
+    _host("y_host", y_host, (m, out_f))
+    _cuda("qs", qs, torch.int8, (m, in_f))
+    _cuda("d", d, torch.float32, (m, in_f // 32))
+    _cuda("y_dev", y_dev, torch.float32, (m, out_f))
+    if z is not None:
+        _cuda("z", z, torch.float32, (m, in_f))
+    rc = lib().memq_decode_step_host(container, _ptr(x_host), _ptr(x2), _ptr(wn),
+                                     ctypes.c_float(eps), _ptr(w),
+                                     None if container == Container.Q8_0 else _ptr(aux),
+                                     _ptr(qs), _ptr(d), _ptr(z), _ptr(y_dev), _ptr(y_host),
+                                     out_f, in_f, m, _stream(stream))
+    _check("memq_decode_step_host", rc)
+    return y_host
 
 
 def memq_device_fault(stream=None) -> int:

@@ -8,6 +8,37 @@ int memq_internal_fault_e4m3(unsigned int *out, bool clear);
 int memq_internal_fault_blk128(unsigned int *out, bool clear);
 int memq_internal_fault_q8_0(unsigned int *out, bool clear);
 int memq_internal_fault_mla(unsigned int *out, bool clear);
+int memq_internal_step_host_e4m3(const float *x_host, float *x_dev, const float *wn, float eps,
+                                 const void *w, const float *aux, int8_t *qs, float *d, float *z,
+                                 float *y_dev, float *y_host, int64_t out_f, int64_t in_f, int m,
+                                 void *stream);
+int memq_internal_step_host_blk128(const float *x_host, float *x_dev, const float *wn, float eps,
+                                   const void *w, const float *aux, int8_t *qs, float *d, float *z,
+                                   float *y_dev, float *y_host, int64_t out_f, int64_t in_f, int m,
+                                   void *stream);
+int memq_internal_step_host_q8_0(const float *x_host, float *x_dev, const float *wn, float eps,
+                                 const void *w, const float *aux, int8_t *qs, float *d, float *z,
+                                 float *y_dev, float *y_host, int64_t out_f, int64_t in_f, int m,
+                                 void *stream);
+
+extern "C" int memq_decode_step_host(int container, const float *x_host, float *x_dev,
+                                     const float *wn, float eps, const void *w, const float *aux,
+                                     int8_t *qs, float *d, float *z, float *y_dev, float *y_host,
+                                     int64_t out_f, int64_t in_f, int m, void *stream) {
+    switch (container) {
+        case MEMQ_CONTAINER_E4M3:
+            return memq_internal_step_host_e4m3(x_host, x_dev, wn, eps, w, aux, qs, d, z, y_dev,
+                                                y_host, out_f, in_f, m, stream);
+        case MEMQ_CONTAINER_E4M3_BLK128:
+            return memq_internal_step_host_blk128(x_host, x_dev, wn, eps, w, aux, qs, d, z, y_dev,
+                                                  y_host, out_f, in_f, m, stream);
+        case MEMQ_CONTAINER_Q8_0:
+            return memq_internal_step_host_q8_0(x_host, x_dev, wn, eps, w, aux, qs, d, z, y_dev,
+                                                y_host, out_f, in_f, m, stream);
+        default:
+            return MEMQ_ERR_SHAPE;
+    }
+}
 
 extern "C" int memq_device_fault(void *stream, uint32_t *fault_out) {
     if (!fault_out) return MEMQ_ERR_NULL;

@@ -1566,21 +1566,27 @@ int group_entry(int count, const uint8_t *const *w, const float *const *aux, flo
 // allows it, else memq_rmsnorm_q8_1 followed by the GEMV.  Either way qs / d (and z when given)
 // receive the activation.
 template <int KIND>
-int fused_entry(const float *x, const float *wn, float eps, const uint8_t *w, const float *aux,
-                int8_t *qs, float *d, float *z, float *y, int64_t out_f, int64_t in_f, int m,
-                void *stream) {
+int fused_check(const float *x, const float *wn, float eps, const uint8_t *w, const float *aux,
+                int8_t *qs, float *d, float *z, float *y, int64_t out_f, int64_t in_f, int m) {
+    // check_gemv_args: > 0 an error; MEMQ_OK when out_f == 0 (nothing to multiply, the
+    // activation is still produced); < 0 work to do
     const int rc = check_gemv_args<KIND>(w, aux, qs, d, y, out_f, in_f, m);
-    if (rc == MEMQ_OK && out_f == 0) {
-        // Nothing to multiply; the activation is still produced.
-    } else if (rc >= 0) {
-        return rc;
-    }
+    if (rc > 0) return rc;
     if (in_f > MEMQ_MAX_NCOLS) return MEMQ_ERR_SHAPE;
     if (!(eps >= 0.0f) || eps == INFINITY) return MEMQ_ERR_SHAPE;
     if (!x || !wn || !qs || !d) return MEMQ_ERR_NULL;
     if (!aligned(x, 16) || !aligned(wn, 16) || (z && !aligned(z, 16)) || !aligned(qs, 4) ||
         !aligned(d, 4))
         return MEMQ_ERR_ALIGN;
+    return MEMQ_OK;
+}
+
+template <int KIND>
+int fused_entry(const float *x, const float *wn, float eps, const uint8_t *w, const float *aux,
+                int8_t *qs, float *d, float *z, float *y, int64_t out_f, int64_t in_f, int m,
+                void *stream) {
+    const int rc = fused_check<KIND>(x, wn, eps, w, aux, qs, d, z, y, out_f, in_f, m);
+    if (rc != MEMQ_OK) return rc;
     int dev = 0;
     DeviceInfo info;
     if (device_info(dev, info) != cudaSuccess) return MEMQ_ERR_LAUNCH;
@@ -1601,6 +1607,33 @@ int fused_entry(const float *x, const float *wn, float eps, const uint8_t *w, co
     const int r = memq_rmsnorm_q8_1(x, wn, z, qs, d, in_f, m, eps, stream);
     if (r != MEMQ_OK || out_f == 0) return r;
     return gemv_entry<KIND>(w, aux, qs, d, y, out_f, in_f, m, stream);
+}
+
+// One decode step for a caller whose activation rows and outputs live in host memory: the
+// arguments are checked as the fused step checks them (nothing is enqueued on an error), then
+// x_host -> x_dev, `step()` (the fused step on the device buffers), y_dev -> y_host,
+// and a wait for the stream.  Past the checks, a failure still waits for the stream, so that
+// no copy is left reading or writing the host buffers when the call returns.
+template <int KIND, typename Step>
+int host_step_entry(const float *x_host, float *x_dev, const float *wn, float eps,
+                    const uint8_t *w, const float *aux, int8_t *qs, float *d, float *z,
+                    float *y_dev, float *y_host, int64_t out_f, int64_t in_f, int m, void *stream,
+                    Step step) {
+    const int rc = fused_check<KIND>(x_dev, wn, eps, w, aux, qs, d, z, y_dev, out_f, in_f, m);
+    if (rc != MEMQ_OK) return rc;
+    if (!x_host || (out_f > 0 && !y_host)) return MEMQ_ERR_NULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t x_bytes = sizeof(float) * static_cast<size_t>(m) * static_cast<size_t>(in_f);
+    const size_t y_bytes = sizeof(float) * static_cast<size_t>(m) * static_cast<size_t>(out_f);
+    int r = cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) == cudaSuccess
+                ? MEMQ_OK
+                : MEMQ_ERR_LAUNCH;
+    if (r == MEMQ_OK) r = step();
+    if (r == MEMQ_OK && y_bytes > 0 &&
+        cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        r = MEMQ_ERR_LAUNCH;
+    const bool waited = cudaStreamSynchronize(st) == cudaSuccess;
+    return r != MEMQ_OK ? r : waited ? MEMQ_OK : MEMQ_ERR_LAUNCH;
 }
 
 // Reads (and optionally clears) this translation unit's device fault word.

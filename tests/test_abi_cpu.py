@@ -40,7 +40,8 @@ def test_header_declares_the_boundary():
                      "memq_gemv_q8_0_group", "memq_silu_mul_q8_1", "memq_repack_e4m3_q8_0",
                      "memq_repack_e4m3_blk128_q8_0", "memq_mla_absorb_q",
                      "memq_mla_decompress_v", "memq_mla_attn_gathered",
-                     "memq_status_string", "memq_device_fault", "memq_version"):
+                     "memq_decode_step_host", "memq_status_string", "memq_device_fault",
+                     "memq_version"):
         assert required in names
 
 
@@ -78,6 +79,16 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert lib.memq_rmsnorm_q8_1_gemv_q8_0(None, fake, 1e-6, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_NULL
     assert lib.memq_rmsnorm_q8_1_gemv_e4m3(fake, fake, 1e-6, fake, fake, fake, fake, None, fake, 4, 64, 9, None) == m.Status.ERR_M_RANGE
     assert lib.memq_rmsnorm_q8_1_gemv_e4m3_blk128(fake, fake, -1.0, fake, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_SHAPE
+    # host-buffer decode step: the same checks, plus the container and the host pointers, all
+    # before any copy
+    host_args = [fake, fake, 1e-6, fake, fake, fake, fake, None, fake, fake, 4, 64]
+    assert lib.memq_decode_step_host(3, fake, *host_args, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_decode_step_host(-1, fake, *host_args, 1, None) == m.Status.ERR_SHAPE
+    assert lib.memq_decode_step_host(0, None, *host_args, 1, None) == m.Status.ERR_NULL
+    assert lib.memq_decode_step_host(2, fake, *host_args, 0, None) == m.Status.ERR_M_RANGE
+    assert lib.memq_decode_step_host(1, fake, P(0x1004), *host_args[1:], 1, None) == m.Status.ERR_ALIGN
+    no_y_host = host_args[:9] + [None] + host_args[10:]
+    assert lib.memq_decode_step_host(2, fake, *no_y_host, 1, None) == m.Status.ERR_NULL
     assert lib.memq_rmsnorm_q8_1_gemv_q8_0(fake, fake, 1e-6, fake, fake, fake, None, fake, 4, 65536, 1, None) == m.Status.ERR_SHAPE
     assert lib.memq_rmsnorm_q8_1_gemv_q8_0(P(0x1004), fake, 1e-6, fake, fake, fake, None, fake, 4, 64, 1, None) == m.Status.ERR_ALIGN
     # grouped GEMVs: the count and the host arrays are checked first

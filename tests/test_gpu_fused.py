@@ -134,3 +134,67 @@ def test_fused_matches_split_chain(memq, oracle):
         # both are within 2e-5*S of the oracle on their own activation; the activations differ
         # at most in rare +-1 codes next to a .5 boundary
         assert np.all(diff <= 1e-4 * s_ref)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("out_f,in_f,m,pinned", [(4096, 4096, 1, True), (777, 5120, 3, False),
+                                                 (5120, 5120, 8, True)])
+def test_decode_step_host_matches_fused(memq, oracle, kind, out_f, in_f, m, pinned):
+    """memq_decode_step_host: x from host memory, the fused step, y back to host memory, in one
+    call.  y_host, qs, d and z equal those of memq_rmsnorm_q8_1_gemv_* on the same device inputs
+    bit for bit, with page-locked and with pageable host buffers, on two calls in a row; y is
+    within the GEMV tolerance of the oracle."""
+    x, wn = synth.activation_rows(in_f, m)
+    w, aux = weights(kind, out_f, in_f, out_f + m)
+    wd, wnd = to_dev(w), to_dev(wn)
+    auxd = None if aux is None else to_dev(aux)
+    y_ref, qs_ref, d_ref, z_ref = fused(memq, kind, x, wn, w, aux, wd=wd)
+    container = {"e4m3": memq.Container.E4M3, "blk": memq.Container.E4M3_BLK128,
+                 "q8_0": memq.Container.Q8_0}[kind]
+    x_host = torch.from_numpy(x.copy())
+    y_host = torch.full((m, out_f), float("nan"))
+    if pinned:
+        x_host, y_host = x_host.pin_memory(), y_host.pin_memory()
+    x_dev = torch.empty((m, in_f), dtype=torch.float32, device="cuda")
+    qs = torch.empty((m, in_f), dtype=torch.int8, device="cuda")
+    d = torch.empty((m, in_f // 32), dtype=torch.float32, device="cuda")
+    z = torch.empty((m, in_f), dtype=torch.float32, device="cuda")
+    y_dev = torch.empty((m, out_f), dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        out = memq.memq_decode_step_host(container, x_host, x_dev, wnd, wd, auxd, y_host, EPS,
+                                         qs=qs, d=d, y_dev=y_dev, z=z)
+        assert out is y_host
+        # the call has waited: y_host is final without a synchronize
+        assert torch.equal(y_host, y_ref.cpu())
+        assert torch.equal(x_dev.cpu(), x_host)
+        assert torch.equal(qs.cpu(), qs_ref.cpu()) and torch.equal(d.cpu(), d_ref.cpu())
+        assert torch.equal(z.cpu(), z_ref.cpu())
+        y_host.fill_(float("nan"))
+    memq.memq_decode_step_host(container, x_host, x_dev, wnd, wd, auxd, y_host, EPS, qs=qs, d=d,
+                               y_dev=y_dev)
+    rows = sample_rows(out_f, 64, seed=m) if out_f > 1024 else None
+    check_gemv(y_host, *ref(oracle, kind, w, aux, qs.cpu().numpy(), d.cpu().numpy(), in_f,
+                            rows=rows), rows=rows)
+    assert memq.memq_device_fault() == 0
+
+
+def test_decode_step_host_rejects_before_copying(memq):
+    """A bad argument returns its status and leaves every buffer untouched."""
+    L = memq.lib()
+    in_f, out_f = 512, 64
+    x_host = torch.ones((1, in_f)).pin_memory()
+    x_dev = torch.zeros((1, in_f), dtype=torch.float32, device="cuda")
+    wn = torch.ones(in_f, dtype=torch.float32, device="cuda")
+    w = torch.zeros((out_f, in_f // 32 * 34), dtype=torch.uint8, device="cuda")
+    qs = torch.zeros((1, in_f), dtype=torch.int8, device="cuda")
+    d = torch.zeros((1, in_f // 32), dtype=torch.float32, device="cuda")
+    y_dev = torch.zeros((1, out_f), dtype=torch.float32, device="cuda")
+    y_host = torch.zeros((1, out_f)).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    args = [x_host.data_ptr(), x_dev.data_ptr(), wn.data_ptr(), EPS, w.data_ptr(), None,
+            qs.data_ptr(), d.data_ptr(), None, y_dev.data_ptr(), y_host.data_ptr(), out_f, in_f]
+    assert L.memq_decode_step_host(5, *args, 1, s) == memq.Status.ERR_SHAPE
+    assert L.memq_decode_step_host(int(memq.Container.Q8_0), *args, 9, s) == memq.Status.ERR_M_RANGE
+    assert L.memq_decode_step_host(int(memq.Container.E4M3), *args, 1, s) == memq.Status.ERR_NULL
+    torch.cuda.synchronize()
+    assert not x_dev.any() and not y_dev.any() and not y_host.any()
