@@ -3,8 +3,10 @@
 A step is one pass of the whole hot path over one synthetic decode token: the fused
 RMSNorm -> q8_1 producer on the token's activation row, then the GEMV against that q8_1
 activation, reading the next of several rotated weight copies so that no launch finds its
-weights in L2.  The default workload is the Q8_0 4096 x 4096 m = 1 GEMV with 16 rotated copies
-(285 MB, well past the 129 MB L2).
+weights in L2.  The default workload (c3) is the m = 1 GEMV at 17408 x 5120 in all three
+weight containers (E4M3, E4M3 + block-128 grid, Q8_0), interleaved in a rotating order, each
+arm on rotated weight copies totalling more than the 129 MB L2.  --sweep c4 / c5 writes one
+JSONL receipt per cell of the GEMV (container x shape x m) and producer grids.
 
 Printed (rank 0, one JSON line):
   value       whole-step throughput: algorithmic bytes of the step (GEMV weights + scales +
@@ -17,7 +19,9 @@ Printed (rank 0, one JSON line):
   e2e         the same metric through the public API with host buffers, per step one replay of
               a CUDA graph holding those calls (the eager Python loop is reported beside it): the
               activation row is copied host->device from pinned memory, the chain runs, the
-              result y is copied device->host and the host waits for it.
+              result y is copied device->host and the host waits for it.  Single-GEMV
+              workloads add the one-native-call leg (memq_decode_step_host, through the
+              binding and straight through the C ABI).
   cpu_baseline  the f64 oracle on the host cores on a bounded sample of the same workload.
 With --impl reference the oracle itself is the timed arm (rank 0 only).
 """
@@ -497,12 +501,99 @@ def capture(fn, n, stream):
     return g
 
 
+# Sweep grids: C4 (GEMV shapes x m, every container) and C5 (producer rows x widths).
+C4_SHAPES = ((5120, 5120), (1024, 5120), (17408, 5120), (5120, 17408))
+C4_M = (1, 2, 4, 8)
+C5_SHAPES = tuple((ncols, rows) for ncols in (1536, 4096, 8192) for rows in (1, 8, 64, 4096))
+
+
+def run_sweep(args, dev):
+    """One JSONL receipt per cell of the C4 or C5 grid, written to --receipts (first record:
+    the command and the peak), and one summary JSON line on stdout.  C4 cell: the GEMV's
+    back-to-back period over rotated weight copies totalling more than twice the L2 (CUDA graph
+    of 16 launches per copy, CUDA events), its algorithmic bytes, GB/s and fraction of the
+    measured peak.  C5 cell: the producer's period per call (z written), from a CUDA graph over
+    rotated input copies."""
+    import torch
+    peak, peak_kind = measured_peak_hbm()
+    stream = torch.cuda.Stream(device=dev)
+    path = args.receipts or f"{args.sweep}_receipts.jsonl"
+    command = "python bench.py " + " ".join(a for a in sys.argv[1:])
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    cells = 0
+    with open(path, "w") as f:
+        f.write(json.dumps({"sweep": args.sweep, "command": command, "peak_gbs": peak,
+                            "peak_source": peak_kind,
+                            "timing": "CUDA events around graph replays, DRAM-cold (rotated "
+                                      "copies > 2x L2)"}) + "\n")
+        if args.sweep == "c4":
+            for kind in ("blk", "q8_0", "e4m3"):
+                for out_f, in_f in C4_SHAPES:
+                    for m in C4_M:
+                        wbytes = gemv_bytes(kind, out_f, in_f, m)
+                        copies = max(4, -(-2 * L2_BYTES // wbytes))
+                        wl = DecodeStep(kind, out_f, in_f, m, copies, dev, fused=False)
+                        with torch.cuda.stream(stream):
+                            wl.producer()
+                            for i in range(copies):
+                                wl.gemv(i)
+                        stream.synchronize()
+                        per = time_gemv_back_to_back(wl, stream, n=16 * copies)
+                        fault = wl.memq.memq_device_fault(stream)
+                        gbs = wbytes / per / 1e9
+                        f.write(json.dumps({
+                            "container": {"blk": "blk128", "q8_0": "q8_0", "e4m3": "e4m3"}[kind],
+                            "out_f": out_f, "in_f": in_f, "m": m, "copies": copies,
+                            "bytes_per_launch": wbytes, "period_us": round(per * 1e6, 3),
+                            "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+                            "fault": fault}) + "\n")
+                        f.flush()
+                        cells += 1
+                        del wl
+                        torch.cuda.empty_cache()
+        else:
+            for ncols, rows in C5_SHAPES:
+                wl = ProducerStep(ncols, rows, dev)
+                with torch.cuda.stream(stream):
+                    for i in range(wl.copies):
+                        wl.step(i)
+                    n = wl.copies * max(1, -(-64 // wl.copies))
+                    g = capture(wl.step, n, stream)
+                    g.replay()
+                    stream.synchronize()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(4):
+                        g.replay()
+                    b.record(stream)
+                stream.synchronize()
+                per = a.elapsed_time(b) / 1e3 / (4 * n)
+                fault = wl.memq.memq_device_fault(stream)
+                gbs = wl.step_bytes / per / 1e9
+                f.write(json.dumps({"ncols": ncols, "rows": rows, "copies": wl.copies,
+                                    "bytes_per_call": wl.step_bytes,
+                                    "period_us": round(per * 1e6, 3), "gbs": round(gbs, 1),
+                                    "frac_of_measured": round(gbs / peak, 4),
+                                    "fault": fault}) + "\n")
+                f.flush()
+                cells += 1
+                del wl, g
+                torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    print(json.dumps({"sweep": args.sweep, "cells": cells, "receipts": path, "peak_gbs": peak,
+                      "clocks": clocks}), flush=True)
+
+
 def run_ours(args, world, rank, local):
     import torch
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     from quantized_decode_memq_gb300 import build
     build.build()
+    if args.sweep:
+        return run_sweep(args, dev)
     if args.workload.split("_")[0] in ("producer", "silu", "repack") or args.workload.startswith("stack"):
         return run_other(args, world, rank, local, dev)
     if args.workload == "c3":
@@ -1723,6 +1814,11 @@ def main(argv=None):
                     help="MLA workloads: the kernels' split (0 = the library's choice)")
     ap.add_argument("--ncu-launches", type=int, default=0,
                     help="profiling entry: run one producer and N GEMV launches, no timing")
+    ap.add_argument("--sweep", choices=["c4", "c5"], default=None,
+                    help="time every cell of the C4 GEMV grid (3 containers x 4 shapes x m = 1, "
+                         "2, 4, 8) or the C5 producer grid and write one JSONL receipt per cell")
+    ap.add_argument("--receipts", default=None,
+                    help="--sweep output file (default <sweep>_receipts.jsonl)")
     args = ap.parse_args(argv)
     if args.steps is None:
         args.steps = 50 if args.workload == "c3" else 100000
