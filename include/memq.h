@@ -107,7 +107,7 @@ int memq_rmsnorm_q8_1(const float *x, const float *w, float *z, int8_t *qs, floa
  * the call, so a row's outputs are bit-identical whether it is computed alone, in an m-batch,
  * or in a group.
  * Q8_0: the same holds within each of its two paths (dp4a at m = 1; tensor cores from m = 2
- * when each CTA gets 8 to 16 rows of a wide activation, from m = 3 to 6 on other shapes); across
+ * when each CTA gets 8 to 16 rows of a wide activation, from m = 4 to 6 on other shapes); across
  * them the block sums are the same exact integers added in another order, and results agree
  * within the GEMV tolerance.
  */

@@ -68,16 +68,19 @@ constexpr bool is_q80(int kind) { return kind == kQ80 || kind == kQ80T; }
 // activation rows on it is bound by shared-memory bandwidth; the tensor-core path reads it once
 // per 16-row block step but needs 16-row tiles and a larger staged activation.  Measured on
 // GB300 (back-to-back, DRAM-cold): tensor cores win from m = 6 on every shape (17408 x 5120,
-// m = 8: 23 us against 49 us; 5120 x 17408, m = 6: 38 against 47 us) and from m = 3 when the
-// activation is small enough to keep several CTAs per SM and there are many rows (17408 x
-// 5120, m = 3: 23.4 against 25.2 us; m = 4: 22.7 against 30.2 us).  With 5120 rows the
+// m = 8: 23 us against 49 us; 5120 x 17408, m = 6: 38 against 47 us), from m = 5 when the
+// activation is small enough to keep several CTAs per SM (17408 x 5120, m = 5: 20.7 against
+// 34.6 us), and from m = 4 with many rows (17408 x 5120: 19.6 against 20.8 us; 12288 x 5120:
+// 15.3 against 16.0 us).  At m = 3 dp4a on two CTAs per SM is ahead there (17408 x 5120: 17.9
+// against 22.1 us; 12288 x 5120: 14.2 against 15.7 us).  With 5120 rows the tile kernel's
 // tensor-core launch has a floor of ~12.4 us (16-row tiles leave CTAs with one full and one
-// ragged tile), so dp4a stays ahead up to m = 4 there (10.9 against 12.5 us at m = 4); with a
-// 17408-wide activation at m = 3-5, or 1024 rows, dp4a is as fast or faster.
+// ragged tile), so dp4a stays ahead up to m = 4 there (10.9 against 12.5 us at m = 4) unless
+// the K-outer kernel applies (it is tried first); with a 17408-wide activation at m = 3-5, or
+// 1024 rows, dp4a is as fast or faster.
 inline bool q80_on_tensor_cores(int64_t out_f, int64_t in_f, int m) {
     if (m >= 6) return true;
     if (m < kQ80MmaMinM || m * in_f > 40960 || out_f < 2048) return false;
-    return m >= 5 || out_f >= 8192;
+    return m >= 5 || (m >= 4 && out_f >= 8192);
 }
 
 // Q8_0 with dp4a: rows per consumer warp in a tile (q80_pair_row: the two half-warps take two
@@ -1363,13 +1366,16 @@ bool plan_stream(int64_t out_f, int64_t in_f, int m, bool fuse, const DeviceInfo
     //    5120 x 17408: 17.2 against 21.8 us).  CTAs of one launch sharing an SM do not stream at
     //    equal rates, so fewer and larger CTAs shorten the tail -- unless a CTA's rows make only
     //    one full tile and a ragged one, or its staged activation leaves a shallow ring.
-    //  * Q8_0 with dp4a: four, three when the staged activation is large (5120 x 17408: 17.5
-    //    against 19.1 us).
+    //  * Q8_0 with dp4a: two by the same rule (17408 x 5120: 15.5 against 15.9 us with three,
+    //    12288 x 5120: 11.1 against 11.6 us -- each CTA's deeper ring keeps more weight bytes in
+    //    flight per SM), else four, three when the staged activation is large (5120 x 17408:
+    //    17.5 against 19.1 us).
     int pref = G::kMinCtasPerSm;
+    const bool two_tiles = out_f >= static_cast<int64_t>(info.sms) * 2 * 2 * G::kTileRows;
     if (KIND == kE4M3 || KIND == kBlk)
-        pref = out_f >= static_cast<int64_t>(info.sms) * 2 * 2 * G::kTileRows ? 2 : 3;
+        pref = two_tiles ? 2 : 3;
     else if (KIND == kQ80)
-        pref = static_cast<int64_t>(m) * in_f > 8192 ? 3 : 4;
+        pref = two_tiles ? 2 : static_cast<int64_t>(m) * in_f > 8192 ? 3 : 4;
     const int k_rows = static_cast<int>(std::min<int64_t>(
         pref, std::max<int64_t>(1, out_f / (static_cast<int64_t>(info.sms) * kMinRowsPerCta))));
     int ctas = k_rows;
