@@ -198,3 +198,24 @@ def test_decode_step_host_rejects_before_copying(memq):
     assert L.memq_decode_step_host(int(memq.Container.E4M3), *args, 1, s) == memq.Status.ERR_NULL
     torch.cuda.synchronize()
     assert not x_dev.any() and not y_dev.any() and not y_host.any()
+
+
+def test_decode_step_host_out_f_zero(memq, oracle):
+    """out_f == 0: the call copies x in, produces the q8_1 activation (as the producer alone
+    would) and waits; w and y_host may be NULL."""
+    L = memq.lib()
+    in_f, m = 1024, 2
+    x, wn = synth.activation_rows(in_f, m)
+    x_host = torch.from_numpy(x.copy()).pin_memory()
+    x_dev = torch.zeros((m, in_f), dtype=torch.float32, device="cuda")
+    wnd = to_dev(wn)
+    qs = torch.zeros((m, in_f), dtype=torch.int8, device="cuda")
+    d = torch.zeros((m, in_f // 32), dtype=torch.float32, device="cuda")
+    z = torch.zeros((m, in_f), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = L.memq_decode_step_host(int(memq.Container.Q8_0), x_host.data_ptr(), x_dev.data_ptr(),
+                                 wnd.data_ptr(), EPS, None, None, qs.data_ptr(), d.data_ptr(),
+                                 z.data_ptr(), None, None, 0, in_f, m, s)
+    assert rc == 0
+    assert torch.equal(x_dev.cpu(), x_host)
+    check_producer(oracle, x, wn, EPS, z, qs, d)
