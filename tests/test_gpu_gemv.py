@@ -322,3 +322,21 @@ def test_graph_back_to_back_launches(memq, oracle, kind, m):
     for i, (w, aux) in enumerate(ws):
         y_ref, s_ref = ref_gemv(oracle, kind, w, aux, qs, d, in_f, rows=rows)
         check_gemv(ys[i], y_ref, s_ref, rows=rows)
+
+
+@pytest.mark.parametrize("out_f", [17408, 12288])
+def test_q8_0_dp4a_two_ctas_m3(memq, oracle, out_f):
+    """Q8_0 at m = 3 on >= 9728 rows runs dp4a on two CTAs per SM (the tensor cores take over
+    from m = 4 there): sampled rows within the GEMV tolerance of the oracle, and each row of the
+    m = 3 call equal bit for bit to the m = 1 call on that activation row (dp4a at both m; its
+    per-(row, token) arithmetic does not depend on m)."""
+    in_f, m = 5120, 3
+    w, aux = weights("q8_0", out_f, in_f, 31)
+    qs, d = act(oracle, m, in_f, 91)
+    y3 = gpu_gemv(memq, "q8_0", w, aux, qs, d)
+    rows = sample_rows(out_f, 96, seed=out_f)
+    y_ref, s_ref = ref_gemv(oracle, "q8_0", w, aux, qs, d, in_f, rows=rows)
+    check_gemv(y3, y_ref, s_ref, rows=rows)
+    for j in range(m):
+        y1 = gpu_gemv(memq, "q8_0", w, aux, qs[j:j + 1], d[j:j + 1])
+        assert torch.equal(y3[j].view(torch.int32), y1[0].view(torch.int32)), j
