@@ -482,6 +482,13 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
 constexpr int kKoCtasPerSm = 3;
 constexpr int kKoTiles = 1;
 constexpr int64_t kKoMinAct = 16384;
+// Q8_0 from m = 3: K-outer from 15360 activation bytes, i.e. also 3 x 5120 (5120 x 5120 m = 3:
+// 8.5 us against 9.2 us for dp4a); at m = 2 the general threshold stays (5120 x 5120 m = 2: 7.9
+// against 7.8 us, 4096 x 4096: 6.6 against 5.2).
+constexpr int64_t kKoMinActQ80M3 = 15360;
+inline int64_t ko_min_act(int kind, int m) {
+    return kind == kQ80T && m >= 3 ? kKoMinActQ80M3 : kKoMinAct;
+}
 std::atomic<uint64_t> g_ko_attr[3][kMaxDevices];  // [E4M3, block-128, Q8_0]: bit per m set
 
 // Encodes (or finds in the cache) a 2-D tensor map over `base` viewed as [rows][cols] elements
@@ -531,10 +538,11 @@ inline int64_t ko_rmax(int nmat, const int64_t *out_f, const DeviceInfo &info) {
 // and CTA-size conditions of launch_kouter.  The Q8_0 entry points decide their path (tensor
 // cores or dp4a) with it before launching.  Measured on GB300 (back-to-back, us, K-outer against
 // dp4a): 5120 x 17408 m = 2 22.1 / 23.4, m = 4 22.2 / 35.9, m = 8 22.1 / 62.2; 5120 x 5120
-// m = 4 8.9 / 10.9, m = 8 8.0 / 19.9; at m = 1 dp4a (15.8 us at 5120 x 17408).
+// m = 3 8.5 / 9.2, m = 4 8.9 / 10.9, m = 8 8.0 / 19.9; at m = 1 dp4a (15.8 us at 5120 x 17408).
 inline bool q80_kouter_applies(int nmat, const int64_t *out_f, int64_t in_f, int m,
                                const int8_t *qs, const float *d, const DeviceInfo &info) {
-    if (m < 2 || in_f % 128 != 0 || !aligned(qs, 16) || !aligned(d, 16) || m * in_f < kKoMinAct)
+    if (m < 2 || in_f % 128 != 0 || !aligned(qs, 16) || !aligned(d, 16) ||
+        m * in_f < ko_min_act(kQ80T, m))
         return false;
     const int64_t r = ko_rmax(nmat, out_f, info);
     return r >= 8 && r <= 16 * kKoTiles;
@@ -554,7 +562,7 @@ cudaError_t launch_kouter(int nmat, const uint8_t *const *w, const float *const 
     using KG = KoGeo<KIND>;
     constexpr int TILES = kKoTiles;
     constexpr int kPassRows = 16 * TILES;
-    if (in_f % 128 != 0 || !aligned(d, 16) || !aligned(qs, 16) || M * in_f < kKoMinAct)
+    if (in_f % 128 != 0 || !aligned(d, 16) || !aligned(qs, 16) || M * in_f < ko_min_act(KIND, M))
         return cudaErrorNotSupported;
     KoArgs a = {};
     a.nmat = nmat;
