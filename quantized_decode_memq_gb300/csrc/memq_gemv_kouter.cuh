@@ -482,12 +482,14 @@ __global__ void __launch_bounds__(kThreads, TILES == 1 ? 3 : 2)
 constexpr int kKoCtasPerSm = 3;
 constexpr int kKoTiles = 1;
 constexpr int64_t kKoMinAct = 16384;
-// Q8_0 from m = 3: K-outer from 15360 activation bytes, i.e. also 3 x 5120 (5120 x 5120 m = 3:
-// 8.5 us against 9.2 us for dp4a); at m = 2 the general threshold stays (5120 x 5120 m = 2: 7.9
-// against 7.8 us, 4096 x 4096: 6.6 against 5.2).
-constexpr int64_t kKoMinActQ80M3 = 15360;
+// From m = 3: K-outer from 15360 activation bytes, i.e. also 3 x 5120 (5120 x 5120 m = 3,
+// K-outer against the tile kernel: E4M3 7.1 / 7.4 us, block-128 7.15 / 7.2 us, Q8_0 8.5 us
+// against 9.2 us for dp4a); at m = 2 the general threshold stays (Q8_0 5120 x 5120: 7.9 against
+// 7.8 us, 4096 x 4096: 6.6 against 5.2).
+constexpr int64_t kKoMinActM3 = 15360;
 inline int64_t ko_min_act(int kind, int m) {
-    return kind == kQ80T && m >= 3 ? kKoMinActQ80M3 : kKoMinAct;
+    (void)kind;
+    return m >= 3 ? kKoMinActM3 : kKoMinAct;
 }
 std::atomic<uint64_t> g_ko_attr[3][kMaxDevices];  // [E4M3, block-128, Q8_0]: bit per m set
 
